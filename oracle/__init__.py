@@ -1,0 +1,313 @@
+"""CPU oracle for the routed-expert MoE forward (test infrastructure).
+
+Only the test suite, the smoke check and the benchmark's CPU-baseline leg may
+import this package.  The CUDA library and its Python binding never import
+it; the product path fails loudly when the CUDA library is missing instead of
+falling back to anything here.
+
+The arithmetic lives in ``moe_oracle.c`` (plain loops, built with gcc on
+first use).  This module marshals numpy arrays and composes the stages in the
+order of mslk/moe/layers.py, MetaShufflingMoE._route -> _routed_expert ->
+_combine_outputs:
+
+    route -> gather*score (bf16, or e4m3 + per-row scale)
+          -> grouped GEMM with w13 -> silu_mul (or silu_mul_quant)
+          -> grouped GEMM with w2  -> scatter-add into the output.
+
+bf16 values travel as ``numpy.uint16`` bit patterns, e4m3 as ``numpy.uint8``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from pathlib import Path
+
+import numpy as np
+
+_HERE = Path(__file__).resolve().parent
+_SRC = _HERE / "moe_oracle.c"
+_LIB = _HERE / "liboracle.so"
+_lock = threading.Lock()
+_lib = None
+
+BF16, F32 = 0, 1
+
+
+def build(force: bool = False) -> Path:
+    """Compile moe_oracle.c into liboracle.so (OpenMP when the compiler has it)."""
+    if not force and _LIB.exists() and _LIB.stat().st_mtime >= _SRC.stat().st_mtime:
+        return _LIB
+    tmp = _LIB.with_suffix(f".{os.getpid()}.tmp")
+    base = ["gcc", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-std=c11", str(_SRC), "-o", str(tmp)]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:] + ["-lm"], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base + ["-lm"], check=True, capture_output=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        try:
+            lib = ctypes.CDLL(str(build()))
+        except OSError:
+            lib = ctypes.CDLL(str(build(force=True)))
+        P, I, L = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        sig = {
+            "oracle_num_threads": ([], I),
+            "oracle_bf16_round": ([P, P, L], None),
+            "oracle_bf16_to_f32": ([P, P, L], None),
+            "oracle_e4m3_encode": ([P, P, L], None),
+            "oracle_e4m3_decode": ([P, P, L], None),
+            "oracle_quantize_rows": ([P, L, L, P, P, P], None),
+            "oracle_route": ([P, I, L, L, I, I, I, I, P, P, P, P, P], I),
+            "oracle_gather_scale": ([P, I, P, P, I, P, I, L, L, P], None),
+            "oracle_gather_scale_quant": ([P, I, P, P, I, P, I, L, L, P, P, P], None),
+            "oracle_grouped_gemm_bf16": ([P, P, P, I, I, I, P], None),
+            "oracle_grouped_gemm_fp8": ([P, P, P, P, P, I, I, I, P], None),
+            "oracle_silu_mul": ([P, P, L, I, I, P], None),
+            "oracle_silu_mul_quant": ([P, P, L, I, I, P, P, P], None),
+            "oracle_scatter_add": ([P, I, I, P, P, I], None),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes, fn.restype = args, res
+        _lib = lib
+        return lib
+
+
+def _p(a):
+    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
+
+
+# ------------------------------------------------------------ number formats
+
+def bf16_round(v) -> np.ndarray:
+    v = _c(v, np.float32)
+    out = np.empty(v.shape, np.uint16)
+    _load().oracle_bf16_round(_p(v), _p(out), v.size)
+    return out
+
+
+def bf16_to_f32(b) -> np.ndarray:
+    b = _c(b, np.uint16)
+    out = np.empty(b.shape, np.float32)
+    _load().oracle_bf16_to_f32(_p(b), _p(out), b.size)
+    return out
+
+
+def e4m3_encode(v) -> np.ndarray:
+    v = _c(v, np.float32)
+    out = np.empty(v.shape, np.uint8)
+    _load().oracle_e4m3_encode(_p(v), _p(out), v.size)
+    return out
+
+
+def e4m3_decode(b) -> np.ndarray:
+    b = _c(b, np.uint8)
+    out = np.empty(b.shape, np.float32)
+    _load().oracle_e4m3_decode(_p(b), _p(out), b.size)
+    return out
+
+
+def quantize_rows(w, scale_ub: float | None = None):
+    """Per-row FP8 quantisation over the last axis: (codes uint8, scales f32)."""
+    w = _c(w, np.float32)
+    cols = w.shape[-1]
+    rows = w.size // cols if cols else 0
+    q = np.empty(w.shape, np.uint8)
+    s = np.empty(w.shape[:-1], np.float32)
+    ub = None if scale_ub is None else np.array([scale_ub], np.float32)
+    _load().oracle_quantize_rows(_p(w), rows, cols, _p(ub), _p(q), _p(s))
+    return q, s
+
+
+# -------------------------------------------------------------------- stages
+
+def _scores_args(scores):
+    if scores.dtype == np.uint16:
+        dtype = BF16
+    elif scores.dtype == np.float32:
+        dtype = F32
+    else:
+        raise TypeError("scores must be bf16 bits (uint16) or float32")
+    st, se = (s // scores.itemsize for s in scores.strides)
+    return dtype, st, se
+
+
+def route(scores, top_k: int, valid_tokens: int | None = None):
+    """Top-k routing; returns dict(counts[E+1], offsets[E+1], expert_indices,
+    token_indices, inv[Tv, k]) with the index arrays cut to Tv * k rows."""
+    T, E = scores.shape
+    Tv = T if valid_tokens is None else int(valid_tokens)
+    dtype, st, se = _scores_args(scores)
+    a = Tv * top_k
+    counts = np.zeros(E + 1, np.int32)
+    offsets = np.zeros(E + 1, np.int32)
+    ei = np.full(max(a, 1), -1, np.int32)
+    ti = np.full(max(a, 1), -1, np.int32)
+    inv = np.full(max(a, 1), -1, np.int32)
+    rc = _load().oracle_route(_p(scores), dtype, st, se, T, E, top_k, Tv, _p(counts), _p(offsets),
+                              _p(ei), _p(ti), _p(inv))
+    if rc != 0:
+        raise ValueError("oracle_route: top_k outside [1, E] or valid tokens outside [0, T]")
+    return dict(counts=counts, offsets=offsets, expert_indices=ei[:a], token_indices=ti[:a],
+                inv=inv[:a].reshape(Tv, top_k))
+
+
+def gather_scale(x, token_indices, expert_indices, scores, valid_rows: int | None = None):
+    x = _c(x, np.uint16)
+    a = len(token_indices)
+    v = a if valid_rows is None else int(valid_rows)
+    ti, ei = _c(token_indices, np.int32), _c(expert_indices, np.int32)
+    dtype, st, se = _scores_args(scores)
+    out = np.zeros((a, x.shape[1]), np.uint16)
+    _load().oracle_gather_scale(_p(x), x.shape[1], _p(ti), _p(ei), v, _p(scores), dtype, st, se, _p(out))
+    return out
+
+
+def gather_scale_quant(x, token_indices, expert_indices, scores, scale_ub: float | None = None,
+                       valid_rows: int | None = None):
+    x = _c(x, np.uint16)
+    a = len(token_indices)
+    v = a if valid_rows is None else int(valid_rows)
+    ti, ei = _c(token_indices, np.int32), _c(expert_indices, np.int32)
+    dtype, st, se = _scores_args(scores)
+    ub = None if scale_ub is None else np.array([scale_ub], np.float32)
+    out = np.zeros((a, x.shape[1]), np.uint8)
+    scale = np.zeros(a, np.float32)
+    _load().oracle_gather_scale_quant(_p(x), x.shape[1], _p(ti), _p(ei), v, _p(scores), dtype, st, se,
+                                      _p(ub), _p(out), _p(scale))
+    return out, scale
+
+
+def grouped_gemm_bf16(x, w, counts):
+    """x[a, K] bf16 bits, w[E, N, K] bf16 bits, counts[E] -> y[a, N] bf16 bits."""
+    x, w = _c(x, np.uint16), _c(w, np.uint16)
+    E, N, K = w.shape
+    counts = _c(counts[:E], np.int32)
+    y = np.zeros((x.shape[0], N), np.uint16)
+    _load().oracle_grouped_gemm_bf16(_p(x), _p(w), _p(counts), E, N, K, _p(y))
+    return y
+
+
+def grouped_gemm_fp8(xq, wq, counts, x_scale, w_scale):
+    """xq[a, K] e4m3, wq[E, N, K] e4m3, x_scale[a], w_scale[E, N] -> y[a, N] bf16 bits."""
+    xq, wq = _c(xq, np.uint8), _c(wq, np.uint8)
+    E, N, K = wq.shape
+    counts = _c(counts[:E], np.int32)
+    xs, ws = _c(x_scale, np.float32), _c(w_scale, np.float32)
+    y = np.zeros((xq.shape[0], N), np.uint16)
+    _load().oracle_grouped_gemm_fp8(_p(xq), _p(wq), _p(counts), _p(xs), _p(ws), E, N, K, _p(y))
+    return y
+
+
+def silu_mul(y, H: int, valid_rows: int | None = None):
+    """y[a, 2H] bf16 bits -> z[a, H] = silu(y[:, :H]) * y[:, H:] (bf16 bits)."""
+    y = _c(y, np.uint16)
+    a = y.shape[0]
+    v = a if valid_rows is None else int(valid_rows)
+    z = np.zeros((a, H), np.uint16)
+    _load().oracle_silu_mul(_p(y), ctypes.c_void_p(y.ctypes.data + 2 * H), y.shape[1], v, H, _p(z))
+    return z
+
+
+def silu_mul_quant(y, H: int, scale_ub: float | None = None, valid_rows: int | None = None):
+    y = _c(y, np.uint16)
+    a = y.shape[0]
+    v = a if valid_rows is None else int(valid_rows)
+    ub = None if scale_ub is None else np.array([scale_ub], np.float32)
+    z = np.zeros((a, H), np.uint8)
+    zs = np.zeros(a, np.float32)
+    _load().oracle_silu_mul_quant(_p(y), ctypes.c_void_p(y.ctypes.data + 2 * H), y.shape[1], v, H,
+                                  _p(ub), _p(z), _p(zs))
+    return z, zs
+
+
+def scatter_add(out, rows, token_indices, valid_rows: int | None = None):
+    """out[T, D] bf16 bits (updated in place and returned), rows[a, D] bf16 bits."""
+    assert out.dtype == np.uint16 and out.flags.c_contiguous
+    rows = _c(rows, np.uint16)
+    ti = _c(token_indices, np.int32)
+    v = len(ti) if valid_rows is None else int(valid_rows)
+    _load().oracle_scatter_add(_p(out), out.shape[0], out.shape[1], _p(rows), _p(ti), v)
+    return out
+
+
+# ------------------------------------------------------------------- forward
+
+def moe_forward(x, scores, top_k: int, weights, *, fp8: bool, valid_tokens: int | None = None,
+                out_init=None, scale_ub: float | None = None, H: int | None = None):
+    """The routed-expert forward of MetaShufflingMoE._no_comm_forward (one GPU,
+    no shared expert), on the CPU.
+
+    x[T, D] bf16 bits; scores[T, E] bf16 bits or f32.  ``weights(ids)`` returns
+    the weights of the experts ``ids`` (ascending) as (w13[n, 2H, D],
+    w2[n, D, H]): bf16 bits, or fp32 when ``fp8`` (quantised per row here).
+    out_init[T, D] (bf16 bits) is the tensor the routed rows are added into
+    (zeros when None).  Returns the final output and every intermediate.
+    """
+    T, D = x.shape
+    E = scores.shape[1]
+    r = route(scores, top_k, valid_tokens)
+    a = int(r["counts"][E])
+    counts = r["counts"][:E]
+    used = [e for e in range(E) if counts[e] > 0]
+    cu = counts[used] if used else np.zeros(0, np.int32)
+    res = dict(route=r, used_experts=used)
+    out = np.zeros((T, D), np.uint16) if out_init is None else np.array(out_init, np.uint16, copy=True)
+    if a == 0:
+        res["out"] = out
+        return res
+    w13, w2 = weights(used)
+    Hd = w2.shape[2] if H is None else H
+    if not fp8:
+        xg = gather_scale(x, r["token_indices"], r["expert_indices"], scores)
+        y = grouped_gemm_bf16(xg, w13, cu)
+        z = silu_mul(y, Hd)
+        o = grouped_gemm_bf16(z, w2, cu)
+        res.update(x_routed=xg, y=y, z=z, o=o)
+    else:
+        w13q, w13s = quantize_rows(w13)
+        w2q, w2s = quantize_rows(w2)
+        xq, xs = gather_scale_quant(x, r["token_indices"], r["expert_indices"], scores, scale_ub)
+        y = grouped_gemm_fp8(xq, w13q, cu, xs, w13s)
+        zq, zs = silu_mul_quant(y, Hd, scale_ub)
+        o = grouped_gemm_fp8(zq, w2q, cu, zs, w2s)
+        res.update(x_routed=xq, x_scale=xs, y=y, z=zq, z_scale=zs, o=o,
+                   w13q=w13q, w13s=w13s, w2q=w2q, w2s=w2s)
+    scatter_add(out, o, r["token_indices"])
+    res["out"] = out
+    return res
+
+
+def moe_forward_tokens(tokens, x, scores, top_k: int, weights, *, fp8: bool, out_init=None,
+                       scale_ub: float | None = None):
+    """The forward's output rows for a sample of tokens only.
+
+    Every stage of the forward works row by row (routing per token, gather and
+    quantisation per routed row, GEMMs per row, the combine per token in
+    ascending expert order), so running it on the sampled tokens alone gives
+    exactly those tokens' rows of the full forward.  ``tokens`` must be valid
+    token ids.  Returns (out[len(tokens), D], the sub-forward's dict).
+    """
+    tokens = np.asarray(tokens, np.int64)
+    xs = np.ascontiguousarray(x[tokens])
+    ss = np.ascontiguousarray(scores[tokens])
+    oi = None if out_init is None else np.ascontiguousarray(out_init[tokens])
+    res = moe_forward(xs, ss, top_k, weights, fp8=fp8, out_init=oi, scale_ub=scale_ub)
+    return res["out"], res

@@ -1,0 +1,37 @@
+"""Small conversions shared by the tests (no arithmetic of the forward here)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """A CPU numpy view of a tensor's bits: bf16 -> uint16, e4m3 -> uint8, others as is."""
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.float8_e4m3fn:
+        return t.view(torch.uint8).numpy()
+    return t.numpy()
+
+
+def bf16_from_bits(b: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(b, np.uint16).view(np.int16)).view(torch.bfloat16)
+
+
+def e4m3_from_bits(b: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(b, np.uint8)).view(torch.float8_e4m3fn)
+
+
+def f64(b: np.ndarray) -> np.ndarray:
+    """bf16 bits -> float64 values (exact)."""
+    return bf16_from_bits(b).double().numpy()
+
+
+def rms(a: np.ndarray) -> float:
+    a = np.asarray(a, np.float64)
+    return float(np.sqrt(np.mean(a * a))) if a.size else 0.0
+
+
+def parse_golden(path) -> list[str]:
+    return [ln.split("#", 1)[0].strip() for ln in open(path) if ln.split("#", 1)[0].strip()]
