@@ -1,0 +1,240 @@
+/*
+ * moe.h — C ABI of the GB300 (sm_103a) routed-expert MoE forward.
+ *
+ * One shared library, libmoe_gb300.so, of hand-written CUDA kernels.  The
+ * entry points are the stages of the single-GPU forward of
+ * mslk/moe/layers.py, MetaShufflingMoE._no_comm_forward:
+ *
+ *   moe_route                 top-k routing into per-expert counts and a
+ *                             by-expert token permutation (index_shuffling)
+ *   moe_gather_scale          gather token rows and multiply by the score
+ *   moe_gather_scale_quant    ... and quantise each row to FP8 (e4m3)
+ *   moe_grouped_gemm          per-expert GEMM with w13 or w2 (bf16)
+ *   moe_grouped_gemm_fp8_rowwise   the same on e4m3 operands with row scales
+ *   moe_silu_mul(_quant)      z = silu(y0) * y1 (and FP8 quantisation)
+ *   moe_scatter_add           add routed rows back into token order
+ *   moe_quantize_rows         per-row FP8 quantisation of a weight matrix
+ *
+ * Conventions (every entry point):
+ *  - Pointers are DEVICE pointers unless stated; the caller owns all memory.
+ *    No entry point allocates device memory; scratch comes from the caller
+ *    (moe_route's workspace).
+ *  - Matrices are row-major and contiguous unless a stride is given.
+ *    bf16 = IEEE binary32 upper half; e4m3 = OCP FP8 E4M3 ("fn": no
+ *    infinities, largest finite 448).
+ *  - Every call is asynchronous on `stream` and never synchronises with the
+ *    host.  Counts that the GPU computes (valid rows, per-expert counts) are
+ *    read on the device.
+ *  - Return value: MOE_OK, or a negative MOE_ERR_* code.  Argument errors are
+ *    detected on the host before anything is launched.  Errors the GPU finds
+ *    (an index out of range, a device count larger than its buffer, a wait
+ *    that timed out) never fault: the kernel skips the offending work and
+ *    records a MOE_DEVERR_* bit, read back with moe_device_error().
+ *  - Identical inputs give identical output bytes (no atomics on data).
+ *  - Alignment: every matrix base pointer is 16-byte aligned; D, H, N and K
+ *    are multiples of 16.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define MOE_OK 0
+#define MOE_ERR_INVALID (-1)     /* null required pointer, bad size, top_k outside [1, E] ... */
+#define MOE_ERR_UNSUPPORTED (-2) /* alignment, a dimension not a multiple of 16, E > 1024 ... */
+#define MOE_ERR_CUDA (-3)        /* a CUDA call failed: moe_last_cuda_error() has the code */
+#define MOE_ERR_WORKSPACE (-4)   /* the workspace is smaller than moe_route_workspace_size() */
+
+/* Element types. */
+#define MOE_DTYPE_BF16 0
+#define MOE_DTYPE_F32 1
+#define MOE_DTYPE_E4M3 2
+
+/* Grouped-GEMM epilogues. */
+#define MOE_EPILOGUE_NONE 0     /* y[r, n] = (x_r . w_e[n]) (times the two scales for FP8), bf16 */
+#define MOE_EPILOGUE_SILU_MUL 1 /* with N = 2H: y[r, j] = silu(v_j) * v_{H+j}, j < H, bf16 */
+
+/* Device-side error bits (moe_device_error). */
+#define MOE_DEVERR_BAD_INDEX 0x1   /* a token or expert index outside its range was skipped */
+#define MOE_DEVERR_BAD_COUNT 0x2   /* a device count exceeded its buffer and was clamped */
+#define MOE_DEVERR_TIMEOUT 0x4     /* a bounded pipeline wait gave up; the tile was abandoned */
+
+/* Text for a status code (static storage). */
+const char* moe_status_string(int status);
+
+/* The cudaError_t of the last MOE_ERR_CUDA returned on this host thread. */
+int moe_last_cuda_error(void);
+
+/*
+ * Read and clear the device-side error word of the current device.
+ * Synchronises `stream`.  *bits receives an OR of MOE_DEVERR_* (0 = none).
+ */
+int moe_device_error(unsigned int* bits, cudaStream_t stream);
+
+/* ------------------------------------------------------------------ routing */
+
+/*
+ * Bytes of device workspace moe_route needs for T token rows, E experts and
+ * top_k (host call, no GPU use).
+ */
+int moe_route_workspace_size(int T, int E, int top_k, size_t* bytes);
+
+/*
+ * Top-k routing and the by-expert permutation: index_shuffling(scores) of
+ * mslk/moe/layers.py (MetaShufflingMoE._route); the selection is torch.topk
+ * as in BaselineMoE._forward.
+ *
+ * scores        [T, E] router scores, element (t, e) at
+ *               scores + t * stride_t + e * stride_e (elements), dtype
+ *               MOE_DTYPE_BF16 or MOE_DTYPE_F32.  NaN scores are undefined.
+ * num_valid_tokens  device int32: tokens t < *num_valid_tokens are routed
+ *               (NULL: all T).  A value outside [0, T] is clamped and flagged.
+ * For each valid token the top_k experts with the largest scores are chosen,
+ * equal scores (+0 == -0) going to the lower expert index.  The Tv * top_k
+ * (token, expert) pairs are then numbered as routed rows in ascending expert
+ * order and, within an expert, ascending token order.  Outputs (device int32):
+ *   counts[E + 1]          rows per expert; counts[E] = Tv * top_k (the total,
+ *                          which the pages slice off with token_counts[:E])
+ *   expert_offsets[E + 1]  exclusive prefix sum of counts; [E] = Tv * top_k
+ *   expert_indices[T * top_k], token_indices[T * top_k]
+ *                          the pair of each routed row; entries at and past
+ *                          Tv * top_k are not written
+ *   inv_rows[T * top_k]    (nullable) inv_rows[t * top_k + j] = the j-th
+ *                          smallest routed row of token t, for t < Tv
+ * ws, ws_bytes  device workspace of at least moe_route_workspace_size bytes,
+ *               256-byte aligned; its contents on entry do not matter.
+ * Requires 1 <= top_k <= E <= 1024 and T >= 0.  The result is deterministic.
+ */
+int moe_route(const void* scores, int scores_dtype, int64_t stride_t, int64_t stride_e, int T, int E,
+              int top_k, const int32_t* num_valid_tokens, int32_t* counts, int32_t* expert_offsets,
+              int32_t* expert_indices, int32_t* token_indices, int32_t* inv_rows, void* ws,
+              size_t ws_bytes, cudaStream_t stream);
+
+/* --------------------------------------------------------- gather + scale */
+
+/*
+ * gather_scale_dense_tokens (mslk/moe/gather_scatter.py,
+ * _mslk_gather_scale_dense_tokens): for routed rows i < valid,
+ *   out[i, :] = bf16( f32(x[t, :]) * f32(scores[t, e]) ),
+ *   t = token_indices[i], e = expert_indices[i].
+ * x [T, D] bf16; token_indices, expert_indices [a] int32; scores as in
+ * moe_route (E experts); valid_token_count: device int32 count of ROUTED ROWS
+ * (NULL: a), e.g. &counts[E] from moe_route.  Rows i >= valid are not written.
+ * out [a, D] bf16.  a == 0 or D == 0 is a no-op.
+ */
+int moe_gather_scale(const void* x, int T, int D, const int32_t* token_indices,
+                     const int32_t* expert_indices, int a, const void* scores, int scores_dtype,
+                     int64_t stride_t, int64_t stride_e, int E, const int32_t* valid_token_count,
+                     void* out, cudaStream_t stream);
+
+/*
+ * gather_scale_quant_dense_tokens (mslk/moe/gather_scatter.py,
+ * _mslk_gather_scale_fp8_rowwise_quant_dense_tokens): the fp32 row
+ * v = x[t, :] * scores[t, e] is quantised to e4m3 with one fp32 scale:
+ *   m = max |v|, then m = min(max(m, 1e-12), *scale_ub) when scale_ub is
+ *   given (device fp32, nullable), else max(m, 1e-12);
+ *   s = 448 / m;  out_scale[i] = 1 / s;
+ *   out[i, j] = e4m3( clamp(v_j * s, -448, 448) ), round to nearest even.
+ * All arithmetic is IEEE fp32 (correctly rounded division and reciprocal).
+ * out [a, D] e4m3, out_scale [a] fp32.  Rows i >= valid are not written.
+ */
+int moe_gather_scale_quant(const void* x, int T, int D, const int32_t* token_indices,
+                           const int32_t* expert_indices, int a, const void* scores,
+                           int scores_dtype, int64_t stride_t, int64_t stride_e, int E,
+                           const int32_t* valid_token_count, const float* scale_ub, void* out,
+                           float* out_scale, cudaStream_t stream);
+
+/*
+ * Per-row FP8 quantisation of an fp32 matrix w [rows, cols] with the rule of
+ * moe_gather_scale_quant (score 1), for FP8-rowwise expert weights (the
+ * per-row weight scales of mslk/moe/layers.py, RoutedExperts.build).
+ * q [rows, cols] e4m3, scale [rows] fp32; scale_ub nullable.
+ */
+int moe_quantize_rows(const float* w, int64_t rows, int cols, const float* scale_ub, void* q,
+                      float* scale, cudaStream_t stream);
+
+/* ----------------------------------------------------------- grouped GEMM */
+
+/*
+ * grouped_gemm(x, w.view(-1, K), token_counts) of mslk/moe/layers.py
+ * (MetaShufflingMoE._routed_expert).  Expert e owns the rows
+ * [off_e, off_e + counts[e]) of x, off_e = counts[0] + ... + counts[e-1], and
+ *   v[r, n] = sum_k x[r, k] * w[e, n, k]     (fp32 accumulation)
+ * epilogue MOE_EPILOGUE_NONE:     y [a_max, N] bf16, y[r, n] = bf16(v[r, n])
+ * epilogue MOE_EPILOGUE_SILU_MUL: N = 2H (the w13 layout of
+ *   RoutedExperts.build: rows [0, H) are the SiLU input, [H, 2H) the gate);
+ *   y [a_max, H] bf16, y[r, j] = bf16(silu(y0) * y1) with y0 = bf16(v[r, j])
+ *   and y1 = bf16(v[r, H + j]), i.e. moe_silu_mul of the unfused output.
+ * x [a_max, K] bf16; w [E, N, K] bf16; counts [E] device int32 (the sum is
+ * the number of routed rows; rows past it are not written).  Runs on the
+ * tensor cores (tcgen05, accumulators in tensor memory, TMA-fed).
+ * Requires N, K multiples of 16 (H a multiple of 16 for SILU_MUL), E <= 1024.
+ */
+int moe_grouped_gemm(const void* x, const void* w, const int32_t* counts, int E, int a_max, int N,
+                     int K, void* y, int epilogue, cudaStream_t stream);
+
+/*
+ * grouped_gemm_fp8_rowwise(x, w, counts, x_scale, w_scale) of
+ * mslk/moe/layers.py: as moe_grouped_gemm on e4m3 operands, with
+ *   v[r, n] = (sum_k x[r, k] * w[e, n, k]) * x_scale[r] * w_scale[e * N + n]
+ * (fp32; the dequantisation order of BaselineMoE._fake_quant).
+ * x [a_max, K] e4m3, w [E, N, K] e4m3, x_scale [a_max] fp32, w_scale [E * N]
+ * fp32.  Epilogues as in moe_grouped_gemm.
+ */
+int moe_grouped_gemm_fp8_rowwise(const void* x, const void* w, const int32_t* counts,
+                                 const float* x_scale, const float* w_scale, int E, int a_max,
+                                 int N, int K, void* y, int epilogue, cudaStream_t stream);
+
+/* ---------------------------------------------------------------- silu_mul */
+
+/*
+ * silu_mul(x0, x1) (MetaShufflingMoE._fused_silu_mul): for rows r < valid,
+ *   z[r, j] = bf16( y0 * sigmoid(y0) * y1 ),  y0 = x0[r * ld + j],
+ *   y1 = x1[r * ld + j], in fp32 (sigmoid(a) = 1 / (1 + exp(-a))).
+ * x0, x1 bf16 with row stride ld elements (ld = 2H for the halves of a
+ * [a, 2H] GEMM output); z [a, H] bf16; valid_rows: device int32 routed-row
+ * count (nullable: a).  Rows r >= valid are not written.
+ */
+int moe_silu_mul(const void* x0, const void* x1, int64_t ld, int a, int H,
+                 const int32_t* valid_rows, void* z, cudaStream_t stream);
+
+/*
+ * silu_mul_quant(x0, x1, scale_ub): the fp32 row of z is quantised over its H
+ * entries with the rule of moe_gather_scale_quant.  z [a, H] e4m3,
+ * z_scale [a] fp32.
+ */
+int moe_silu_mul_quant(const void* x0, const void* x1, int64_t ld, int a, int H,
+                       const int32_t* valid_rows, const float* scale_ub, void* z, float* z_scale,
+                       cudaStream_t stream);
+
+/* ------------------------------------------------------------- scatter-add */
+
+/*
+ * scatter_add_dense_tokens (mslk/moe/gather_scatter.py,
+ * _mslk_scatter_add_dense_tokens), made deterministic: every routed row
+ * r < valid is added into out[token_indices[r], :].  Each output token is
+ * owned by one warp: acc = f32(out[t, :]); acc += f32(in[r, :]) for t's rows
+ * in ascending r; out[t, :] = bf16(acc).  No atomics.
+ * out [T, D] bf16 (read and written); in [a, D] bf16; token_indices [a].
+ * inv_rows [Tv * top_k] from moe_route (t's rows, ascending) is required when
+ * top_k > 1; with top_k == 1 it may be NULL (row r then owns its token).
+ * valid_token_count: device int32 routed-row count (NULL: a); with inv_rows
+ * it must equal Tv * top_k.  Tokens that receive no row are not written.
+ */
+int moe_scatter_add(void* out, const void* in, const int32_t* token_indices,
+                    const int32_t* inv_rows, int top_k, int a, int T, int D,
+                    const int32_t* valid_token_count, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,272 @@
+"""ctypes binding of libmoe_gb300 (include/moe.h), with the same entry-point names.
+
+Argument marshalling only: tensors become device pointers and sizes, the
+current PyTorch stream becomes the cudaStream_t, and a non-zero status raises
+MoEError.  Output tensors may be passed in (pre-allocated, e.g. to keep rows
+past the valid count untouched) or are allocated here with torch.empty.
+Every computation runs in the library's CUDA kernels; loading fails loudly if
+the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import re
+from pathlib import Path
+
+import torch
+
+_PKG = Path(__file__).resolve().parent
+LIB_PATH = _PKG / "libmoe_gb300.so"
+HEADER = _PKG.parent / "include" / "moe.h"
+
+MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_WORKSPACE = 0, -1, -2, -3, -4
+MOE_DTYPE_BF16, MOE_DTYPE_F32, MOE_DTYPE_E4M3 = 0, 1, 2
+MOE_EPILOGUE_NONE, MOE_EPILOGUE_SILU_MUL = 0, 1
+MOE_DEVERR_BAD_INDEX, MOE_DEVERR_BAD_COUNT, MOE_DEVERR_TIMEOUT = 1, 2, 4
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int, cuda_error: int = 0):
+        self.status = status
+        msg = f"{fn} failed: {_lib.moe_status_string(status).decode()} ({status})"
+        if status == MOE_ERR_CUDA:
+            msg += f", cudaError {cuda_error}"
+        super().__init__(msg)
+
+
+def _load() -> ctypes.CDLL:
+    if not LIB_PATH.exists():
+        raise ImportError(f"{LIB_PATH.name} is not built: run `python -m moe_token_routing_index_gb300.build` "
+                          "(the CUDA library is required; there is no fallback)")
+    lib = ctypes.CDLL(str(LIB_PATH))
+    P, I, L, S, U = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.POINTER(ctypes.c_uint)
+    sigs = {
+        "moe_status_string": ([I], ctypes.c_char_p),
+        "moe_last_cuda_error": ([], I),
+        "moe_device_error": ([U, P], I),
+        "moe_route_workspace_size": ([I, I, I, ctypes.POINTER(S)], I),
+        "moe_route": ([P, I, L, L, I, I, I, P, P, P, P, P, P, P, S, P], I),
+        "moe_gather_scale": ([P, I, I, P, P, I, P, I, L, L, I, P, P, P], I),
+        "moe_gather_scale_quant": ([P, I, I, P, P, I, P, I, L, L, I, P, P, P, P, P], I),
+        "moe_quantize_rows": ([P, L, I, P, P, P, P], I),
+        "moe_grouped_gemm": ([P, P, P, I, I, I, I, P, I, P], I),
+        "moe_grouped_gemm_fp8_rowwise": ([P, P, P, P, P, I, I, I, I, P, I, P], I),
+        "moe_silu_mul": ([P, P, L, I, I, P, P, P], I),
+        "moe_silu_mul_quant": ([P, P, L, I, I, P, P, P, P, P], I),
+        "moe_scatter_add": ([P, P, P, P, I, I, I, I, P, P], I),
+    }
+    for name, (args, res) in sigs.items():
+        fn = getattr(lib, name)
+        fn.argtypes, fn.restype = args, res
+    return lib
+
+
+_lib = _load()
+
+
+def header_symbols() -> list[str]:
+    """Names of the functions include/moe.h declares."""
+    text = HEADER.read_text()
+    return sorted(set(re.findall(r"^(?:int|const char\*)\s+(moe_\w+)\s*\(", text, flags=re.M)))
+
+
+def library() -> ctypes.CDLL:
+    return _lib
+
+
+def _check(fn: str, status: int):
+    if status != MOE_OK:
+        raise MoEError(fn, status, _lib.moe_last_cuda_error() if status == MOE_ERR_CUDA else 0)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return MOE_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return MOE_DTYPE_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _need(t: torch.Tensor, dtype, name: str):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+
+
+def device_error(stream=None) -> int:
+    """Read and clear the device-side error bits (synchronises the stream)."""
+    bits = ctypes.c_uint(0)
+    _check("moe_device_error", _lib.moe_device_error(ctypes.byref(bits), _stream(stream)))
+    return bits.value
+
+
+# ------------------------------------------------------------------ routing
+
+def moe_route_workspace_size(T: int, E: int, top_k: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check("moe_route_workspace_size", _lib.moe_route_workspace_size(T, E, top_k, ctypes.byref(n)))
+    return n.value
+
+
+def moe_route(scores: torch.Tensor, top_k: int, num_valid_tokens: torch.Tensor | None = None, *,
+              with_inv: bool = True, out: dict | None = None, workspace: torch.Tensor | None = None, stream=None):
+    """Route scores[T, E]; returns dict(counts, expert_offsets, expert_indices,
+    token_indices, inv_rows) of int32 device tensors (index arrays of T * top_k)."""
+    T, E = scores.shape
+    dev = scores.device
+    o = dict(out or {})
+    i32 = dict(dtype=torch.int32, device=dev)
+    o.setdefault("counts", torch.empty(E + 1, **i32))
+    o.setdefault("expert_offsets", torch.empty(E + 1, **i32))
+    o.setdefault("expert_indices", torch.empty(T * top_k, **i32))
+    o.setdefault("token_indices", torch.empty(T * top_k, **i32))
+    if with_inv:
+        o.setdefault("inv_rows", torch.empty(T * top_k, **i32))
+    else:
+        o["inv_rows"] = None
+    ws_bytes = moe_route_workspace_size(T, E, top_k)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    if num_valid_tokens is not None:
+        _need(num_valid_tokens, torch.int32, "num_valid_tokens")
+    st = _lib.moe_route(_ptr(scores), _dtype_code(scores), scores.stride(0), scores.stride(1), T, E, top_k,
+                        _ptr(num_valid_tokens), _ptr(o["counts"]), _ptr(o["expert_offsets"]),
+                        _ptr(o["expert_indices"]), _ptr(o["token_indices"]), _ptr(o["inv_rows"]),
+                        _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("moe_route", st)
+    return o
+
+
+# ------------------------------------------------------------------- gather
+
+def moe_gather_scale(x, token_indices, expert_indices, scores, valid_token_count=None, *, out=None, stream=None):
+    T, D = x.shape
+    a = token_indices.shape[0]
+    _need(x, torch.bfloat16, "x")
+    if out is None:
+        out = torch.empty(a, D, dtype=x.dtype, device=x.device)
+    st = _lib.moe_gather_scale(_ptr(x), T, D, _ptr(token_indices), _ptr(expert_indices), a, _ptr(scores),
+                               _dtype_code(scores), scores.stride(0), scores.stride(1), scores.shape[1],
+                               _ptr(valid_token_count), _ptr(out), _stream(stream))
+    _check("moe_gather_scale", st)
+    return out
+
+
+def moe_gather_scale_quant(x, token_indices, expert_indices, scores, scale_ub=None, valid_token_count=None, *,
+                           out=None, out_scale=None, stream=None):
+    T, D = x.shape
+    a = token_indices.shape[0]
+    _need(x, torch.bfloat16, "x")
+    if out is None:
+        out = torch.empty(a, D, dtype=torch.float8_e4m3fn, device=x.device)
+    if out_scale is None:
+        out_scale = torch.empty(a, dtype=torch.float32, device=x.device)
+    st = _lib.moe_gather_scale_quant(_ptr(x), T, D, _ptr(token_indices), _ptr(expert_indices), a, _ptr(scores),
+                                     _dtype_code(scores), scores.stride(0), scores.stride(1), scores.shape[1],
+                                     _ptr(valid_token_count), _ptr(scale_ub), _ptr(out), _ptr(out_scale),
+                                     _stream(stream))
+    _check("moe_gather_scale_quant", st)
+    return out, out_scale
+
+
+def moe_quantize_rows(w: torch.Tensor, scale_ub=None, *, out=None, out_scale=None, stream=None):
+    """Per-row FP8 quantisation over the last dim of an fp32 tensor."""
+    _need(w, torch.float32, "w")
+    cols = w.shape[-1]
+    rows = w.numel() // cols if cols else 0
+    if out is None:
+        out = torch.empty(w.shape, dtype=torch.float8_e4m3fn, device=w.device)
+    if out_scale is None:
+        out_scale = torch.empty(w.shape[:-1], dtype=torch.float32, device=w.device)
+    st = _lib.moe_quantize_rows(_ptr(w), rows, cols, _ptr(scale_ub), _ptr(out), _ptr(out_scale), _stream(stream))
+    _check("moe_quantize_rows", st)
+    return out, out_scale
+
+
+# ------------------------------------------------------------- grouped GEMM
+
+def moe_grouped_gemm(x, w, counts, *, epilogue: int = MOE_EPILOGUE_NONE, out=None, stream=None):
+    """x[a_max, K] bf16, w[E, N, K] bf16, counts[>= E] int32 -> y[a_max, N or N/2]."""
+    a_max, K = x.shape
+    E, N, K2 = w.shape
+    assert K == K2
+    _need(x, torch.bfloat16, "x")
+    _need(w, torch.bfloat16, "w")
+    n_out = N // 2 if epilogue == MOE_EPILOGUE_SILU_MUL else N
+    if out is None:
+        out = torch.empty(a_max, n_out, dtype=torch.bfloat16, device=x.device)
+    st = _lib.moe_grouped_gemm(_ptr(x), _ptr(w), _ptr(counts), E, a_max, N, K, _ptr(out), epilogue, _stream(stream))
+    _check("moe_grouped_gemm", st)
+    return out
+
+
+def moe_grouped_gemm_fp8_rowwise(x, w, counts, x_scale, w_scale, *, epilogue: int = MOE_EPILOGUE_NONE, out=None,
+                                 stream=None):
+    a_max, K = x.shape
+    E, N, K2 = w.shape
+    assert K == K2
+    _need(x, torch.float8_e4m3fn, "x")
+    _need(w, torch.float8_e4m3fn, "w")
+    n_out = N // 2 if epilogue == MOE_EPILOGUE_SILU_MUL else N
+    if out is None:
+        out = torch.empty(a_max, n_out, dtype=torch.bfloat16, device=x.device)
+    st = _lib.moe_grouped_gemm_fp8_rowwise(_ptr(x), _ptr(w), _ptr(counts), _ptr(x_scale), _ptr(w_scale), E, a_max,
+                                           N, K, _ptr(out), epilogue, _stream(stream))
+    _check("moe_grouped_gemm_fp8_rowwise", st)
+    return out
+
+
+# ----------------------------------------------------------------- silu_mul
+
+def moe_silu_mul(y, H: int | None = None, valid_rows=None, *, out=None, stream=None):
+    """y[a, 2H] bf16 -> z[a, H] = silu(y[:, :H]) * y[:, H:]."""
+    a, n2 = y.shape
+    H = n2 // 2 if H is None else H
+    _need(y, torch.bfloat16, "y")
+    if out is None:
+        out = torch.empty(a, H, dtype=torch.bfloat16, device=y.device)
+    x1 = ctypes.c_void_p(y.data_ptr() + H * y.element_size())
+    st = _lib.moe_silu_mul(_ptr(y), x1, y.stride(0), a, H, _ptr(valid_rows), _ptr(out), _stream(stream))
+    _check("moe_silu_mul", st)
+    return out
+
+
+def moe_silu_mul_quant(y, H: int | None = None, scale_ub=None, valid_rows=None, *, out=None, out_scale=None,
+                       stream=None):
+    a, n2 = y.shape
+    H = n2 // 2 if H is None else H
+    _need(y, torch.bfloat16, "y")
+    if out is None:
+        out = torch.empty(a, H, dtype=torch.float8_e4m3fn, device=y.device)
+    if out_scale is None:
+        out_scale = torch.empty(a, dtype=torch.float32, device=y.device)
+    x1 = ctypes.c_void_p(y.data_ptr() + H * y.element_size())
+    st = _lib.moe_silu_mul_quant(_ptr(y), x1, y.stride(0), a, H, _ptr(valid_rows), _ptr(scale_ub), _ptr(out),
+                                 _ptr(out_scale), _stream(stream))
+    _check("moe_silu_mul_quant", st)
+    return out, out_scale
+
+
+# -------------------------------------------------------------- scatter-add
+
+def moe_scatter_add(out, rows, token_indices, inv_rows=None, top_k: int = 1, valid_token_count=None, *,
+                    stream=None):
+    """out[T, D] += rows[a, D] by token, in place (deterministic)."""
+    T, D = out.shape
+    a = rows.shape[0]
+    _need(out, torch.bfloat16, "out")
+    _need(rows, torch.bfloat16, "rows")
+    st = _lib.moe_scatter_add(_ptr(out), _ptr(rows), _ptr(token_indices), _ptr(inv_rows), top_k, a, T, D,
+                              _ptr(valid_token_count), _stream(stream))
+    _check("moe_scatter_add", st)
+    return out

@@ -1,0 +1,254 @@
+// The C ABI of libmoe_gb300 (declared in include/moe.h): argument checks on
+// the host, then the launchers of the kernel translation units.
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+// Device-side error word (MOE_DEVERR_* bits), one per device that loads the library.
+__device__ unsigned int g_moe_device_error;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int* g_err_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = (int)e;
+  return MOE_ERR_CUDA;
+}
+
+int current_device(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (*dev < 0 || *dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+// Device address of the error word on the current device (looked up once per device).
+int device_error_word(unsigned int** out) {
+  int dev;
+  int rc = current_device(&dev);
+  if (rc != MOE_OK) return rc;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_moe_device_error);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_err_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  *out = g_err_ptr[dev];
+  return MOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int finish(cudaError_t e) { return e == cudaSuccess ? MOE_OK : cuda_fail(e); }
+
+int check_scores(const void* scores, int dtype, int E) {
+  if (!scores) return MOE_ERR_INVALID;
+  if (dtype != MOE_DTYPE_BF16 && dtype != MOE_DTYPE_F32) return MOE_ERR_INVALID;
+  if (E < 1) return MOE_ERR_INVALID;
+  if (E > 1024) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+}  // namespace
+
+namespace moe {
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return kNumSmsGB300;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_sm_count[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = kNumSmsGB300;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+}  // namespace moe
+
+extern "C" {
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape, alignment or type";
+    case MOE_ERR_CUDA: return "CUDA error (see moe_last_cuda_error)";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+int moe_last_cuda_error(void) { return t_last_cuda_error; }
+
+int moe_device_error(unsigned int* bits, cudaStream_t stream) {
+  if (!bits) return MOE_ERR_INVALID;
+  unsigned int* p;
+  int rc = device_error_word(&p);
+  if (rc != MOE_OK) return rc;
+  cudaError_t e = cudaMemcpyAsync(bits, p, sizeof(unsigned int), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, sizeof(unsigned int), stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  return finish(e);
+}
+
+int moe_route_workspace_size(int T, int E, int top_k, size_t* bytes) {
+  if (!bytes || T < 0 || E < 1 || top_k < 1 || top_k > E) return MOE_ERR_INVALID;
+  if (E > 1024) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)T * top_k > INT32_MAX) return MOE_ERR_INVALID;
+  *bytes = moe::route_workspace_bytes(T, E, top_k);
+  return MOE_OK;
+}
+
+int moe_route(const void* scores, int scores_dtype, int64_t stride_t, int64_t stride_e, int T, int E, int top_k,
+              const int32_t* num_valid_tokens, int32_t* counts, int32_t* expert_offsets, int32_t* expert_indices,
+              int32_t* token_indices, int32_t* inv_rows, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  size_t need;
+  int rc = moe_route_workspace_size(T, E, top_k, &need);
+  if (rc != MOE_OK) return rc;
+  if (!counts || !expert_offsets) return MOE_ERR_INVALID;
+  if (T > 0) {
+    rc = check_scores(scores, scores_dtype, E);
+    if (rc != MOE_OK) return rc;
+    if (!expert_indices || !token_indices || !ws) return MOE_ERR_INVALID;
+    if (stride_t < 0 || stride_e < 0) return MOE_ERR_INVALID;
+  }
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE;
+  if (ws && (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOE_ERR_INVALID;
+  moe::RouteArgs a{scores, scores_dtype, stride_t, stride_e, T, E, top_k, num_valid_tokens, counts, expert_offsets,
+                   expert_indices, token_indices, inv_rows, ws, nullptr};
+  rc = device_error_word(&a.err);
+  if (rc != MOE_OK) return rc;
+  return finish(moe::launch_route(a, stream));
+}
+
+static int check_gather(const void* x, int T, int D, const int32_t* ti, const int32_t* ei, int a,
+                        const void* scores, int dtype, int E, const void* out) {
+  if (T < 0 || D < 0 || a < 0) return MOE_ERR_INVALID;
+  if (a == 0 || D == 0) return MOE_OK;
+  if (!x || !ti || !ei || !out) return MOE_ERR_INVALID;
+  int rc = check_scores(scores, dtype, E);
+  if (rc != MOE_OK) return rc;
+  if (D % 16 != 0 || !aligned16(x) || !aligned16(out)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int moe_gather_scale(const void* x, int T, int D, const int32_t* token_indices, const int32_t* expert_indices, int a,
+                     const void* scores, int scores_dtype, int64_t stride_t, int64_t stride_e, int E,
+                     const int32_t* valid_token_count, void* out, cudaStream_t stream) {
+  int rc = check_gather(x, T, D, token_indices, expert_indices, a, scores, scores_dtype, E, out);
+  if (rc != MOE_OK || a == 0 || D == 0) return rc;
+  moe::GatherArgs g{x, T, D, token_indices, expert_indices, a, scores, scores_dtype, stride_t, stride_e, E,
+                    valid_token_count, nullptr, out, nullptr, nullptr};
+  rc = device_error_word(&g.err);
+  if (rc != MOE_OK) return rc;
+  return finish(moe::launch_gather_scale(g, stream));
+}
+
+int moe_gather_scale_quant(const void* x, int T, int D, const int32_t* token_indices, const int32_t* expert_indices,
+                           int a, const void* scores, int scores_dtype, int64_t stride_t, int64_t stride_e, int E,
+                           const int32_t* valid_token_count, const float* scale_ub, void* out, float* out_scale,
+                           cudaStream_t stream) {
+  int rc = check_gather(x, T, D, token_indices, expert_indices, a, scores, scores_dtype, E, out);
+  if (rc != MOE_OK || a == 0 || D == 0) return rc;
+  if (!out_scale) return MOE_ERR_INVALID;
+  if (D > 16384) return MOE_ERR_UNSUPPORTED;
+  moe::GatherArgs g{x, T, D, token_indices, expert_indices, a, scores, scores_dtype, stride_t, stride_e, E,
+                    valid_token_count, scale_ub, out, out_scale, nullptr};
+  rc = device_error_word(&g.err);
+  if (rc != MOE_OK) return rc;
+  return finish(moe::launch_gather_scale_quant(g, stream));
+}
+
+int moe_quantize_rows(const float* w, int64_t rows, int cols, const float* scale_ub, void* q, float* scale,
+                      cudaStream_t stream) {
+  if (rows < 0 || cols < 0) return MOE_ERR_INVALID;
+  if (rows == 0 || cols == 0) return MOE_OK;
+  if (!w || !q || !scale) return MOE_ERR_INVALID;
+  if (cols % 16 != 0 || !aligned16(w) || !aligned16(q)) return MOE_ERR_UNSUPPORTED;
+  return finish(moe::launch_quantize_rows(w, rows, cols, scale_ub, q, scale, stream));
+}
+
+static int check_silu(const void* x0, const void* x1, int64_t ld, int a, int H, const void* z) {
+  if (a < 0 || H < 0) return MOE_ERR_INVALID;
+  if (a == 0 || H == 0) return MOE_OK;
+  if (!x0 || !x1 || !z || ld < H) return MOE_ERR_INVALID;
+  if (H % 16 != 0 || ld % 8 != 0 || !aligned16(x0) || !aligned16(x1) || !aligned16(z)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int moe_silu_mul(const void* x0, const void* x1, int64_t ld, int a, int H, const int32_t* valid_rows, void* z,
+                 cudaStream_t stream) {
+  int rc = check_silu(x0, x1, ld, a, H, z);
+  if (rc != MOE_OK || a == 0 || H == 0) return rc;
+  moe::SiluArgs g{x0, x1, ld, a, H, valid_rows, nullptr, z, nullptr, nullptr};
+  rc = device_error_word(&g.err);
+  if (rc != MOE_OK) return rc;
+  return finish(moe::launch_silu_mul(g, stream));
+}
+
+int moe_silu_mul_quant(const void* x0, const void* x1, int64_t ld, int a, int H, const int32_t* valid_rows,
+                       const float* scale_ub, void* z, float* z_scale, cudaStream_t stream) {
+  int rc = check_silu(x0, x1, ld, a, H, z);
+  if (rc != MOE_OK || a == 0 || H == 0) return rc;
+  if (!z_scale) return MOE_ERR_INVALID;
+  if (H > 16384) return MOE_ERR_UNSUPPORTED;
+  moe::SiluArgs g{x0, x1, ld, a, H, valid_rows, scale_ub, z, z_scale, nullptr};
+  rc = device_error_word(&g.err);
+  if (rc != MOE_OK) return rc;
+  return finish(moe::launch_silu_mul_quant(g, stream));
+}
+
+int moe_scatter_add(void* out, const void* in, const int32_t* token_indices, const int32_t* inv_rows, int top_k,
+                    int a, int T, int D, const int32_t* valid_token_count, cudaStream_t stream) {
+  if (a < 0 || T < 0 || D < 0 || top_k < 1) return MOE_ERR_INVALID;
+  if (a == 0 || D == 0 || T == 0) return MOE_OK;
+  if (!out || !in) return MOE_ERR_INVALID;
+  if (top_k > 1 && !inv_rows) return MOE_ERR_INVALID;
+  if (!inv_rows && !token_indices) return MOE_ERR_INVALID;
+  if (D % 16 != 0 || !aligned16(out) || !aligned16(in)) return MOE_ERR_UNSUPPORTED;
+  moe::ScatterArgs g{out, in, token_indices, inv_rows, top_k, a, T, D, valid_token_count, nullptr};
+  int rc = device_error_word(&g.err);
+  if (rc != MOE_OK) return rc;
+  return finish(moe::launch_scatter_add(g, stream));
+}
+
+static int grouped_gemm_common(const void* x, const void* w, const int32_t* counts, const float* x_scale,
+                               const float* w_scale, int E, int a_max, int N, int K, void* y, int epilogue,
+                               bool fp8, cudaStream_t stream) {
+  if (E < 1 || a_max < 0 || N < 0 || K < 0) return MOE_ERR_INVALID;
+  if (epilogue != MOE_EPILOGUE_NONE && epilogue != MOE_EPILOGUE_SILU_MUL) return MOE_ERR_INVALID;
+  if (a_max == 0 || N == 0) return MOE_OK;
+  if (!x || !w || !counts || !y) return MOE_ERR_INVALID;
+  if (fp8 && (!x_scale || !w_scale)) return MOE_ERR_INVALID;
+  if (E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (N % 16 != 0 || K % 16 != 0 || K == 0) return MOE_ERR_UNSUPPORTED;
+  if (epilogue == MOE_EPILOGUE_SILU_MUL && (N % 32 != 0)) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return MOE_ERR_UNSUPPORTED;
+  moe::GemmArgs g{x, w, counts, x_scale, w_scale, E, a_max, N, K, y, epilogue, fp8, nullptr};
+  int rc = device_error_word(&g.err);
+  if (rc != MOE_OK) return rc;
+  cudaError_t e = moe::launch_grouped_gemm(g, stream);
+  if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
+  return finish(e);
+}
+
+int moe_grouped_gemm(const void* x, const void* w, const int32_t* counts, int E, int a_max, int N, int K, void* y,
+                     int epilogue, cudaStream_t stream) {
+  return grouped_gemm_common(x, w, counts, nullptr, nullptr, E, a_max, N, K, y, epilogue, false, stream);
+}
+
+int moe_grouped_gemm_fp8_rowwise(const void* x, const void* w, const int32_t* counts, const float* x_scale,
+                                 const float* w_scale, int E, int a_max, int N, int K, void* y, int epilogue,
+                                 cudaStream_t stream) {
+  return grouped_gemm_common(x, w, counts, x_scale, w_scale, E, a_max, N, K, y, epilogue, true, stream);
+}
+
+}  // extern "C"

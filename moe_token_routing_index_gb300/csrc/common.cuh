@@ -1,0 +1,88 @@
+// Internal helpers shared by the kernel translation units of libmoe_gb300.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kNumSmsGB300 = 152;
+constexpr float kFp8Max = 448.0f;
+constexpr float kFp8Eps = 1e-12f;
+
+// Record a device-side error bit (first writer does not matter: bits are OR-ed).
+__device__ __forceinline__ void flag_error(unsigned int* err, unsigned int bit) {
+  if (err) atomicOr(err, bit);
+}
+
+// Read a device int32 count, clamped to [0, hi]; NULL means hi.
+__device__ __forceinline__ int read_count(const int32_t* p, int hi, unsigned int* err) {
+  if (!p) return hi;
+  int v = *p;
+  if (v < 0 || v > hi) {
+    flag_error(err, MOE_DEVERR_BAD_COUNT);
+    v = v < 0 ? 0 : hi;
+  }
+  return v;
+}
+
+__device__ __forceinline__ float load_score(const void* scores, int dtype, int64_t off) {
+  if (dtype == MOE_DTYPE_F32) return __ldg(reinterpret_cast<const float*>(scores) + off);
+  return __bfloat162float(__ldg(reinterpret_cast<const __nv_bfloat16*>(scores) + off));
+}
+
+// 8 bf16 in a uint4 <-> 8 floats.
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 p = __bfloat1622float2(h[i]);
+    f[2 * i] = p.x;
+    f[2 * i + 1] = p.y;
+  }
+}
+
+__device__ __forceinline__ uint4 f32_to_bf16x8(const float* f) {
+  uint4 v;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  return v;
+}
+
+// Two floats -> two e4m3 codes (round to nearest even, saturating to +-448),
+// low byte = a, high byte = b.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float a, float b) {
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
+
+// silu(a) * b = a * sigmoid(a) * b in fp32, left to right, sigmoid(a) = 1 / (1 + e^-a).
+__device__ __forceinline__ float silu_mul_f32(float a, float b) {
+  float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-a)));
+  return __fmul_rn(__fmul_rn(a, sg), b);
+}
+
+// The FP8-rowwise scale rule: m = max|v| clamped to [EPS, ub] (or >= EPS);
+// returns s = 448 / m and writes the stored dequantisation scale 1 / s.
+__device__ __forceinline__ float fp8_row_scale(float m, const float* ub, float* inv_out) {
+  m = fmaxf(m, kFp8Eps);
+  if (ub) m = fminf(m, __ldg(ub));
+  float s = __fdiv_rn(kFp8Max, m);
+  *inv_out = __frcp_rn(s);
+  return s;
+}
+
+__device__ __forceinline__ float fp8_scaled_clamped(float v, float s) {
+  return fminf(fmaxf(__fmul_rn(v, s), -kFp8Max), kFp8Max);
+}
+
+// Max over a warp of non-negative floats (their bit patterns order like the values).
+__device__ __forceinline__ float warp_max_nonneg(float v) {
+  return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v)));
+}
+
+}  // namespace moe

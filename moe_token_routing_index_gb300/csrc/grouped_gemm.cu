@@ -1,0 +1,571 @@
+// Grouped GEMM of the routed experts on the 5th-generation tensor cores
+// (mslk/moe/layers.py, MetaShufflingMoE._routed_expert: grouped_gemm and
+// grouped_gemm_fp8_rowwise over w13 and w2).
+//
+// y[r, n] = sum_k x[r, k] * w[e, n, k] for the rows r of expert e, i.e. a
+// "TN" GEMM per expert with both operands K-major.
+//
+// Kernel structure (one CTA per SM, persistent, 6 warps):
+//   warp 0     TMA producer: 128-row A tile (routed rows) and two 128-row B
+//              tiles (weight rows) of 128 bytes of K per stage, 128B-swizzled,
+//              into a 4-stage shared-memory ring guarded by mbarriers.
+//   warp 1     MMA issuer: tcgen05.mma (M=128, N=256, fp32 accumulate) into one
+//              of two 256-column accumulators in tensor memory; tcgen05.commit
+//              frees the smem stage and, after the last K block, hands the
+//              accumulator to the epilogue.  Also allocates/frees the 512
+//              tensor-memory columns.
+//   warps 2-5  epilogue: tcgen05.ld of the accumulator rows (one TMEM lane per
+//              thread), optional FP8 dequantisation, optional SiLU*mul of the
+//              two halves, bf16 rounding, stores with row/column masks.
+// Tiles: for each expert e, ceil(count_e / 128) row tiles x the N tiles;
+// consecutive tile ids walk the row tiles of one weight slice first, so CTAs
+// running together share that slice in L2.  Every CTA derives the tile list
+// from the device counts itself (no host synchronisation).
+//
+// Every mbarrier wait is bounded (1 s of %globaltimer); on expiry the kernel
+// records MOE_DEVERR_TIMEOUT, all roles stop, in-flight copies and MMAs are
+// drained with bounded waits, and tensor memory is freed before exit.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128;            // rows of a tile (routed rows)
+constexpr int kBN = 256;            // accumulator columns (MMA N)
+constexpr int kBKBytes = 128;       // bytes of K per stage (one 128B swizzle atom per row)
+constexpr int kStages = 4;
+constexpr int kAccBufs = 2;
+constexpr int kTmemCols = kAccBufs * kBN;  // 512
+constexpr int kThreads = 192;
+constexpr int kABytes = kBM * kBKBytes;          // 16 KB
+constexpr int kBBytes = kBN * kBKBytes;          // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;   // 48 KB
+constexpr int kMaxExperts = 1024;
+constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // 1 s
+constexpr uint64_t kDrainTimeoutNs = 100000000ull;  // 100 ms
+
+struct SmemLayout {
+  // offsets from the 1024-aligned base
+  static constexpr int a = 0;
+  static constexpr int b = a + kStages * kABytes;
+  static constexpr int bars = b + kStages * kBBytes;        // full[S], empty[S], tfull[2], tempty[2], drain
+  static constexpr int nbars = 2 * kStages + 2 * kAccBufs + 1;
+  static constexpr int misc = bars + nbars * 8;             // tmem base, abort flag, total tiles, pad
+  static constexpr int sched = misc + 16;                   // tile_start[E+1], row_off[E+1], mtiles[E]
+  static constexpr int bytes_for(int E) { return sched + (3 * E + 2) * 4; }
+};
+
+// ------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete; false after `limit_ns`
+// or as soon as another role has raised the abort flag.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t limit_ns = kWaitTimeoutNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (abort_flag && *abort_flag) return false;
+      if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128B swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);         // start address
+  d |= (uint64_t)1 << 16;                          // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;                // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;                          // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;                          // swizzle: 128B
+  return d;
+}
+
+// Instruction descriptor: fp32 accumulate, A/B K-major, M = 128, N = 256.
+template <bool FP8>
+__device__ __forceinline__ uint32_t instr_desc() {
+  const uint32_t fmt = FP8 ? 0u /*E4M3*/ : 1u /*BF16*/;
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+}
+
+template <bool FP8>
+__device__ __forceinline__ void mma_issue(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if constexpr (FP8) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+  }
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive fp32 accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ------------------------------------------------------------- scheduling
+
+struct Tile {
+  int expert, row0, rows, n_idx;
+};
+
+// Decode tile id -> (expert, first routed row, valid rows, N-tile index).
+__device__ __forceinline__ Tile decode_tile(int tile, int E, int n_tiles, const int* tile_start, const int* row_off,
+                                            const int* mtiles) {
+  const int mt_global = tile / n_tiles;  // which row tile, counting over experts
+  int lo = 0, hi = E - 1;                // find e with tile_start[e] <= mt_global < tile_start[e + 1]
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tile_start[mid] <= mt_global) lo = mid;
+    else hi = mid - 1;
+  }
+  const int e = lo;
+  const int local = tile - tile_start[e] * n_tiles;  // within the expert: N-major, row tiles innermost
+  const int m_idx = local % mtiles[e];
+  Tile t;
+  t.expert = e;
+  t.n_idx = local / mtiles[e];
+  t.row0 = row_off[e] + m_idx * kBM;
+  const int rows_left = row_off[e + 1] - t.row0;
+  t.rows = rows_left < kBM ? rows_left : kBM;
+  return t;
+}
+
+// ----------------------------------------------------------------- kernel
+
+template <bool FP8, int EPI>
+__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
+    const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+    const int32_t* __restrict__ counts, const float* __restrict__ x_scale, const float* __restrict__ w_scale, int E,
+    int a_max, int N, int K, __nv_bfloat16* __restrict__ y, unsigned int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  const uint32_t sbase = smem_u32(smem);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SmemLayout::bars);
+  auto bar_full = [&](int s) { return smem_u32(&bars[s]); };
+  auto bar_empty = [&](int s) { return smem_u32(&bars[kStages + s]); };
+  auto bar_tfull = [&](int b) { return smem_u32(&bars[2 * kStages + b]); };
+  auto bar_tempty = [&](int b) { return smem_u32(&bars[2 * kStages + kAccBufs + b]); };
+  const uint32_t bar_drain = smem_u32(&bars[2 * kStages + 2 * kAccBufs]);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + SmemLayout::misc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + SmemLayout::misc + 4);
+  int* s_total = reinterpret_cast<int*>(smem + SmemLayout::misc + 8);
+  int* tile_start = reinterpret_cast<int*>(smem + SmemLayout::sched);  // [E + 1]
+  int* row_off = tile_start + (E + 1);                                  // [E + 1]
+  int* mtiles = row_off + (E + 1);                                      // [E]
+
+  // ---- prologue: barriers, tensor memory, the tile list from the counts
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    for (int b = 0; b < kAccBufs; ++b) {
+      mbar_init(bar_tfull(b), 1);
+      mbar_init(bar_tempty(b), 4);  // one arrive per epilogue warp
+    }
+    mbar_init(bar_drain, 1);
+    *s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tma_prefetch_desc(&map_a);
+    tma_prefetch_desc(&map_b);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(s_tmem)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (warp == 2) {
+    // Row offsets and row-tile starts: warp-wide exclusive scans over the experts.
+    // Counts are clamped so that no tile reaches past a_max rows.
+    int run_rows = 0, run_tiles = 0;
+    bool bad = false;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      int c = e < E ? counts[e] : 0;
+      if (c < 0) {
+        c = 0;
+        bad = true;
+      }
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int start = run_rows + incl - c;
+      if (start > a_max) start = a_max;
+      int end = run_rows + incl;
+      if (end > a_max) {
+        end = a_max;
+        bad = true;
+      }
+      const int mt = (end - start + kBM - 1) / kBM;
+      int tincl = mt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, tincl, o);
+        if (lane >= o) tincl += v;
+      }
+      if (e < E) {
+        row_off[e] = start;
+        tile_start[e] = run_tiles + tincl - mt;
+        mtiles[e] = mt;
+      }
+      run_rows = min(__shfl_sync(0xffffffffu, run_rows + incl, 31), a_max);
+      run_tiles += __shfl_sync(0xffffffffu, tincl, 31);
+    }
+    if (lane == 0) {
+      row_off[E] = run_rows;
+      tile_start[E] = run_tiles;
+      *s_total = run_tiles;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0 && blockIdx.x == 0) flag_error(err, MOE_DEVERR_BAD_COUNT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tmem_base = *s_tmem;
+  const int n_out = (EPI == MOE_EPILOGUE_SILU_MUL) ? N / 2 : N;
+  const int n_tile_cols = (EPI == MOE_EPILOGUE_SILU_MUL) ? kBN / 2 : kBN;  // output columns per tile
+  const int n_tiles = (n_out + n_tile_cols - 1) / n_tile_cols;
+  const int total_tiles = *s_total * n_tiles;
+  const int elems_per_kb = FP8 ? kBKBytes : kBKBytes / 2;
+  const int num_kb = (K + elems_per_kb - 1) / elems_per_kb;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_parity = 0;  // per stage: issued since start, parity of that issue
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+        const Tile t = decode_tile(tile, E, n_tiles, tile_start, row_off, mtiles);
+        int b_row0, b_row1;
+        if (EPI == MOE_EPILOGUE_SILU_MUL) {
+          b_row0 = t.expert * N + t.n_idx * (kBN / 2);
+          b_row1 = b_row0 + N / 2;
+        } else {
+          b_row0 = t.expert * N + t.n_idx * kBN;
+          b_row1 = b_row0 + kBN / 2;
+        }
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(bar_empty(s), phase ^ 1u, s_abort)) {
+            ok = false;
+            break;
+          }
+          const uint32_t a_dst = sbase + SmemLayout::a + s * kABytes;
+          const uint32_t b_dst = sbase + SmemLayout::b + s * kBBytes;
+          mbar_arrive_expect_tx(bar_full(s), kStageBytes);
+          const int kc = kb * elems_per_kb;
+          tma_load_2d(a_dst, &map_a, bar_full(s), kc, t.row0);
+          tma_load_2d(b_dst, &map_b, bar_full(s), kc, b_row0);
+          tma_load_2d(b_dst + kBBytes / 2, &map_b, bar_full(s), kc, b_row1);
+          issued_mask |= 1u << s;
+          issued_parity = (issued_parity & ~(1u << s)) | (phase << s);
+          if (++s == kStages) {
+            s = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        flag_error(err, MOE_DEVERR_TIMEOUT);
+        *s_abort = 1;
+        // Let the copies already issued land before the CTA can exit.
+        for (int i = 0; i < kStages; ++i)
+          if ((issued_mask >> i) & 1u) mbar_wait(bar_full(i), (issued_parity >> i) & 1u, nullptr, kDrainTimeoutNs);
+      }
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------------- MMA
+    if (lane == 0) {
+      const uint32_t idesc = instr_desc<FP8>();
+      int s = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true, issued_any = false;
+      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(bar_tempty(acc), acc_phase ^ 1u, s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * kBN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(bar_full(s), phase, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = sbase + SmemLayout::a + s * kABytes;
+          const uint32_t b_addr = sbase + SmemLayout::b + s * kBBytes;
+#pragma unroll
+          for (int kk = 0; kk < kBKBytes / 32; ++kk) {  // 32 bytes of K per instruction
+            mma_issue<FP8>(d, smem_desc_sw128(a_addr + kk * 32), smem_desc_sw128(b_addr + kk * 32), idesc,
+                           (kb | kk) != 0);
+          }
+          issued_any = true;
+          mma_commit(bar_empty(s));
+          if (++s == kStages) {
+            s = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(bar_tfull(acc));
+        if (++acc == kAccBufs) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        flag_error(err, MOE_DEVERR_TIMEOUT);
+        *s_abort = 1;
+        if (issued_any) {  // wait for the MMAs in flight before tensor memory is freed
+          mma_commit(bar_drain);
+          mbar_wait(bar_drain, 0, nullptr, kDrainTimeoutNs);
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int sub = warp & 3;                // TMEM lane quarter this warp may access
+    const int row_in_tile = sub * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      const Tile t = decode_tile(tile, E, n_tiles, tile_start, row_off, mtiles);
+      if (!mbar_wait(bar_tfull(acc), acc_phase, s_abort)) {
+        if (lane == 0) flag_error(err, MOE_DEVERR_TIMEOUT);
+        *s_abort = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * kBN);
+      const bool row_ok = row_in_tile < t.rows;
+      const int row = t.row0 + row_in_tile;
+      float xs = 1.0f;
+      if (FP8 && row_ok) xs = __ldg(x_scale + row);
+      __nv_bfloat16* yrow = y + (int64_t)row * n_out;
+      const int col0 = t.n_idx * n_tile_cols;
+      const float* wsc = FP8 ? w_scale + (int64_t)t.expert * N : nullptr;
+      if (EPI == MOE_EPILOGUE_SILU_MUL) {
+        const int H = N / 2;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 2; c += 32) {
+          float v0[32], v1[32];
+          tmem_ld32(tbase + c, v0);
+          tmem_ld32(tbase + kBN / 2 + c, v1);
+          if (row_ok && col0 + c < n_out) {
+            float z[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              float a0 = v0[i], a1 = v1[i];
+              if (FP8) {
+                const int col = col0 + c + i < H ? col0 + c + i : H - 1;
+                a0 = __fmul_rn(__fmul_rn(a0, xs), __ldg(wsc + col));
+                a1 = __fmul_rn(__fmul_rn(a1, xs), __ldg(wsc + H + col));
+              }
+              // the unfused pipeline rounds the GEMM output to bf16 before silu_mul
+              a0 = __bfloat162float(__float2bfloat16_rn(a0));
+              a1 = __bfloat162float(__float2bfloat16_rn(a1));
+              z[i] = silu_mul_f32(a0, a1);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (col0 + c + 8 * q < n_out)
+                *reinterpret_cast<uint4*>(yrow + col0 + c + 8 * q) = f32_to_bf16x8(z + 8 * q);
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < kBN; c += 32) {
+          float v[32];
+          tmem_ld32(tbase + c, v);
+          if (row_ok && col0 + c < n_out) {
+            if (FP8) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const int col = col0 + c + i < n_out ? col0 + c + i : n_out - 1;
+                v[i] = __fmul_rn(__fmul_rn(v[i], xs), __ldg(wsc + col));
+              }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (col0 + c + 8 * q < n_out)
+                *reinterpret_cast<uint4*>(yrow + col0 + c + 8 * q) = f32_to_bf16x8(v + 8 * q);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_tempty(acc));
+      if (++acc == kAccBufs) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  // ---- teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols) : "memory");
+}
+
+// ------------------------------------------------------------------- host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Row-major [rows, cols] matrix of 1- or 2-byte elements, box of 128 rows x 128 bytes, 128B swizzle.
+bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, bool fp8) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int esize = fp8 ? 1 : 2;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(cols * esize)};
+  cuuint32_t box[2] = {(cuuint32_t)(kBKBytes / esize), (cuuint32_t)kBM};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <bool FP8, int EPI>
+cudaError_t launch_impl(const GemmArgs& g, cudaStream_t s) {
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, g.x, g.a_max, g.K, FP8) || !make_map(&mb, g.w, (int64_t)g.E * g.N, g.K, FP8))
+    return cudaErrorInvalidValue;
+  const int smem = SmemLayout::bytes_for(g.E) + 1024;
+  auto kern = grouped_gemm_kernel<FP8, EPI>;
+  // The attribute is per device; setting it on every call is cheap and keeps multi-device use correct.
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int n_out = (EPI == MOE_EPILOGUE_SILU_MUL) ? g.N / 2 : g.N;
+  const int n_tile_cols = (EPI == MOE_EPILOGUE_SILU_MUL) ? kBN / 2 : kBN;
+  const int64_t n_tiles = (n_out + n_tile_cols - 1) / n_tile_cols;
+  const int64_t tiles_ub = ((int64_t)(g.a_max + kBM - 1) / kBM + g.E) * n_tiles;
+  const int sms = device_sm_count();
+  const int grid = (int)(tiles_ub < sms ? tiles_ub : sms);
+  kern<<<grid, kThreads, smem, s>>>(ma, mb, g.counts, g.x_scale, g.w_scale, g.E, g.a_max, g.N, g.K,
+                                    static_cast<__nv_bfloat16*>(g.y), g.err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm(const GemmArgs& g, cudaStream_t s) {
+  if (g.E > kMaxExperts) return cudaErrorNotSupported;
+  if (g.fp8) {
+    if (g.epilogue == MOE_EPILOGUE_SILU_MUL) return launch_impl<true, MOE_EPILOGUE_SILU_MUL>(g, s);
+    return launch_impl<true, MOE_EPILOGUE_NONE>(g, s);
+  }
+  if (g.epilogue == MOE_EPILOGUE_SILU_MUL) return launch_impl<false, MOE_EPILOGUE_SILU_MUL>(g, s);
+  return launch_impl<false, MOE_EPILOGUE_NONE>(g, s);
+}
+
+}  // namespace moe

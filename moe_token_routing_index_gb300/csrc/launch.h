@@ -1,0 +1,96 @@
+// Internal launcher interface between the C ABI (api.cu) and the kernel
+// translation units.  Arguments are validated by the caller.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+struct RouteArgs {
+  const void* scores;
+  int dtype;
+  int64_t stride_t, stride_e;
+  int T, E, top_k;
+  const int32_t* num_valid;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* expert_indices;
+  int32_t* token_indices;
+  int32_t* inv;
+  void* ws;
+  unsigned int* err;
+};
+
+size_t route_workspace_bytes(int T, int E, int top_k);
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
+
+struct GatherArgs {
+  const void* x;
+  int T, D;
+  const int32_t* token_indices;
+  const int32_t* expert_indices;
+  int a;
+  const void* scores;
+  int dtype;
+  int64_t stride_t, stride_e;
+  int E;
+  const int32_t* valid;
+  const float* scale_ub;  // quantising variant only
+  void* out;
+  float* out_scale;       // quantising variant only
+  unsigned int* err;
+};
+
+cudaError_t launch_gather_scale(const GatherArgs& a, cudaStream_t s);
+cudaError_t launch_gather_scale_quant(const GatherArgs& a, cudaStream_t s);
+cudaError_t launch_quantize_rows(const float* w, int64_t rows, int cols, const float* ub, void* q, float* scale,
+                                 cudaStream_t s);
+
+struct SiluArgs {
+  const void* x0;
+  const void* x1;
+  int64_t ld;
+  int a, H;
+  const int32_t* valid;
+  const float* scale_ub;  // quantising variant only
+  void* z;
+  float* z_scale;         // quantising variant only
+  unsigned int* err;
+};
+
+cudaError_t launch_silu_mul(const SiluArgs& a, cudaStream_t s);
+cudaError_t launch_silu_mul_quant(const SiluArgs& a, cudaStream_t s);
+
+struct ScatterArgs {
+  void* out;
+  const void* in;
+  const int32_t* token_indices;
+  const int32_t* inv;
+  int top_k, a, T, D;
+  const int32_t* valid;
+  unsigned int* err;
+};
+
+cudaError_t launch_scatter_add(const ScatterArgs& a, cudaStream_t s);
+
+struct GemmArgs {
+  const void* x;        // [a_max, K] bf16 or e4m3
+  const void* w;        // [E, N, K]
+  const int32_t* counts;
+  const float* x_scale; // FP8 only
+  const float* w_scale; // FP8 only
+  int E, a_max, N, K;
+  void* y;
+  int epilogue;
+  bool fp8;
+  unsigned int* err;
+};
+
+cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace moe

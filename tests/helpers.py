@@ -35,3 +35,32 @@ def rms(a: np.ndarray) -> float:
 
 def parse_golden(path) -> list[str]:
     return [ln.split("#", 1)[0].strip() for ln in open(path) if ln.split("#", 1)[0].strip()]
+
+
+def dev_bf16(b: np.ndarray, device="cuda") -> torch.Tensor:
+    """bf16 bits (uint16) -> a bf16 tensor on the device."""
+    return bf16_from_bits(b).to(device)
+
+
+def dev_e4m3(b: np.ndarray, device="cuda") -> torch.Tensor:
+    return e4m3_from_bits(b).to(device)
+
+
+def sentinel_like(shape, dtype, device="cuda") -> torch.Tensor:
+    """A tensor whose every byte is 0xA5, to detect writes past the valid rows."""
+    t = torch.empty(shape, dtype=dtype, device=device)
+    t.view(torch.uint8).fill_(0xA5)
+    return t
+
+
+def is_sentinel(t: torch.Tensor) -> bool:
+    return bool((t.contiguous().view(torch.uint8) == 0xA5).all())
+
+
+def e4m3_step_diff(a: np.ndarray, b: np.ndarray) -> np.ndarray:
+    """Distance in code steps between e4m3 codes of the same sign (large if signs differ)."""
+    a = a.astype(np.int32)
+    b = b.astype(np.int32)
+    same = ((a & 0x80) == (b & 0x80)) | ((a & 0x7F) == 0) | ((b & 0x7F) == 0)
+    mag = np.abs((a & 0x7F) - (b & 0x7F))
+    return np.where(same, mag, 1000)

@@ -1,0 +1,71 @@
+"""The C-ABI library: it builds for sm_103a, loads without a GPU, exports every
+function include/moe.h declares, and rejects bad arguments on the host (these
+calls return before any CUDA call, so they run without a GPU)."""
+import ctypes
+import subprocess
+
+import pytest
+
+from moe_token_routing_index_gb300 import build as mbuild
+
+
+@pytest.fixture(scope="module")
+def lib():
+    mbuild.build()
+    from moe_token_routing_index_gb300 import binding
+
+    return binding
+
+
+def test_library_exports_every_header_symbol(lib):
+    names = lib.header_symbols()
+    assert len(names) >= 13
+    exported = subprocess.run(["nm", "-D", "--defined-only", str(lib.LIB_PATH)], capture_output=True,
+                              text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in exported.splitlines() if ln.strip()}
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        assert hasattr(lib.library(), n)
+
+
+def test_status_strings(lib):
+    L = lib.library()
+    assert L.moe_status_string(0) == b"ok"
+    assert b"invalid" in L.moe_status_string(-1)
+    assert b"workspace" in L.moe_status_string(-4)
+
+
+def test_host_side_validation_without_gpu(lib):
+    L = lib.library()
+    n = ctypes.c_size_t(0)
+    assert L.moe_route_workspace_size(-1, 8, 1, ctypes.byref(n)) == lib.MOE_ERR_INVALID
+    assert L.moe_route_workspace_size(64, 8, 9, ctypes.byref(n)) == lib.MOE_ERR_INVALID      # top_k > E
+    assert L.moe_route_workspace_size(64, 2048, 1, ctypes.byref(n)) == lib.MOE_ERR_UNSUPPORTED
+    assert L.moe_route_workspace_size(64, 8, 2, ctypes.byref(n)) == lib.MOE_OK and n.value > 0
+    fake = ctypes.c_void_p(0x1000)
+    # route: workspace too small
+    assert L.moe_route(fake, 0, 8, 1, 64, 8, 2, None, fake, fake, fake, fake, None, fake, 16, None) \
+        == lib.MOE_ERR_WORKSPACE
+    # route: null counts
+    assert L.moe_route(fake, 0, 8, 1, 64, 8, 2, None, None, fake, fake, fake, None, fake, 1 << 20, None) \
+        == lib.MOE_ERR_INVALID
+    # gather: D not a multiple of 16; empty is a no-op
+    assert L.moe_gather_scale(fake, 4, 24, fake, fake, 4, fake, 0, 8, 1, 8, None, fake, None) \
+        == lib.MOE_ERR_UNSUPPORTED
+    assert L.moe_gather_scale(None, 4, 32, None, None, 0, None, 0, 8, 1, 8, None, None, None) == lib.MOE_OK
+    # gather: bad score dtype
+    assert L.moe_gather_scale(fake, 4, 32, fake, fake, 4, fake, 7, 8, 1, 8, None, fake, None) == lib.MOE_ERR_INVALID
+    # quantising gather needs out_scale
+    assert L.moe_gather_scale_quant(fake, 4, 32, fake, fake, 4, fake, 0, 8, 1, 8, None, None, fake, None, None) \
+        == lib.MOE_ERR_INVALID
+    # scatter: top_k > 1 needs the inverse permutation
+    assert L.moe_scatter_add(fake, fake, fake, None, 2, 8, 4, 32, None, None) == lib.MOE_ERR_INVALID
+    # silu: misaligned row stride
+    assert L.moe_silu_mul(fake, fake, 36, 4, 32, None, fake, None) == lib.MOE_ERR_UNSUPPORTED
+    # grouped GEMM: N not a multiple of 16, unknown epilogue, too many experts
+    assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 24, 64, fake, 0, None) == lib.MOE_ERR_UNSUPPORTED
+    assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 32, 64, fake, 9, None) == lib.MOE_ERR_INVALID
+    assert L.moe_grouped_gemm(fake, fake, fake, 2048, 64, 32, 64, fake, 0, None) == lib.MOE_ERR_UNSUPPORTED
+    assert L.moe_grouped_gemm_fp8_rowwise(fake, fake, fake, None, fake, 4, 64, 32, 64, fake, 0, None) \
+        == lib.MOE_ERR_INVALID

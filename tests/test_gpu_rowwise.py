@@ -1,0 +1,165 @@
+"""The row-wise CUDA stages against the oracle: gather*score and the FP8
+quantising gather (bit-exact), silu_mul (within one bf16 step), silu_mul_quant
+(codes within one e4m3 step) and the scatter-add combine (bit-exact), at the
+workloads' full sizes and on ragged small cases; rows past the valid count
+must keep their sentinel bytes."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_token_routing_index_gb300 import workloads
+from tests.helpers import bits, dev_bf16, e4m3_step_diff, is_sentinel, sentinel_like
+
+pytestmark = pytest.mark.gpu
+
+
+def _mb():
+    from moe_token_routing_index_gb300 import binding
+
+    return binding
+
+
+def _routed(cfg):
+    """Inputs of the gather stage: x, scores and the oracle's routing (int32 on device)."""
+    x = workloads.make_tokens(cfg)
+    s = workloads.make_scores(cfg)
+    r = oracle.route(bits(s), cfg.top_k, cfg.valid_tokens)
+    return x, s, r
+
+
+def _idx(a, n=None):
+    t = torch.from_numpy(np.ascontiguousarray(a, np.int32))
+    if n is not None and n > len(a):      # pad the buffer like the router's T * top_k arrays
+        t = torch.cat([t, torch.zeros(n - len(a), dtype=torch.int32)])
+    return t.cuda()
+
+
+GATHER_CASES = ["tiny", "decode", "decode_zero", "fine_grained"]
+QUANT_CASES = ["prefill_fp8", "padded_fp8"]
+
+
+@pytest.mark.parametrize("name", GATHER_CASES + QUANT_CASES)
+def test_gather_scale_bit_exact(name):
+    mb = _mb()
+    cfg = workloads.CONFIGS[name]
+    x, s, r = _routed(cfg)
+    a_buf = cfg.T * cfg.top_k
+    valid = torch.tensor([r["counts"][cfg.E]], dtype=torch.int32, device="cuda")
+    out = sentinel_like((a_buf, cfg.D), torch.bfloat16)
+    mb.moe_gather_scale(x.cuda(), _idx(r["token_indices"], a_buf), _idx(r["expert_indices"], a_buf), s.cuda(),
+                        valid, out=out)
+    assert mb.device_error() == 0
+    ref = oracle.gather_scale(bits(x), r["token_indices"], r["expert_indices"], bits(s))
+    a = len(r["token_indices"])
+    np.testing.assert_array_equal(bits(out[:a]), ref)
+    assert is_sentinel(out[a:])
+
+
+@pytest.mark.parametrize("name", QUANT_CASES + ["tiny", "fine_grained"])
+@pytest.mark.parametrize("ub", [None, 1200.0, 0.5])
+def test_gather_scale_quant_bit_exact(name, ub):
+    mb = _mb()
+    cfg = workloads.CONFIGS[name]
+    x, s, r = _routed(cfg)
+    a_buf = cfg.T * cfg.top_k
+    valid = torch.tensor([r["counts"][cfg.E]], dtype=torch.int32, device="cuda")
+    ub_t = None if ub is None else torch.tensor([ub], dtype=torch.float32, device="cuda")
+    out = sentinel_like((a_buf, cfg.D), torch.float8_e4m3fn)
+    osc = sentinel_like((a_buf,), torch.float32)
+    mb.moe_gather_scale_quant(x.cuda(), _idx(r["token_indices"], a_buf), _idx(r["expert_indices"], a_buf),
+                              s.cuda(), ub_t, valid, out=out, out_scale=osc)
+    assert mb.device_error() == 0
+    q, sc = oracle.gather_scale_quant(bits(x), r["token_indices"], r["expert_indices"], bits(s), ub)
+    a = len(r["token_indices"])
+    np.testing.assert_array_equal(bits(out[:a]), q)
+    np.testing.assert_array_equal(osc[:a].cpu().numpy(), sc)
+    assert is_sentinel(out[a:]) and is_sentinel(osc[a:])
+
+
+@pytest.mark.parametrize("T,D,a,E", [(5, 16, 7, 3), (40, 272, 33, 6), (9, 2064, 13, 2), (3, 16384, 4, 2)])
+def test_gather_ragged_shapes(T, D, a, E):
+    mb = _mb()
+    g = torch.Generator().manual_seed(T + D + a)
+    x = torch.randn(T, D, generator=g).to(torch.bfloat16)
+    s = torch.rand(T, E, generator=g)                      # f32 scores this time
+    ti = torch.randint(0, T, (a,), generator=g, dtype=torch.int32)
+    ei = torch.randint(0, E, (a,), generator=g, dtype=torch.int32)
+    out = mb.moe_gather_scale(x.cuda(), ti.cuda(), ei.cuda(), s.cuda())
+    np.testing.assert_array_equal(bits(out), oracle.gather_scale(bits(x), ti.numpy(), ei.numpy(), s.numpy()))
+    q, sc = mb.moe_gather_scale_quant(x.cuda(), ti.cuda(), ei.cuda(), s.cuda())
+    q_ref, sc_ref = oracle.gather_scale_quant(bits(x), ti.numpy(), ei.numpy(), s.numpy())
+    np.testing.assert_array_equal(bits(q), q_ref)
+    np.testing.assert_array_equal(sc.cpu().numpy(), sc_ref)
+
+
+def test_gather_bad_index_is_skipped_and_flagged():
+    mb = _mb()
+    x = torch.randn(4, 32).to(torch.bfloat16).cuda()
+    s = torch.rand(4, 2).cuda()
+    ti = torch.tensor([0, 9, 1], dtype=torch.int32, device="cuda")
+    ei = torch.tensor([0, 1, 5], dtype=torch.int32, device="cuda")
+    out = sentinel_like((3, 32), torch.bfloat16)
+    mb.moe_gather_scale(x, ti, ei, s, out=out)
+    assert mb.device_error() & mb.MOE_DEVERR_BAD_INDEX
+    assert is_sentinel(out[1:]) and not is_sentinel(out[:1])
+
+
+def _y_rows(a, H, seed, scale=2.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(a, 2 * H, generator=g) * scale).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("a,H,valid", [(64, 512, 64), (8192, 8192, 8192), (32768, 2048, 30000), (7, 16, 5),
+                                       (33, 1552, 20)])
+def test_silu_mul_within_one_bf16_step(a, H, valid):
+    mb = _mb()
+    y = _y_rows(a, H, a + H)
+    out = sentinel_like((a, H), torch.bfloat16)
+    mb.moe_silu_mul(y.cuda(), H, torch.tensor([valid], dtype=torch.int32, device="cuda"), out=out)
+    ref = oracle.silu_mul(bits(y), H, valid)
+    got = bits(out[:valid]).astype(np.int32)
+    diff = np.abs(got - ref[:valid].astype(np.int32))
+    assert diff.max() <= 1 and (diff == 0).mean() > 0.999
+    assert is_sentinel(out[valid:])
+
+
+@pytest.mark.parametrize("a,H,valid,ub", [(8192, 8192, 8192, 1200.0), (65536, 1536, 44000, None), (9, 48, 9, 0.25),
+                                          (20, 16384, 17, None)])
+def test_silu_mul_quant_within_one_e4m3_step(a, H, valid, ub):
+    mb = _mb()
+    y = _y_rows(a, H, a + 3 * H)
+    ub_t = None if ub is None else torch.tensor([ub], dtype=torch.float32, device="cuda")
+    out = sentinel_like((a, H), torch.float8_e4m3fn)
+    osc = sentinel_like((a,), torch.float32)
+    mb.moe_silu_mul_quant(y.cuda(), H, ub_t, torch.tensor([valid], dtype=torch.int32, device="cuda"), out=out,
+                          out_scale=osc)
+    q_ref, s_ref = oracle.silu_mul_quant(bits(y), H, ub, valid)
+    steps = e4m3_step_diff(bits(out[:valid]), q_ref[:valid])
+    assert steps.max() <= 1 and (steps == 0).mean() > 0.999
+    np.testing.assert_allclose(osc[:valid].cpu().numpy(), s_ref[:valid], rtol=1e-6)
+    assert is_sentinel(out[valid:]) and is_sentinel(osc[valid:])
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill_fp8", "fine_grained", "padded_fp8"])
+@pytest.mark.parametrize("use_inv", [True, False])
+def test_scatter_add_bit_exact(name, use_inv):
+    mb = _mb()
+    cfg = workloads.CONFIGS[name]
+    if cfg.top_k > 1 and not use_inv:
+        pytest.skip("top_k > 1 needs the inverse permutation")
+    s = workloads.make_scores(cfg)
+    r = oracle.route(bits(s), cfg.top_k, cfg.valid_tokens)
+    a = len(r["token_indices"])
+    g = torch.Generator().manual_seed(a)
+    rows = torch.randn(a, cfg.D, generator=g).to(torch.bfloat16)
+    init = torch.randn(cfg.T, cfg.D, generator=g).to(torch.bfloat16)
+    out = init.cuda()
+    valid = torch.tensor([a], dtype=torch.int32, device="cuda")
+    inv = _idx(r["inv"].ravel()) if use_inv else None
+    mb.moe_scatter_add(out, rows.cuda(), _idx(r["token_indices"]), inv, cfg.top_k, valid)
+    assert mb.device_error() == 0
+    ref = oracle.scatter_add(bits(init).copy(), bits(rows), r["token_indices"])
+    np.testing.assert_array_equal(bits(out), ref)
+    Tv = cfg.valid_tokens
+    assert torch.equal(out[Tv:].cpu(), init[Tv:]), "tokens past the valid count stay as they were"
