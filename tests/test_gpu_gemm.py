@@ -1,0 +1,174 @@
+"""The tcgen05 grouped GEMMs (bf16 and FP8 rowwise) against the oracle.
+
+Tolerance: the kernel accumulates in fp32 on the tensor cores, the oracle in
+fp64; both round once to bf16.  So an output may differ from the oracle by one
+bf16 step of the result plus the fp32 accumulation error, bounded by
+2^-20 * sum_k |x_k w_k| (K terms, each addition off by at most 2^-24 relative,
+with ample slack).  The fused SiLU*mul epilogue must equal the unfused GEMM
+followed by moe_silu_mul bit for bit (same accumulators, same arithmetic).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_token_routing_index_gb300 import workloads
+from tests.helpers import bits, dev_bf16, dev_e4m3, f64, is_sentinel, sentinel_like
+
+pytestmark = pytest.mark.gpu
+
+
+def _mb():
+    from moe_token_routing_index_gb300 import binding
+
+    return binding
+
+
+def _bf16_ulp(v: np.ndarray) -> np.ndarray:
+    a = np.abs(v).astype(np.float64)
+    e = np.floor(np.log2(np.where(a > 0, a, 1e-38)))
+    return np.exp2(e - 7)
+
+
+def _check_close(got_bits, ref_bits, abs_bound, min_exact=0.9):
+    got, ref = f64(got_bits), f64(ref_bits)
+    err = np.abs(got - ref)
+    tol = _bf16_ulp(ref) + abs_bound
+    bad = err > tol
+    assert not bad.any(), f"{bad.sum()} of {bad.size} outside tolerance; worst {err[bad].max():.3e}"
+    assert (err == 0).mean() >= min_exact, f"only {(err == 0).mean():.4f} bit-exact"
+
+
+def _abs_bound_bf16(x_bits, w_bits, counts, rows=None):
+    """2^-20 * sum_k |x_rk w_enk| for every output (r, n), per expert segment."""
+    xa, wa = np.abs(f64(x_bits)), np.abs(f64(w_bits))
+    out = np.zeros((x_bits.shape[0], w_bits.shape[1]))
+    off = 0
+    for e, c in enumerate(counts):
+        out[off:off + c] = xa[off:off + c] @ wa[e].T
+        off += c
+    return 2.0 ** -20 * out
+
+
+def _problem(E, counts, N, K, a_max=None, seed=0, std=0.05):
+    g = torch.Generator().manual_seed(seed)
+    a = int(sum(counts))
+    a_max = a if a_max is None else a_max
+    x = torch.randn(a_max, K, generator=g).to(torch.bfloat16)
+    w = (torch.randn(E, N, K, generator=g) * std).to(torch.bfloat16)
+    return x, w, np.array(counts, np.int32), a
+
+
+SHAPES = [
+    # E, counts, N, K, a_max
+    (1, [128], 256, 64, None),          # one tile, one K block
+    (3, [5, 0, 130], 256, 64, None),    # ragged experts, an empty expert
+    (2, [77, 200], 512, 320, None),     # several N tiles and K blocks
+    (4, [1, 0, 0, 129], 48, 80, 300),   # partial N tile, K tail, rows past the counts
+    (5, [300, 17, 0, 64, 250], 1040, 272, 700),
+]
+
+
+@pytest.mark.parametrize("E,counts,N,K,a_max", SHAPES)
+def test_grouped_gemm_bf16(E, counts, N, K, a_max):
+    mb = _mb()
+    x, w, cnt, a = _problem(E, counts, N, K, a_max, seed=N + K)
+    y = sentinel_like((x.shape[0], N), torch.bfloat16)
+    mb.moe_grouped_gemm(x.cuda(), w.cuda(), torch.from_numpy(cnt).cuda(), out=y)
+    assert mb.device_error() == 0
+    ref = oracle.grouped_gemm_bf16(bits(x[:a]), bits(w), cnt)
+    _check_close(bits(y[:a]), ref, _abs_bound_bf16(bits(x[:a]), bits(w), cnt))
+    assert is_sentinel(y[a:])
+
+
+@pytest.mark.parametrize("E,counts,N,K,a_max", SHAPES)
+def test_fused_silu_mul_equals_unfused(E, counts, N, K, a_max):
+    if N % 32:
+        pytest.skip("SiLU*mul needs N = 2H with H a multiple of 16")
+    mb = _mb()
+    x, w, cnt, a = _problem(E, counts, N, K, a_max, seed=3 * N + K, std=0.2)
+    xd, wd, cd = x.cuda(), w.cuda(), torch.from_numpy(cnt).cuda()
+    H = N // 2
+    y = mb.moe_grouped_gemm(xd, wd, cd)
+    z_unfused = mb.moe_silu_mul(y[:a].contiguous(), H)
+    z = sentinel_like((x.shape[0], H), torch.bfloat16)
+    mb.moe_grouped_gemm(xd, wd, cd, epilogue=mb.MOE_EPILOGUE_SILU_MUL, out=z)
+    assert mb.device_error() == 0
+    assert torch.equal(z[:a], z_unfused)
+    assert is_sentinel(z[a:])
+
+
+def test_all_experts_empty_is_a_no_op():
+    mb = _mb()
+    x, w, cnt, a = _problem(3, [0, 0, 0], 64, 64, 50)
+    y = sentinel_like((50, 64), torch.bfloat16)
+    mb.moe_grouped_gemm(x.cuda(), w.cuda(), torch.from_numpy(cnt).cuda(), out=y)
+    assert mb.device_error() == 0 and is_sentinel(y)
+
+
+@pytest.mark.parametrize("E,counts,N,K,a_max", SHAPES)
+def test_grouped_gemm_fp8(E, counts, N, K, a_max):
+    mb = _mb()
+    x, w, cnt, a = _problem(E, counts, N, K, a_max, seed=5 * N + K)
+    xq, xs = oracle.gather_scale_quant(bits(x), np.arange(x.shape[0], dtype=np.int32),
+                                       np.zeros(x.shape[0], np.int32), bits(torch.ones(x.shape[0], 1,
+                                                                                       dtype=torch.bfloat16)))
+    wq, ws = oracle.quantize_rows(w.float().numpy())
+    y = sentinel_like((x.shape[0], N), torch.bfloat16)
+    mb.moe_grouped_gemm_fp8_rowwise(dev_e4m3(xq), dev_e4m3(wq), torch.from_numpy(cnt).cuda(),
+                                    torch.from_numpy(xs).cuda(), torch.from_numpy(ws).cuda(), out=y)
+    assert mb.device_error() == 0
+    ref = oracle.grouped_gemm_fp8(xq[:a], wq, cnt, xs[:a], ws)
+    dx = oracle.e4m3_decode(xq[:a]).astype(np.float64)
+    dw = oracle.e4m3_decode(wq).astype(np.float64)
+    bound = np.zeros((a, N))
+    off = 0
+    for e, c in enumerate(cnt):
+        bound[off:off + c] = (np.abs(dx[off:off + c]) @ np.abs(dw[e]).T) * xs[off:off + c, None] * ws[e][None, :]
+        off += c
+    _check_close(bits(y[:a]), ref, 2.0 ** -20 * bound)
+    assert is_sentinel(y[a:])
+    if N % 32 == 0:
+        z = mb.moe_grouped_gemm_fp8_rowwise(dev_e4m3(xq), dev_e4m3(wq), torch.from_numpy(cnt).cuda(),
+                                            torch.from_numpy(xs).cuda(), torch.from_numpy(ws).cuda(),
+                                            epilogue=mb.MOE_EPILOGUE_SILU_MUL)
+        assert torch.equal(z[:a], mb.moe_silu_mul(y[:a].contiguous(), N // 2))
+
+
+def _sample_rows(cnt, rng, per_expert=3):
+    """First, last and a few random rows of every non-empty expert (sorted)."""
+    rows, off = [], 0
+    for c in cnt:
+        if c:
+            rows += [off, off + c - 1] + list(rng.integers(off, off + c, per_expert))
+        off += c
+    return np.unique(np.array(rows, np.int64))
+
+
+@pytest.mark.parametrize("name", ["decode", "decode_zero", "fine_grained"])
+def test_grouped_gemm_bf16_workloads_sampled(name):
+    """Full-size w13 and w2 GEMMs of the bf16 workloads; oracle on sampled rows."""
+    mb = _mb()
+    cfg = workloads.CONFIGS[name]
+    s = workloads.make_scores(cfg)
+    r = oracle.route(bits(s), cfg.top_k, cfg.valid_tokens)
+    cnt = r["counts"][:cfg.E]
+    a = int(cnt.sum())
+    g = torch.Generator().manual_seed(11)
+    x = torch.randn(a, cfg.D, generator=g).to(torch.bfloat16)
+    w13, w2 = workloads.make_weights(cfg, device="cuda")
+    cd = torch.from_numpy(cnt).cuda()
+    y = mb.moe_grouped_gemm(x.cuda(), w13, cd)
+    z = mb.moe_grouped_gemm(x.cuda(), w13, cd, epilogue=mb.MOE_EPILOGUE_SILU_MUL)
+    o = mb.moe_grouped_gemm(z, w2, cd)
+    assert mb.device_error() == 0
+    rows = _sample_rows(cnt, np.random.default_rng(0))
+    exp_of_row = np.repeat(np.arange(cfg.E), cnt)[rows]
+    used = sorted(set(exp_of_row.tolist()))
+    sub_cnt = np.array([(exp_of_row == e).sum() for e in used], np.int32)
+    w13_u, w2_u = bits(w13[used]), bits(w2[used])
+    y_ref = oracle.grouped_gemm_bf16(bits(x)[rows], w13_u, sub_cnt)
+    _check_close(bits(y[rows]), y_ref, _abs_bound_bf16(bits(x)[rows], w13_u, sub_cnt))
+    assert torch.equal(z, mb.moe_silu_mul(y, cfg.H))
+    o_ref = oracle.grouped_gemm_bf16(bits(z)[rows], w2_u, sub_cnt)
+    _check_close(bits(o[rows]), o_ref, _abs_bound_bf16(bits(z)[rows], w2_u, sub_cnt))
