@@ -1,0 +1,448 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 routed-expert MoE forward.
+
+One step = one whole forward (route -> gather -> grouped GEMM w13 -> SiLU*mul
+-> grouped GEMM w2 -> scatter-add) over one batch of the workload, with the
+inputs resident in HBM.  Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Default workload: the decode-shaped layer (T=128, D=5120, H=8192, E=16,
+top_k=1, bf16).  --config prefill_fp8 | fine_grained | padded_fp8 | tiny |
+decode_zero measures the other workloads.  Under torchrun (N > 1) every rank
+runs an independent replica on its own GPU (no data-path collective); the
+timing is the max over ranks and the value counts the tokens of all ranks.
+
+--impl reference times the CPU oracle (the plain reference implementation of
+the method, on the host cores) on bounded token samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "routed-MoE tokens/s; gather/scatter HBM GB/s; grouped-GEMM TFLOP/s (1 GB300)"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 4.5 / 2.25   # nominal dense FP8 : BF16 tensor-core ratio
+
+
+def load_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_desc(cfg):
+    tv = f" Tv={cfg.Tv}" if cfg.Tv is not None else ""
+    prec = "fp8-rowwise e4m3" if cfg.fp8 else "bf16"
+    ub = f" scale_ub={cfg.scale_ub:g}" if cfg.scale_ub else ""
+    skew = {"uniform": "uniform routing", "zipf": "Zipf(1.1)-skewed routing",
+            "zero_experts": f"experts {list(cfg.zero_experts)} get no token"}[cfg.skew]
+    return f"{cfg.name}: T={cfg.T}{tv} D={cfg.D} H={cfg.H} E={cfg.E} top_k={cfg.top_k} {prec}{ub}, {skew}"
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of the SM clock and throttle reasons."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.rows, self.proc, self.thread = [], None, None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+        if gpu_id is not None:
+            cmd += ["-i", gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 9:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def gpu_id_for(dev) -> str | None:
+    import torch
+
+    try:
+        props = torch.cuda.get_device_properties(dev)
+        return f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def _host_bits(t):
+    import numpy as np
+    import torch
+
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def oracle_tokens_per_s(cfg, x, s, w13, w2, seconds: float, max_tokens: int | None = None):
+    """Time the oracle's forward (as it stands) on a bounded sample of tokens.
+
+    Returns (tokens/s, tokens in the sample, threads, wall seconds).  The
+    sample is the first n valid tokens, n grown until about `seconds` of work.
+    """
+    import numpy as np
+
+    import oracle
+
+    xb, sb = _host_bits(x), _host_bits(s)
+    Tv = cfg.valid_tokens
+    cache = {}
+
+    def weights(ids):
+        missing = [e for e in ids if e not in cache]
+        if missing:
+            if cfg.fp8:
+                a13, a2 = w13[missing].float().cpu().numpy(), w2[missing].float().cpu().numpy()
+            else:
+                a13, a2 = _host_bits(w13[missing]), _host_bits(w2[missing])
+            for i, e in enumerate(missing):
+                cache[e] = (a13[i], a2[i])
+        return np.stack([cache[e][0] for e in ids]), np.stack([cache[e][1] for e in ids])
+
+    n = 1
+    limit = Tv if max_tokens is None else min(Tv, max_tokens)
+    while True:
+        toks = np.arange(n)
+        weights(sorted(set(oracle.route(sb[toks], cfg.top_k)["expert_indices"].tolist())))  # warm the copy
+        t0 = time.perf_counter()
+        oracle.moe_forward_tokens(toks, xb, sb, cfg.top_k, weights, fp8=cfg.fp8, scale_ub=cfg.scale_ub)
+        dt = time.perf_counter() - t0
+        if dt >= 0.3 * seconds or n >= limit:
+            break
+        n = int(min(limit, max(n + 1, seconds / max(dt / n, 1e-6))))
+    done, total = n, dt
+    while total < 0.8 * seconds:          # a small workload is repeated until the sample is long enough
+        t0 = time.perf_counter()
+        oracle.moe_forward_tokens(toks, xb, sb, cfg.top_k, weights, fp8=cfg.fp8, scale_ub=cfg.scale_ub)
+        total += time.perf_counter() - t0
+        done += n
+    return done / total, n, oracle.num_threads(), total
+
+
+# ------------------------------------------------------------- our arm
+
+def run_ours(args, cfg):
+    import torch
+    import torch.distributed as dist
+
+    from moe_token_routing_index_gb300 import binding as mb
+    from moe_token_routing_index_gb300 import workloads
+    from moe_token_routing_index_gb300.forward import MoELayer
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    # inputs: seeded per rank (replicas process different batches of the same shape)
+    x = workloads.make_tokens(cfg, seed=rank).to(dev)
+    s = workloads.make_scores(cfg, seed=rank).to(dev)
+    w13, w2 = workloads.make_weights(cfg, seed=0, device=dev)
+    layer = MoELayer.from_weights(cfg, w13, w2)
+    nv = None if cfg.Tv is None else torch.tensor([cfg.Tv], dtype=torch.int32, device=dev)
+    out = torch.zeros(cfg.T, cfg.D, dtype=torch.bfloat16, device=dev)
+    stages = layer.stages(x, s, nv, out, accumulate=False)
+    names = [n for n, _ in stages]
+
+    def step(ev=None):
+        for i, (_, launch) in enumerate(stages):
+            if ev is not None:
+                ev[i][0].record()
+            launch()
+            if ev is not None:
+                ev[i][1].record()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if mb.device_error() != 0:
+        raise RuntimeError("device-side error during warm-up")
+    counts = layer.buffers(cfg.T, dev).route["counts"].cpu().tolist()
+
+    K = args.steps
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in stages] for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_id_for(dev))
+    time.sleep(0.25)
+    t_start.record()
+    for k in range(K):
+        step(ev[k])
+    t_end.record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    ms = t_start.elapsed_time(t_end) / K
+    stage_ms = {n: statistics.fmean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(K))
+                for i, n in enumerate(names)}
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if mb.device_error() != 0:
+        raise RuntimeError("device-side error during the timed steps")
+
+    # end to end through the public API: pinned host inputs in, result out, every step
+    xh = x.cpu().pin_memory()
+    sh = s.cpu().pin_memory()
+    nvh = None if nv is None else nv.cpu().pin_memory()
+    outh = torch.empty(cfg.T, cfg.D, dtype=torch.bfloat16).pin_memory()
+    xd, sd = torch.empty_like(x), torch.empty_like(s)
+    nvd = None if nv is None else torch.empty_like(nv)
+    outd = torch.zeros_like(out)
+
+    def e2e_step():
+        xd.copy_(xh, non_blocking=True)
+        sd.copy_(sh, non_blocking=True)
+        if nvd is not None:
+            nvd.copy_(nvh, non_blocking=True)
+        layer(xd, sd, nvd, out=outd)
+        outh.copy_(outd, non_blocking=True)
+
+    for _ in range(max(2, min(args.warmup, 10))):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    e_start.record()
+    for _ in range(K):
+        e2e_step()
+    e_end.record()
+    torch.cuda.synchronize()
+    e2e_ms = e_start.elapsed_time(e_end) / K
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = xh.numel() * xh.element_size() + sh.numel() * sh.element_size() + (0 if nvh is None else 4)
+    d2h = outh.numel() * outh.element_size()
+
+    result = None
+    if rank == 0:
+        result = report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, layer)
+        if not args.no_cpu_baseline and world == 1:
+            tps, n, cores, dt = oracle_tokens_per_s(cfg, x, s, w13, w2, args.cpu_seconds)
+            result["cpu_baseline"] = {"value": round(tps, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+                                      "sample": f"first {n} valid tokens of the workload (repeated to {dt:.1f} s of wall time)"}
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
+def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, layer):
+    peaks, peak_kind = load_peaks()
+    E, D, H, k = cfg.E, cfg.D, cfg.H, cfg.top_k
+    a = cfg.routed_rows
+    active = sum(1 for c in counts[:E] if c > 0)
+    wb = 1 if cfg.fp8 else 2        # weight / activation element bytes into the GEMMs
+    tokens = cfg.valid_tokens * world
+    value = tokens / (ms * 1e-3)
+
+    # algorithmic work per stage (one launch each per step)
+    gemm1 = "gemm_w13" if cfg.fp8 else "gemm_w13_silu"
+    work = {
+        "route": ("hbm", cfg.valid_tokens * E * 2 + a * 12 + 8 * (E + 1)),
+        ("gather_quant" if cfg.fp8 else "gather"): ("hbm", cfg.valid_tokens * D * 2 + a * D * wb + a * (14 if cfg.fp8 else 10)),
+        gemm1: ("gemm", active * 2 * H * D * wb + a * D * wb + a * (2 * H * 2 if cfg.fp8 else H * 2),
+                2.0 * a * 2 * H * D),
+        "gemm_w2": ("gemm", active * D * H * wb + a * H * wb + a * D * 2, 2.0 * a * D * H),
+        "scatter": ("hbm", a * D * 2 + cfg.valid_tokens * D * 2 + (a * 4 if k > 1 else 0)),
+    }
+    if cfg.fp8:
+        work["silu_quant"] = ("hbm", a * 2 * H * 2 + a * H + a * 4)
+    peak_t = peaks["bf16_tflops_sustained"] * (FP8_OVER_BF16 if cfg.fp8 else 1.0)
+    stages = {}
+    for name, t in stage_ms.items():
+        kind, *w = work[name]
+        d = {"us": round(t * 1e3, 2)}
+        if kind == "hbm":
+            d["GB/s"] = round(w[0] / (t * 1e-3) / 1e9, 1)
+            d["hbm_frac"] = round(d["GB/s"] / peaks["hbm_gbs"], 3)
+        else:
+            d["GB/s"] = round(w[0] / (t * 1e-3) / 1e9, 1)
+            d["TFLOP/s"] = round(w[1] / (t * 1e-3) / 1e12, 1)
+            d["hbm_frac"] = round(d["GB/s"] / peaks["hbm_gbs"], 3)
+            d["tensor_frac"] = round(d["TFLOP/s"] / peak_t, 3)
+        stages[name] = d
+    dom = max(stage_ms, key=stage_ms.get)
+    kind, *w = work[dom]
+    t_dom = stage_ms[dom] * 1e-3
+    if kind == "gemm" and w[1] / (peak_t * 1e12) > w[0] / (peaks["hbm_gbs"] * 1e9):
+        roof = {"bound": "tensor", "achieved": round(w[1] / t_dom / 1e12, 1), "peak": round(peak_t, 1),
+                "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": round(w[0] / t_dom / 1e9, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["kernel"] = dom
+    roof["peak_source"] = f"{peak_kind} ({'sustained bf16 x nominal fp8/bf16 ratio' if cfg.fp8 and roof['bound'] == 'tensor' else 'MEASURED_PEAKS.json'})"
+    roof["traffic"] = TRAFFIC.get((cfg.name, dom))
+    roof["algorithmic_bytes"] = int(w[0])
+    if kind == "gemm":
+        roof["algorithmic_flops"] = w[1]
+
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3" if cfg.fp8 else "bf16",
+        "data": "synthetic, seeded: x~N(0,1), scores=bf16(sigmoid(N(0,1) logits)), expert weights N(0,0.02) random init",
+        "config": {"workload": workload_desc(cfg), "T": cfg.T, "valid_tokens": cfg.valid_tokens, "D": D, "H": H,
+                   "E": E, "top_k": k, "routed_rows": a, "active_experts": active,
+                   "l2": "inputs larger than L2: each step streams the active experts' weights "
+                         f"({(active * 3 * H * D * wb) / 1e9:.2f} GB) from HBM",
+                   "parallelism": "replicas" if world == 1 else f"{world} independent replicas (weak scaling)"},
+        "roofline": roof,
+        "stages": stages,
+        "gemm_tflops": round(sum(work[n][2] for n in (gemm1, "gemm_w2")) /
+                             (sum(stage_ms[n] for n in (gemm1, "gemm_w2")) * 1e-3) / 1e12, 1),
+        "e2e": {"value": round(tokens / (e2e_ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": layer.kernel_launches() * args.steps,
+        "clocks": clocks,
+    }
+    return res
+
+
+# ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, from the captures
+# summarised under profiles/ (None until captured for the current kernel).
+TRAFFIC: dict = {}
+
+
+# ------------------------------------------------------- reference arm
+
+def run_reference(args, cfg):
+    """The CPU oracle, as it stands, on the host cores: each step is a bounded
+    token sample of the workload; rank 0 only."""
+    import torch
+
+    from moe_token_routing_index_gb300 import workloads
+
+    if int(os.environ.get("RANK", "0")) != 0:
+        return None
+    import oracle
+
+    x = workloads.make_tokens(cfg)
+    s = workloads.make_scores(cfg)
+    w13, w2 = workloads.make_weights(cfg, device="cuda" if torch.cuda.is_available() else "cpu")
+    budget = 150.0                                  # seconds for the whole --steps/--warmup run
+    tps, n, cores, dt = oracle_tokens_per_s(cfg, x, s, w13, w2, min(10.0, budget / (args.steps + args.warmup)))
+    per_tok = dt / n
+    n_step = int(max(1, min(cfg.valid_tokens, budget / (args.steps + args.warmup) / per_tok)))
+    xb, sb = _host_bits(x), _host_bits(s)
+    import numpy as np
+
+    cache = {}
+
+    def weights(ids):
+        missing = [e for e in ids if e not in cache]
+        if missing:
+            a13 = w13[missing].float().cpu().numpy() if cfg.fp8 else _host_bits(w13[missing])
+            a2 = w2[missing].float().cpu().numpy() if cfg.fp8 else _host_bits(w2[missing])
+            for i, e in enumerate(missing):
+                cache[e] = (a13[i], a2[i])
+        return np.stack([cache[e][0] for e in ids]), np.stack([cache[e][1] for e in ids])
+
+    Tv = cfg.valid_tokens
+
+    def step(i):
+        toks = (np.arange(n_step) + i * n_step) % Tv
+        oracle.moe_forward_tokens(np.unique(toks), xb, sb, cfg.top_k, weights, fp8=cfg.fp8, scale_ub=cfg.scale_ub)
+        return len(np.unique(toks))
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    done = sum(step(args.warmup + i) for i in range(args.steps))
+    dt = time.perf_counter() - t0
+    value = done / dt
+    res = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 accumulate",
+        "data": "synthetic, seeded (same workload generator as the GPU arm)",
+        "config": {"workload": workload_desc(cfg), "sample_tokens_per_step": n_step},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"{n_step} valid tokens per step (of {Tv}), tokens cycling through the workload"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(res), flush=True)
+    return res
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=500)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--config", default="decode")
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU-baseline leg")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work of the oracle baseline sample")
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be at least 3")
+    from moe_token_routing_index_gb300 import workloads
+
+    cfg = workloads.CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

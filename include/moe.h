@@ -221,8 +221,10 @@ int moe_silu_mul_quant(const void* x0, const void* x1, int64_t ld, int a, int H,
  * scatter_add_dense_tokens (mslk/moe/gather_scatter.py,
  * _mslk_scatter_add_dense_tokens), made deterministic: every routed row
  * r < valid is added into out[token_indices[r], :].  Each output token is
- * owned by one warp: acc = f32(out[t, :]); acc += f32(in[r, :]) for t's rows
- * in ascending r; out[t, :] = bf16(acc).  No atomics.
+ * owned by one warp: acc = f32(out[t, :]) (accumulate != 0) or 0
+ * (accumulate == 0: the routed sum overwrites out, as adding into zeros
+ * would); acc += f32(in[r, :]) for t's rows in ascending r;
+ * out[t, :] = bf16(acc).  No atomics.
  * out [T, D] bf16 (read and written); in [a, D] bf16; token_indices [a].
  * inv_rows [Tv * top_k] from moe_route (t's rows, ascending) is required when
  * top_k > 1; with top_k == 1 it may be NULL (row r then owns its token).
@@ -231,7 +233,7 @@ int moe_silu_mul_quant(const void* x0, const void* x1, int64_t ld, int a, int H,
  */
 int moe_scatter_add(void* out, const void* in, const int32_t* token_indices,
                     const int32_t* inv_rows, int top_k, int a, int T, int D,
-                    const int32_t* valid_token_count, cudaStream_t stream);
+                    const int32_t* valid_token_count, int accumulate, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

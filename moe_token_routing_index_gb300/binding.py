@@ -53,7 +53,7 @@ def _load() -> ctypes.CDLL:
         "moe_grouped_gemm_fp8_rowwise": ([P, P, P, P, P, I, I, I, I, P, I, P], I),
         "moe_silu_mul": ([P, P, L, I, I, P, P, P], I),
         "moe_silu_mul_quant": ([P, P, L, I, I, P, P, P, P, P], I),
-        "moe_scatter_add": ([P, P, P, P, I, I, I, I, P, P], I),
+        "moe_scatter_add": ([P, P, P, P, I, I, I, I, P, I, P], I),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(lib, name)
@@ -260,13 +260,14 @@ def moe_silu_mul_quant(y, H: int | None = None, scale_ub=None, valid_rows=None, 
 # -------------------------------------------------------------- scatter-add
 
 def moe_scatter_add(out, rows, token_indices, inv_rows=None, top_k: int = 1, valid_token_count=None, *,
-                    stream=None):
-    """out[T, D] += rows[a, D] by token, in place (deterministic)."""
+                    accumulate: bool = True, stream=None):
+    """out[T, D] += rows[a, D] by token, in place (deterministic); with
+    accumulate=False the routed sum overwrites the valid tokens of out."""
     T, D = out.shape
     a = rows.shape[0]
     _need(out, torch.bfloat16, "out")
     _need(rows, torch.bfloat16, "rows")
     st = _lib.moe_scatter_add(_ptr(out), _ptr(rows), _ptr(token_indices), _ptr(inv_rows), top_k, a, T, D,
-                              _ptr(valid_token_count), _stream(stream))
+                              _ptr(valid_token_count), int(accumulate), _stream(stream))
     _check("moe_scatter_add", st)
     return out

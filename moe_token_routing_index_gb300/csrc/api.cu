@@ -207,14 +207,14 @@ int moe_silu_mul_quant(const void* x0, const void* x1, int64_t ld, int a, int H,
 }
 
 int moe_scatter_add(void* out, const void* in, const int32_t* token_indices, const int32_t* inv_rows, int top_k,
-                    int a, int T, int D, const int32_t* valid_token_count, cudaStream_t stream) {
+                    int a, int T, int D, const int32_t* valid_token_count, int accumulate, cudaStream_t stream) {
   if (a < 0 || T < 0 || D < 0 || top_k < 1) return MOE_ERR_INVALID;
   if (a == 0 || D == 0 || T == 0) return MOE_OK;
   if (!out || !in) return MOE_ERR_INVALID;
   if (top_k > 1 && !inv_rows) return MOE_ERR_INVALID;
   if (!inv_rows && !token_indices) return MOE_ERR_INVALID;
   if (D % 16 != 0 || !aligned16(out) || !aligned16(in)) return MOE_ERR_UNSUPPORTED;
-  moe::ScatterArgs g{out, in, token_indices, inv_rows, top_k, a, T, D, valid_token_count, nullptr};
+  moe::ScatterArgs g{out, in, token_indices, inv_rows, top_k, a, T, D, valid_token_count, accumulate != 0, nullptr};
   int rc = device_error_word(&g.err);
   if (rc != MOE_OK) return rc;
   return finish(moe::launch_scatter_add(g, stream));

@@ -70,6 +70,7 @@ struct ScatterArgs {
   const int32_t* inv;
   int top_k, a, T, D;
   const int32_t* valid;
+  bool accumulate;
   unsigned int* err;
 };
 

@@ -243,6 +243,7 @@ __global__ void __launch_bounds__(kThreads) silu_mul_quant_kernel(const __nv_bfl
 // ------------------------------------------------------------- scatter-add
 
 // top_k == 1 without the inverse permutation: routed row r owns token ti[r].
+template <bool ACC>
 __global__ void __launch_bounds__(kThreads) scatter_add_rows_kernel(uint4* __restrict__ out,
                                                                     const uint4* __restrict__ in,
                                                                     const int32_t* __restrict__ ti, int a, int T,
@@ -263,25 +264,31 @@ __global__ void __launch_bounds__(kThreads) scatter_add_rows_kernel(uint4* __res
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u)
         if (c0 + 32 * u < D8) {
-          vo[u] = o[c0 + 32 * u];
+          if (ACC) vo[u] = o[c0 + 32 * u];
           vi[u] = __ldg(src + c0 + 32 * u);
         }
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         if (c0 + 32 * u >= D8) break;
-        float fo[8], fi[8];
-        bf16x8_to_f32(vo[u], fo);
-        bf16x8_to_f32(vi[u], fi);
+        if (ACC) {
+          float fo[8], fi[8];
+          bf16x8_to_f32(vo[u], fo);
+          bf16x8_to_f32(vi[u], fi);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) fo[i] = __fadd_rn(fo[i], fi[i]);
-        o[c0 + 32 * u] = f32_to_bf16x8(fo);
+          for (int i = 0; i < 8; ++i) fo[i] = __fadd_rn(fo[i], fi[i]);
+          o[c0 + 32 * u] = f32_to_bf16x8(fo);
+        } else {
+          o[c0 + 32 * u] = vi[u];  // bf16(0 + x) = x
+        }
       }
     }
   }
 }
 
 // With the inverse permutation: one warp owns token t and adds its top_k rows
-// in ascending row order into an fp32 accumulator started from out[t].
+// in ascending row order into an fp32 accumulator started from out[t] (ACC)
+// or from zero.
+template <bool ACC>
 __global__ void __launch_bounds__(kThreads) scatter_add_tokens_kernel(uint4* __restrict__ out,
                                                                       const uint4* __restrict__ in,
                                                                       const int32_t* __restrict__ inv, int k, int a,
@@ -308,8 +315,14 @@ __global__ void __launch_bounds__(kThreads) scatter_add_tokens_kernel(uint4* __r
     for (int c0 = lane; c0 < D8; c0 += 32 * 2) {
       float acc[2][8];
 #pragma unroll
-      for (int u = 0; u < 2; ++u)
-        if (c0 + 32 * u < D8) bf16x8_to_f32(o[c0 + 32 * u], acc[u]);
+      for (int u = 0; u < 2; ++u) {
+        if (ACC && c0 + 32 * u < D8) {
+          bf16x8_to_f32(o[c0 + 32 * u], acc[u]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
+        }
+      }
       for (int j = 0; j < k; ++j) {
         const int r = (j < 32) ? __shfl_sync(0xffffffffu, my_row, j) : __ldg(inv + (int64_t)t * k + j);
         if ((unsigned)r >= (unsigned)a) {  // only reachable for top_k > 32
@@ -400,13 +413,14 @@ cudaError_t launch_scatter_add(const ScatterArgs& g, cudaStream_t s) {
   const int D8 = g.D / 8;
   if (g.inv) {
     const int grid = persistent_grid(g.T, kWarps);
-    scatter_add_tokens_kernel<<<grid, kThreads, 0, s>>>(static_cast<uint4*>(g.out),
-                                                        static_cast<const uint4*>(g.in), g.inv, g.top_k, g.a, g.T,
-                                                        D8, g.valid, g.err);
+    auto k = g.accumulate ? scatter_add_tokens_kernel<true> : scatter_add_tokens_kernel<false>;
+    k<<<grid, kThreads, 0, s>>>(static_cast<uint4*>(g.out), static_cast<const uint4*>(g.in), g.inv, g.top_k, g.a,
+                                g.T, D8, g.valid, g.err);
   } else {
     const int grid = persistent_grid(g.a, kWarps);
-    scatter_add_rows_kernel<<<grid, kThreads, 0, s>>>(static_cast<uint4*>(g.out), static_cast<const uint4*>(g.in),
-                                                      g.token_indices, g.a, g.T, D8, g.valid, g.err);
+    auto k = g.accumulate ? scatter_add_rows_kernel<true> : scatter_add_rows_kernel<false>;
+    k<<<grid, kThreads, 0, s>>>(static_cast<uint4*>(g.out), static_cast<const uint4*>(g.in), g.token_indices, g.a,
+                                g.T, D8, g.valid, g.err);
   }
   return cudaGetLastError();
 }

@@ -304,7 +304,7 @@ void oracle_grouped_gemm_bf16(const uint16_t* x, const uint16_t* w, const int32_
     int64_t off = 0;
     for (int e = 0; e < E; ++e) {
         int64_t cnt = counts[e];
-#pragma omp parallel for schedule(dynamic, 1)
+#pragma omp parallel for collapse(2) schedule(static)
         for (int64_t r = off; r < off + cnt; ++r) {
             for (int n = 0; n < N; ++n) {
                 const uint16_t* wr = w + ((int64_t)e * N + n) * K;
@@ -331,7 +331,7 @@ void oracle_grouped_gemm_fp8(const uint8_t* x, const uint8_t* w, const int32_t* 
     int64_t off = 0;
     for (int e = 0; e < E; ++e) {
         int64_t cnt = counts[e];
-#pragma omp parallel for schedule(dynamic, 1)
+#pragma omp parallel for collapse(2) schedule(static)
         for (int64_t r = off; r < off + cnt; ++r) {
             for (int n = 0; n < N; ++n) {
                 const uint8_t* wr = w + ((int64_t)e * N + n) * K;

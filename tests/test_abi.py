@@ -60,7 +60,7 @@ def test_host_side_validation_without_gpu(lib):
     assert L.moe_gather_scale_quant(fake, 4, 32, fake, fake, 4, fake, 0, 8, 1, 8, None, None, fake, None, None) \
         == lib.MOE_ERR_INVALID
     # scatter: top_k > 1 needs the inverse permutation
-    assert L.moe_scatter_add(fake, fake, fake, None, 2, 8, 4, 32, None, None) == lib.MOE_ERR_INVALID
+    assert L.moe_scatter_add(fake, fake, fake, None, 2, 8, 4, 32, None, 1, None) == lib.MOE_ERR_INVALID
     # silu: misaligned row stride
     assert L.moe_silu_mul(fake, fake, 36, 4, 32, None, fake, None) == lib.MOE_ERR_UNSUPPORTED
     # grouped GEMM: N not a multiple of 16, unknown epilogue, too many experts

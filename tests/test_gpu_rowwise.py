@@ -163,3 +163,9 @@ def test_scatter_add_bit_exact(name, use_inv):
     np.testing.assert_array_equal(bits(out), ref)
     Tv = cfg.valid_tokens
     assert torch.equal(out[Tv:].cpu(), init[Tv:]), "tokens past the valid count stay as they were"
+    # overwrite mode: the same as adding into zeros, and still leaves the padding tokens alone
+    out2 = init.cuda()
+    mb.moe_scatter_add(out2, rows.cuda(), _idx(r["token_indices"]), inv, cfg.top_k, valid, accumulate=False)
+    ref0 = oracle.scatter_add(np.zeros_like(bits(init)), bits(rows), r["token_indices"])
+    np.testing.assert_array_equal(bits(out2[:Tv]), ref0[:Tv])
+    assert torch.equal(out2[Tv:].cpu(), init[Tv:])
