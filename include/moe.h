@@ -118,6 +118,43 @@ int moe_route(const void* scores, int scores_dtype, int64_t stride_t, int64_t st
               int32_t* expert_indices, int32_t* token_indices, int32_t* inv_rows, void* ws,
               size_t ws_bytes, cudaStream_t stream);
 
+/*
+ * moe_route without a caller workspace: for callers that cannot allocate
+ * device memory.  (The pages have no counterpart of this entry point.)
+ *
+ * Some callers may not call cudaMalloc or any other allocating routine where
+ * they route tokens: a plugin inside a framework whose own allocator owns the
+ * whole device-memory budget, a serving loop that cannot afford the implicit
+ * device synchronisation and unbounded latency of an allocation, or code that
+ * must not re-enter the allocator (for example inside an out-of-memory
+ * handler).  They pass inputs and outputs exactly as for moe_route; the
+ * workspace comes from a fixed array of MOE_ROUTE_NO_ALLOC_SCRATCH_BYTES that
+ * the library keeps in global memory of every GPU that loads it, until the
+ * process exits.  Nothing is allocated: no cudaMalloc, cudaFree or allocating
+ * library routine is called.
+ *
+ * - Sizes: returns MOE_ERR_WORKSPACE (and launches nothing) when
+ *   moe_route_workspace_size(T, E, top_k) exceeds
+ *   MOE_ROUTE_NO_ALLOC_SCRATCH_BYTES (1 MiB).  For example T = 16384,
+ *   top_k = 4, E = 128 needs 0.5 MiB and fits; T = 65536, top_k = 1,
+ *   E = 128 needs 1.25 MiB and is rejected.
+ * - Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ *   first call before any stream capture.  A failed lookup returns
+ *   MOE_ERR_CUDA with the code in moe_last_cuda_error().
+ * - Sharing: every call on a device uses the same array and leaves its
+ *   contents behind.  The routing kernels write every scratch word before
+ *   reading it, so nothing needs clearing between calls, but calls whose
+ *   kernels overlap on the GPU (for example on two streams without ordering
+ *   between them) race on the array and give wrong results: order them.
+ * Arguments, outputs and results are those of moe_route.
+ */
+#define MOE_ROUTE_NO_ALLOC_SCRATCH_BYTES (1u << 20)
+int moe_route_no_alloc(const void* scores, int scores_dtype, int64_t stride_t, int64_t stride_e, int T,
+                       int E, int top_k, const int32_t* num_valid_tokens, int32_t* counts,
+                       int32_t* expert_offsets, int32_t* expert_indices, int32_t* token_indices,
+                       int32_t* inv_rows, cudaStream_t stream);
+
 /* --------------------------------------------------------- gather + scale */
 
 /*

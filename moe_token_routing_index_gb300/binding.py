@@ -46,6 +46,7 @@ def _load() -> ctypes.CDLL:
         "moe_device_error": ([U, P], I),
         "moe_route_workspace_size": ([I, I, I, ctypes.POINTER(S)], I),
         "moe_route": ([P, I, L, L, I, I, I, P, P, P, P, P, P, P, S, P], I),
+        "moe_route_no_alloc": ([P, I, L, L, I, I, I, P, P, P, P, P, P, P], I),
         "moe_gather_scale": ([P, I, I, P, P, I, P, I, L, L, I, P, P, P], I),
         "moe_gather_scale_quant": ([P, I, I, P, P, I, P, I, L, L, I, P, P, P, P, P], I),
         "moe_quantize_rows": ([P, L, I, P, P, P, P], I),

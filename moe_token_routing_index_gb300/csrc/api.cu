@@ -60,6 +60,8 @@ int check_scores(const void* scores, int dtype, int E) {
 }  // namespace
 
 namespace moe {
+void record_cuda_error(int e) { t_last_cuda_error = e; }
+
 int device_sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return kNumSmsGB300;

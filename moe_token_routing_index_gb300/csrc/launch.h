@@ -94,4 +94,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s);
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
+// Make `e` (a cudaError_t) what moe_last_cuda_error() reports on this thread.
+void record_cuda_error(int e);
+
 }  // namespace moe
