@@ -166,6 +166,25 @@ def oracle_tokens_per_s(cfg, x, s, w13, w2, seconds: float, max_tokens: int | No
     return done / total, n, oracle.num_threads(), total
 
 
+# ------------------------------------------------------------ multi-rank
+
+def max_over_ranks(value: float, device) -> float:
+    """The largest value over all ranks (the step time that bounds the job)."""
+    import torch
+    import torch.distributed as dist
+
+    if not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, max_ms_per_step: float) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's step time."""
+    return tokens_per_rank * world / (max_ms_per_step * 1e-3)
+
+
 # ------------------------------------------------------------- our arm
 
 def run_ours(args, cfg):
@@ -189,6 +208,11 @@ def run_ours(args, cfg):
     s = workloads.make_scores(cfg, seed=rank).to(dev)
     w13, w2 = workloads.make_weights(cfg, seed=0, device=dev)
     layer = MoELayer.from_weights(cfg, w13, w2)
+    if args.no_cpu_baseline or world > 1 or rank != 0:
+        # only the oracle baseline needs the source weights (fp32 for FP8 layers)
+        del w13, w2
+        w13 = w2 = None
+        torch.cuda.empty_cache()
     nv = None if cfg.Tv is None else torch.tensor([cfg.Tv], dtype=torch.int32, device=dev)
     out = torch.zeros(cfg.T, cfg.D, dtype=torch.bfloat16, device=dev)
     stages = layer.stages(x, s, nv, out, accumulate=False)
@@ -228,14 +252,33 @@ def run_ours(args, cfg):
     ms = t_start.elapsed_time(t_end) / K
     stage_ms = {n: statistics.fmean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(K))
                 for i, n in enumerate(names)}
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
     if mb.device_error() != 0:
         raise RuntimeError("device-side error during the timed steps")
 
-    # end to end through the public API: pinned host inputs in, result out, every step
+    e2e_ms, h2d, d2h = (None, 0, 0) if args.no_e2e else run_e2e(args, cfg, layer, x, s, nv, out, world)
+
+    result = None
+    if rank == 0:
+        result = report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, layer)
+        if not args.no_cpu_baseline and world == 1:
+            tps, n, cores, dt = oracle_tokens_per_s(cfg, x, s, w13, w2, args.cpu_seconds)
+            result["cpu_baseline"] = {"value": round(tps, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+                                      "sample": f"first {n} valid tokens of the workload (repeated to {dt:.1f} s of wall time)"}
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
+def run_e2e(args, cfg, layer, x, s, nv, out, world):
+    """The same forward through the public API with pinned host buffers: each
+    step copies its inputs host -> device and its result device -> host."""
+    import torch
+    import torch.distributed as dist
+
+    K = args.steps
     xh = x.cpu().pin_memory()
     sh = s.cpu().pin_memory()
     nvh = None if nv is None else nv.cpu().pin_memory()
@@ -264,25 +307,10 @@ def run_ours(args, cfg):
     e_end.record()
     torch.cuda.synchronize()
     e2e_ms = e_start.elapsed_time(e_end) / K
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, x.device)
     h2d = xh.numel() * xh.element_size() + sh.numel() * sh.element_size() + (0 if nvh is None else 4)
     d2h = outh.numel() * outh.element_size()
-
-    result = None
-    if rank == 0:
-        result = report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, layer)
-        if not args.no_cpu_baseline and world == 1:
-            tps, n, cores, dt = oracle_tokens_per_s(cfg, x, s, w13, w2, args.cpu_seconds)
-            result["cpu_baseline"] = {"value": round(tps, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
-                                      "sample": f"first {n} valid tokens of the workload (repeated to {dt:.1f} s of wall time)"}
-        print(json.dumps(result), flush=True)
-    if world > 1:
-        dist.barrier()
-        dist.destroy_process_group()
-    return result
+    return e2e_ms, h2d, d2h
 
 
 def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, layer):
@@ -292,7 +320,7 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
     active = sum(1 for c in counts[:E] if c > 0)
     wb = 1 if cfg.fp8 else 2        # weight / activation element bytes into the GEMMs
     tokens = cfg.valid_tokens * world
-    value = tokens / (ms * 1e-3)
+    value = job_tokens_per_s(cfg.valid_tokens, world, ms)
 
     # algorithmic work per stage (one launch each per step)
     gemm1 = "gemm_w13" if cfg.fp8 else "gemm_w13_silu"
@@ -331,7 +359,7 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     roof["kernel"] = dom
     roof["peak_source"] = f"{peak_kind} ({'sustained bf16 x nominal fp8/bf16 ratio' if cfg.fp8 and roof['bound'] == 'tensor' else 'MEASURED_PEAKS.json'})"
-    roof["traffic"] = TRAFFIC.get((cfg.name, dom))
+    roof["traffic"] = traffic_for(cfg.name, dom)
     roof["algorithmic_bytes"] = int(w[0])
     if kind == "gemm":
         roof["algorithmic_flops"] = w[1]
@@ -350,8 +378,10 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
         "stages": stages,
         "gemm_tflops": round(sum(work[n][2] for n in (gemm1, "gemm_w2")) /
                              (sum(stage_ms[n] for n in (gemm1, "gemm_w2")) * 1e-3) / 1e12, 1),
-        "e2e": {"value": round(tokens / (e2e_ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "e2e": None if e2e_ms is None else {
+            "value": round(job_tokens_per_s(cfg.valid_tokens, world, e2e_ms), 1), "unit": UNIT,
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": layer.kernel_launches() * args.steps,
         "clocks": clocks,
     }
@@ -359,8 +389,29 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
 
 
 # ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, from the captures
-# summarised under profiles/ (None until captured for the current kernel).
-TRAFFIC: dict = {}
+# summarised under profiles/, with the hash of the kernel sources they were taken
+# on: when those sources change the figure no longer applies and is reported as null.
+TRAFFIC: dict = {
+    ("decode", "gemm_w13_silu"): (2_689_735_000 + 5_240_320, "grouped_gemm.cu", "17e071b8aa3f"),
+    ("prefill_fp8", "gemm_w13"): (1_386_018_000 + 249_785_600, "grouped_gemm.cu", "17e071b8aa3f"),
+}
+
+
+def kernel_source_hash(name: str) -> str:
+    import hashlib
+
+    csrc = ROOT / "moe_token_routing_index_gb300" / "csrc"
+    h = hashlib.sha1()
+    for f in (name, "common.cuh"):
+        h.update((csrc / f).read_bytes())
+    return h.hexdigest()[:12]
+
+
+def traffic_for(workload: str, stage: str):
+    t = TRAFFIC.get((workload, stage))
+    if t is None or kernel_source_hash(t[1]) != t[2]:
+        return None
+    return t[0]
 
 
 # ------------------------------------------------------- reference arm
@@ -380,7 +431,8 @@ def run_reference(args, cfg):
     s = workloads.make_scores(cfg)
     w13, w2 = workloads.make_weights(cfg, device="cuda" if torch.cuda.is_available() else "cpu")
     budget = 150.0                                  # seconds for the whole --steps/--warmup run
-    tps, n, cores, dt = oracle_tokens_per_s(cfg, x, s, w13, w2, min(10.0, budget / (args.steps + args.warmup)))
+    # calibrate the per-token cost, then size each step's sample to the budget
+    tps, n, cores, dt = oracle_tokens_per_s(cfg, x, s, w13, w2, min(3.0, budget / (args.steps + args.warmup)))
     per_tok = dt / n
     n_step = int(max(1, min(cfg.valid_tokens, budget / (args.steps + args.warmup) / per_tok)))
     xb, sb = _host_bits(x), _host_bits(s)
@@ -433,6 +485,7 @@ def main(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU-baseline leg")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work of the oracle baseline sample")
+    p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")
