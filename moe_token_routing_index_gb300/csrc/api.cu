@@ -1,6 +1,8 @@
 // The C ABI of libmoe_gb300 (declared in include/moe.h): argument checks on
 // the host, then the launchers of the kernel translation units.
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "common.cuh"
 #include "launch.h"
@@ -61,6 +63,19 @@ int check_scores(const void* scores, int dtype, int E) {
 
 namespace moe {
 void record_cuda_error(int e) { t_last_cuda_error = e; }
+
+int resident_blocks_per_sm(const void* kernel, int threads) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  static std::map<std::pair<int, const void*>, int> cache;
+  std::lock_guard<std::mutex> lock(g_mu);
+  auto it = cache.find({dev, kernel});
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1) n = 1;
+  cache[{dev, kernel}] = n;
+  return n;
+}
 
 int device_sm_count() {
   int dev = 0;

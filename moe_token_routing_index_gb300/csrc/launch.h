@@ -94,6 +94,10 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s);
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 
+// Blocks of `kernel` (with `threads` threads, no dynamic shared memory) that
+// fit on one SM at once (cached per device and kernel; at least 1).
+int resident_blocks_per_sm(const void* kernel, int threads);
+
 // Make `e` (a cudaError_t) what moe_last_cuda_error() reports on this thread.
 void record_cuda_error(int e);
 

@@ -7,9 +7,11 @@
 //
 // Every kernel moves rows in 16-byte vectors (8 bf16 / 16 e4m3 / 4 fp32),
 // coalesced across a warp, on a persistent grid of (SMs x 8) 256-thread
-// blocks.  Plain stages give one warp a row; quantising stages give one
-// block a row, held in registers between the row-max reduction and the
-// quantisation, so each input byte is read from HBM once.
+// blocks.  Plain stages give one warp a row; quantising stages give a group
+// of 1-8 warps a row, held in registers between the row-max reduction and
+// the quantisation, so each input byte is read from HBM once.
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -18,12 +20,16 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kBlocksPerSm = 8;
 constexpr int kUnroll = 4;
+constexpr int kChunk = 32 * kUnroll;  // 16-byte vectors per work item of the plain row kernels
 
-inline int persistent_grid(int64_t work_items, int items_per_block) {
+// Grid of a persistent kernel: as many blocks as fit on the device at once
+// (SMs x resident blocks per SM of this kernel), or fewer when there is less
+// work, so every block stays resident and walks a long run of rows.
+template <typename Kernel>
+int persistent_grid(Kernel kernel, int64_t work_items, int items_per_block) {
   int64_t need = (work_items + items_per_block - 1) / items_per_block;
-  int64_t cap = (int64_t)device_sm_count() * kBlocksPerSm;
+  int64_t cap = (int64_t)device_sm_count() * resident_blocks_per_sm(reinterpret_cast<const void*>(kernel), kThreads);
   if (need < 1) need = 1;
   return (int)(need < cap ? need : cap);
 }
@@ -42,6 +48,29 @@ __device__ __forceinline__ float block_max_nonneg(float m, float* s_red) {
   return r;
 }
 
+// Barrier over the `nthreads` threads of one row group (ids 1..8; 0 is __syncthreads).
+__device__ __forceinline__ void group_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Max of a non-negative float over the G warps of a row group; every thread of
+// the group gets the result.  s_red holds one slot per warp of the block.
+template <int G>
+__device__ __forceinline__ float group_max_nonneg(float m, float* s_red, int group) {
+  m = warp_max_nonneg(m);
+  if constexpr (G == 1) {
+    return m;
+  } else {
+    const int warp = threadIdx.x >> 5;
+    if ((threadIdx.x & 31) == 0) s_red[warp] = m;
+    group_sync(1 + group, 32 * G);
+    float r = s_red[group * G];
+#pragma unroll
+    for (int w = 1; w < G; ++w) r = fmaxf(r, s_red[group * G + w]);
+    return r;
+  }
+}
+
 // 8 floats -> 8 e4m3 codes (already scaled and clamped), packed little-endian.
 __device__ __forceinline__ uint2 e4m3x8(const float* f) {
   uint2 q;
@@ -52,86 +81,289 @@ __device__ __forceinline__ uint2 e4m3x8(const float* f) {
 
 // ------------------------------------------------------------ gather*score
 
+// Work item = (routed row, chunk of 32 lanes x kGatherUnroll vectors);
+// consecutive items are consecutive chunks of a row, spread over all warps of
+// the grid.  The indices of a warp's next item are loaded one item ahead.
+constexpr int kGatherUnroll = 8;
+constexpr int kGatherChunk = 32 * kGatherUnroll;
+
 __global__ void __launch_bounds__(kThreads) gather_scale_kernel(
     const uint4* __restrict__ x, int T, int D8, const int32_t* __restrict__ ti, const int32_t* __restrict__ ei,
     int a, const void* __restrict__ scores, int dtype, int64_t st, int64_t se, int E,
     const int32_t* __restrict__ valid_p, uint4* __restrict__ out, unsigned int* err) {
   const int valid = read_count(valid_p, a, err);
   const int lane = threadIdx.x & 31;
-  for (int r = global_warp(); r < valid; r += num_warps()) {
-    const int t = __ldg(ti + r), e = __ldg(ei + r);
-    if ((unsigned)t >= (unsigned)T || (unsigned)e >= (unsigned)E) {
+  const int chunks = (D8 + kGatherChunk - 1) / kGatherChunk;
+  const int64_t items = (int64_t)valid * chunks;
+  const int64_t step = num_warps();
+  int64_t it = global_warp();
+  int t = 0, e = 0;
+  if (it < items) {
+    const int r = (int)(it / chunks);
+    t = __ldg(ti + r);
+    e = __ldg(ei + r);
+  }
+  for (; it < items; it += step) {
+    const int r = (int)(it / chunks);
+    const int c0 = (int)(it - (int64_t)r * chunks) * kGatherChunk + lane;
+    const int ct = t, ce = e;
+    if (it + step < items) {  // next item's indices
+      const int rn = (int)((it + step) / chunks);
+      t = __ldg(ti + rn);
+      e = __ldg(ei + rn);
+    }
+    if ((unsigned)ct >= (unsigned)T || (unsigned)ce >= (unsigned)E) {
       if (lane == 0) flag_error(err, MOE_DEVERR_BAD_INDEX);
       continue;
     }
-    const float s = load_score(scores, dtype, (int64_t)t * st + (int64_t)e * se);
-    const uint4* src = x + (int64_t)t * D8;
+    const float s = load_score(scores, dtype, (int64_t)ct * st + (int64_t)ce * se);
+    const uint4* src = x + (int64_t)ct * D8;
     uint4* dst = out + (int64_t)r * D8;
-    for (int c0 = lane; c0 < D8; c0 += 32 * kUnroll) {
-      uint4 v[kUnroll];
+    uint4 v[kGatherUnroll];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u)
-        if (c0 + 32 * u < D8) v[u] = __ldg(src + c0 + 32 * u);
+    for (int u = 0; u < kGatherUnroll; ++u)
+      if (c0 + 32 * u < D8) v[u] = __ldg(src + c0 + 32 * u);
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        if (c0 + 32 * u >= D8) break;
-        float f[8];
-        bf16x8_to_f32(v[u], f);
+    for (int u = 0; u < kGatherUnroll; ++u) {
+      if (c0 + 32 * u >= D8) break;
+      float f[8];
+      bf16x8_to_f32(v[u], f);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], s);
-        dst[c0 + 32 * u] = f32_to_bf16x8(f);
-      }
+      for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], s);
+      dst[c0 + 32 * u] = f32_to_bf16x8(f);
     }
   }
 }
 
 // ------------------------------------------------- gather*score -> FP8 row
+//
+// A row group of G warps owns one routed row at a time: the fp32 row v = x * s
+// stays in registers (VPT 16-byte vectors per thread, G * 32 * VPT >= D / 8),
+// the group reduces max|v| (warp shuffles, then one named barrier when G > 1),
+// and quantises.  As soon as the current row has been expanded to fp32, the
+// packed input of the group's next row is loaded into the freed registers, so
+// those loads are in flight while the current row is reduced, quantised and
+// stored.  The 8 / G groups of a block walk their rows independently.
 
-template <int VPT>  // 16-byte vectors per thread: VPT * 256 >= D / 8
+template <int G, int VPT>
 __global__ void __launch_bounds__(kThreads) gather_scale_quant_kernel(
     const uint4* __restrict__ x, int T, int D8, const int32_t* __restrict__ ti, const int32_t* __restrict__ ei,
     int a, const void* __restrict__ scores, int dtype, int64_t st, int64_t se, int E,
     const int32_t* __restrict__ valid_p, const float* __restrict__ ub, uint2* __restrict__ out,
     float* __restrict__ out_scale, unsigned int* err) {
+  constexpr int kGroupThreads = 32 * G, kGroups = kThreads / kGroupThreads;
   __shared__ float s_red[kWarps];
   const int valid = read_count(valid_p, a, err);
-  for (int r = blockIdx.x; r < valid; r += gridDim.x) {
-    const int t = __ldg(ti + r), e = __ldg(ei + r);
-    if ((unsigned)t >= (unsigned)T || (unsigned)e >= (unsigned)E) {  // uniform over the block
-      if (threadIdx.x == 0) flag_error(err, MOE_DEVERR_BAD_INDEX);
-      continue;
+  const int group = threadIdx.x / kGroupThreads, gt = threadIdx.x % kGroupThreads;
+  const int stride = gridDim.x * kGroups;
+  // Software pipeline: the indices of row r + 2*stride and the data of row
+  // r + stride are in flight while row r is reduced, quantised and stored.
+  uint4 raw[VPT];
+  float s = 0.0f;
+  bool ok = false;
+  int nt = 0, ne = 0;  // indices of the next row
+  auto fetch_data = [&](int t, int e) {
+    ok = (unsigned)t < (unsigned)T && (unsigned)e < (unsigned)E;
+    if (ok) {
+      s = load_score(scores, dtype, (int64_t)t * st + (int64_t)e * se);
+      const uint4* src = x + (int64_t)t * D8;
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int c = gt + kGroupThreads * i;
+        if (c < D8) raw[i] = __ldg(src + c);
+      }
     }
-    const float s = load_score(scores, dtype, (int64_t)t * st + (int64_t)e * se);
-    const uint4* src = x + (int64_t)t * D8;
+  };
+  int r = blockIdx.x * kGroups + group;
+  if (r < valid) fetch_data(__ldg(ti + r), __ldg(ei + r));
+  if (r + stride < valid) {
+    nt = __ldg(ti + r + stride);
+    ne = __ldg(ei + r + stride);
+  }
+  for (; r < valid; r += stride) {
+    const bool cur_ok = ok;  // uniform over the group
     float f[VPT][8];
     float m = 0.0f;
+    if (cur_ok) {
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-      const int c = threadIdx.x + kThreads * i;
-      if (c < D8) {
-        bf16x8_to_f32(__ldg(src + c), f[i]);
+      for (int i = 0; i < VPT; ++i) {
+        const int c = gt + kGroupThreads * i;
+        if (c < D8) {
+          bf16x8_to_f32(raw[i], f[i]);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          f[i][q] = __fmul_rn(f[i][q], s);
-          m = fmaxf(m, fabsf(f[i][q]));
+          for (int q = 0; q < 8; ++q) {
+            f[i][q] = __fmul_rn(f[i][q], s);
+            m = fmaxf(m, fabsf(f[i][q]));
+          }
         }
       }
     }
-    m = block_max_nonneg(m, s_red);
+    if (r + stride < valid) fetch_data(nt, ne);
+    if (r + 2 * stride < valid) {
+      nt = __ldg(ti + r + 2 * stride);
+      ne = __ldg(ei + r + 2 * stride);
+    }
+    if (!cur_ok) {
+      if (gt == 0) flag_error(err, MOE_DEVERR_BAD_INDEX);
+      continue;
+    }
+    m = group_max_nonneg<G>(m, s_red, group);
     float inv;
     const float sc = fp8_row_scale(m, ub, &inv);
-    if (threadIdx.x == 0) out_scale[r] = inv;
+    if (gt == 0) out_scale[r] = inv;
     uint2* dst = out + (int64_t)r * D8;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
-      const int c = threadIdx.x + kThreads * i;
+      const int c = gt + kGroupThreads * i;
       if (c < D8) {
 #pragma unroll
         for (int q = 0; q < 8; ++q) f[i][q] = fp8_scaled_clamped(f[i][q], sc);
         dst[c] = e4m3x8(f[i]);
       }
     }
-    __syncthreads();  // s_red is reused by the next row
+    if constexpr (G > 1) group_sync(1 + group, kGroupThreads);  // s_red is reused by the next row
+  }
+}
+
+// ----------------------------------- gather*score -> FP8, TMA-staged rows
+//
+// Each warp owns a ring of NB row slots in shared memory.  Lane 0 reads the
+// row's token index and issues one bulk copy (cp.async.bulk, completion on
+// the slot's mbarrier) of the whole x row into a slot; the warp then makes two
+// passes over the staged row (max |x * s|, then scale, quantise and store) and
+// hands the slot to the row NB ahead.  Rows in flight per SM = warps x NB, with
+// almost no registers, and each x byte crosses HBM once.
+
+__device__ __forceinline__ uint64_t global_timer_ns_rw() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ bool bar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait (1 s) for the phase with `parity` to complete.
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
+  if (bar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns_rw();
+  for (uint32_t i = 1;; ++i) {
+    if (bar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 0 && global_timer_ns_rw() - t0 > 1000000000ull) return false;
+  }
+}
+
+// One bulk copy of `bytes` (multiple of 16, 16-byte aligned) global -> shared, tracked by `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+constexpr int kStagedWarps = 8;
+
+__global__ void __launch_bounds__(kStagedWarps * 32, 1) gather_scale_quant_staged_kernel(
+    const uint4* __restrict__ x, int T, int D8, const int32_t* __restrict__ ti, const int32_t* __restrict__ ei,
+    int a, const void* __restrict__ scores, int dtype, int64_t st, int64_t se, int E,
+    const int32_t* __restrict__ valid_p, const float* __restrict__ ub, uint2* __restrict__ out,
+    float* __restrict__ out_scale, int NB, unsigned int* err) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t row_bytes = (uint32_t)D8 * 16u;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);                      // [warps][NB]
+  int2* s_idx = reinterpret_cast<int2*>(smem + kStagedWarps * NB * 8);     // [warps][NB]: token, expert
+  uint8_t* slots = smem + ((kStagedWarps * NB * 16 + 127) / 128) * 128;    // [warps][NB][row_bytes]
+  const int valid = read_count(valid_p, a, err);
+  const int gw = blockIdx.x * kStagedWarps + warp, nw = gridDim.x * kStagedWarps;
+  auto bar_addr = [&](int b) { return (uint32_t)__cvta_generic_to_shared(&bars[warp * NB + b]); };
+  auto slot = [&](int b) { return slots + (size_t)(warp * NB + b) * row_bytes; };
+  if (lane == 0)
+    for (int b = 0; b < NB; ++b) bar_init(bar_addr(b), 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  __syncwarp();
+  // lane 0: read the indices of routed row r and start its copy into slot b
+  auto issue = [&](int r, int b) {
+    const int t = __ldg(ti + r), e = __ldg(ei + r);
+    const bool ok = (unsigned)t < (unsigned)T && (unsigned)e < (unsigned)E;
+    s_idx[warp * NB + b] = make_int2(ok ? t : -1, e);
+    if (ok) bulk_load((uint32_t)__cvta_generic_to_shared(slot(b)), x + (int64_t)t * D8, row_bytes, bar_addr(b));
+  };
+  if (lane == 0)
+    for (int b = 0; b < NB; ++b)
+      if (gw + b * nw < valid) issue(gw + b * nw, b);
+  __syncwarp();
+  uint32_t phase = 0;  // bit b: parity of the next completion of slot b
+  int i = 0;
+  bool timed_out = false;
+  for (;; ++i) {
+    const int r = gw + i * nw;
+    if (r >= valid) break;
+    const int b = i % NB;
+    const int2 te = s_idx[warp * NB + b];
+    if (te.x >= 0) {
+      if (!bar_wait(bar_addr(b), (phase >> b) & 1u)) {
+        timed_out = true;
+        break;
+      }
+      phase ^= 1u << b;
+      const float s = load_score(scores, dtype, (int64_t)te.x * st + (int64_t)te.y * se);
+      const uint4* row = reinterpret_cast<const uint4*>(slot(b));
+      float m = 0.0f;
+      for (int c = lane; c < D8; c += 32) {
+        float f[8];
+        bf16x8_to_f32(row[c], f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) m = fmaxf(m, fabsf(__fmul_rn(f[q], s)));
+      }
+      m = warp_max_nonneg(m);
+      float inv;
+      const float sc = fp8_row_scale(m, ub, &inv);
+      if (lane == 0) out_scale[r] = inv;
+      uint2* dst = out + (int64_t)r * D8;
+      for (int c = lane; c < D8; c += 32) {
+        float f[8];
+        bf16x8_to_f32(row[c], f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) f[q] = fp8_scaled_clamped(__fmul_rn(f[q], s), sc);
+        dst[c] = e4m3x8(f);
+      }
+    } else if (lane == 0) {
+      flag_error(err, MOE_DEVERR_BAD_INDEX);
+    }
+    // the slot's reads (generic proxy) finish before the next bulk copy (async proxy) writes it
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0 && r + NB * nw < valid) issue(r + NB * nw, b);
+    __syncwarp();
+  }
+  // On a normal exit every issued copy has been consumed (a copy is issued only
+  // for a row below `valid`, and the loop waits on every such row).  After a
+  // timeout, the copies of iterations i .. i+NB-1 may still be in flight: wait
+  // for them (bounded) so none lands after the block has exited.
+  if (timed_out && lane == 0) {
+    flag_error(err, MOE_DEVERR_TIMEOUT);
+    for (int j = i; j < i + NB; ++j) {
+      const int b = j % NB;
+      if (gw + j * nw < valid && s_idx[warp * NB + b].x >= 0) {
+        const uint64_t t0 = global_timer_ns_rw();
+        while (!bar_try_wait(bar_addr(b), (phase >> b) & 1u) && global_timer_ns_rw() - t0 < 100000000ull) {
+        }
+      }
+    }
   }
 }
 
@@ -169,52 +401,72 @@ __global__ void __launch_bounds__(kThreads) silu_mul_kernel(const __nv_bfloat16*
                                                             uint4* __restrict__ z, unsigned int* err) {
   const int valid = read_count(valid_p, a, err);
   const int lane = threadIdx.x & 31;
-  for (int r = global_warp(); r < valid; r += num_warps()) {
+  const int chunks = (H8 + kChunk - 1) / kChunk;
+  const int64_t items = (int64_t)valid * chunks;
+  for (int64_t it = global_warp(); it < items; it += num_warps()) {
+    const int r = (int)(it / chunks);
+    const int c0 = (int)(it - (int64_t)r * chunks) * kChunk + lane;
     const uint4* p0 = reinterpret_cast<const uint4*>(x0 + (int64_t)r * ld);
     const uint4* p1 = reinterpret_cast<const uint4*>(x1 + (int64_t)r * ld);
     uint4* dst = z + (int64_t)r * H8;
-    for (int c0 = lane; c0 < H8; c0 += 32 * kUnroll) {
-      uint4 v0[kUnroll], v1[kUnroll];
+    uint4 v0[kUnroll], v1[kUnroll];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u)
-        if (c0 + 32 * u < H8) {
-          v0[u] = __ldg(p0 + c0 + 32 * u);
-          v1[u] = __ldg(p1 + c0 + 32 * u);
-        }
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        if (c0 + 32 * u >= H8) break;
-        float f0[8], f1[8];
-        bf16x8_to_f32(v0[u], f0);
-        bf16x8_to_f32(v1[u], f1);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) f0[i] = silu_mul_f32(f0[i], f1[i]);
-        dst[c0 + 32 * u] = f32_to_bf16x8(f0);
+    for (int u = 0; u < kUnroll; ++u)
+      if (c0 + 32 * u < H8) {
+        v0[u] = __ldg(p0 + c0 + 32 * u);
+        v1[u] = __ldg(p1 + c0 + 32 * u);
       }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (c0 + 32 * u >= H8) break;
+      float f0[8], f1[8];
+      bf16x8_to_f32(v0[u], f0);
+      bf16x8_to_f32(v1[u], f1);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f0[i] = silu_mul_f32(f0[i], f1[i]);
+      dst[c0 + 32 * u] = f32_to_bf16x8(f0);
     }
   }
 }
 
-template <int VPT>
+// Row groups as in the quantising gather; the fp32 row of z is held in
+// registers and the next row's two packed halves are prefetched.
+template <int G, int VPT>
 __global__ void __launch_bounds__(kThreads) silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ x0,
                                                                   const __nv_bfloat16* __restrict__ x1, int64_t ld,
                                                                   int a, int H8, const int32_t* __restrict__ valid_p,
                                                                   const float* __restrict__ ub, uint2* __restrict__ z,
                                                                   float* __restrict__ z_scale, unsigned int* err) {
+  constexpr int kGroupThreads = 32 * G, kGroups = kThreads / kGroupThreads;
   __shared__ float s_red[kWarps];
   const int valid = read_count(valid_p, a, err);
-  for (int r = blockIdx.x; r < valid; r += gridDim.x) {
-    const uint4* p0 = reinterpret_cast<const uint4*>(x0 + (int64_t)r * ld);
-    const uint4* p1 = reinterpret_cast<const uint4*>(x1 + (int64_t)r * ld);
+  const int group = threadIdx.x / kGroupThreads, gt = threadIdx.x % kGroupThreads;
+  const int stride = gridDim.x * kGroups;
+  uint4 r0[VPT], r1[VPT];
+  auto fetch = [&](int row) {
+    const uint4* p0 = reinterpret_cast<const uint4*>(x0 + (int64_t)row * ld);
+    const uint4* p1 = reinterpret_cast<const uint4*>(x1 + (int64_t)row * ld);
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int c = gt + kGroupThreads * i;
+      if (c < H8) {
+        r0[i] = __ldg(p0 + c);
+        r1[i] = __ldg(p1 + c);
+      }
+    }
+  };
+  int r = blockIdx.x * kGroups + group;
+  if (r < valid) fetch(r);
+  for (; r < valid; r += stride) {
     float f[VPT][8];
     float m = 0.0f;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
-      const int c = threadIdx.x + kThreads * i;
+      const int c = gt + kGroupThreads * i;
       if (c < H8) {
         float g[8];
-        bf16x8_to_f32(__ldg(p0 + c), f[i]);
-        bf16x8_to_f32(__ldg(p1 + c), g);
+        bf16x8_to_f32(r0[i], f[i]);
+        bf16x8_to_f32(r1[i], g);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           f[i][q] = silu_mul_f32(f[i][q], g[q]);
@@ -222,27 +474,29 @@ __global__ void __launch_bounds__(kThreads) silu_mul_quant_kernel(const __nv_bfl
         }
       }
     }
-    m = block_max_nonneg(m, s_red);
+    if (r + stride < valid) fetch(r + stride);
+    m = group_max_nonneg<G>(m, s_red, group);
     float inv;
     const float sc = fp8_row_scale(m, ub, &inv);
-    if (threadIdx.x == 0) z_scale[r] = inv;
+    if (gt == 0) z_scale[r] = inv;
     uint2* dst = z + (int64_t)r * H8;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
-      const int c = threadIdx.x + kThreads * i;
+      const int c = gt + kGroupThreads * i;
       if (c < H8) {
 #pragma unroll
         for (int q = 0; q < 8; ++q) f[i][q] = fp8_scaled_clamped(f[i][q], sc);
         dst[c] = e4m3x8(f[i]);
       }
     }
-    __syncthreads();
+    if constexpr (G > 1) group_sync(1 + group, kGroupThreads);
   }
 }
 
 // ------------------------------------------------------------- scatter-add
 
 // top_k == 1 without the inverse permutation: routed row r owns token ti[r].
+// Work items as in the gather: (row, chunk).
 template <bool ACC>
 __global__ void __launch_bounds__(kThreads) scatter_add_rows_kernel(uint4* __restrict__ out,
                                                                     const uint4* __restrict__ in,
@@ -251,7 +505,11 @@ __global__ void __launch_bounds__(kThreads) scatter_add_rows_kernel(uint4* __res
                                                                     unsigned int* err) {
   const int valid = read_count(valid_p, a, err);
   const int lane = threadIdx.x & 31;
-  for (int r = global_warp(); r < valid; r += num_warps()) {
+  const int chunks = (D8 + kChunk - 1) / kChunk;
+  const int64_t items = (int64_t)valid * chunks;
+  for (int64_t it = global_warp(); it < items; it += num_warps()) {
+    const int r = (int)(it / chunks);
+    const int c0 = (int)(it - (int64_t)r * chunks) * kChunk + lane;
     const int t = __ldg(ti + r);
     if ((unsigned)t >= (unsigned)T) {
       if (lane == 0) flag_error(err, MOE_DEVERR_BAD_INDEX);
@@ -259,35 +517,33 @@ __global__ void __launch_bounds__(kThreads) scatter_add_rows_kernel(uint4* __res
     }
     uint4* o = out + (int64_t)t * D8;
     const uint4* src = in + (int64_t)r * D8;
-    for (int c0 = lane; c0 < D8; c0 += 32 * kUnroll) {
-      uint4 vo[kUnroll], vi[kUnroll];
+    uint4 vo[kUnroll], vi[kUnroll];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u)
-        if (c0 + 32 * u < D8) {
-          if (ACC) vo[u] = o[c0 + 32 * u];
-          vi[u] = __ldg(src + c0 + 32 * u);
-        }
+    for (int u = 0; u < kUnroll; ++u)
+      if (c0 + 32 * u < D8) {
+        if (ACC) vo[u] = o[c0 + 32 * u];
+        vi[u] = __ldg(src + c0 + 32 * u);
+      }
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        if (c0 + 32 * u >= D8) break;
-        if (ACC) {
-          float fo[8], fi[8];
-          bf16x8_to_f32(vo[u], fo);
-          bf16x8_to_f32(vi[u], fi);
+    for (int u = 0; u < kUnroll; ++u) {
+      if (c0 + 32 * u >= D8) break;
+      if (ACC) {
+        float fo[8], fi[8];
+        bf16x8_to_f32(vo[u], fo);
+        bf16x8_to_f32(vi[u], fi);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) fo[i] = __fadd_rn(fo[i], fi[i]);
-          o[c0 + 32 * u] = f32_to_bf16x8(fo);
-        } else {
-          o[c0 + 32 * u] = vi[u];  // bf16(0 + x) = x
-        }
+        for (int i = 0; i < 8; ++i) fo[i] = __fadd_rn(fo[i], fi[i]);
+        o[c0 + 32 * u] = f32_to_bf16x8(fo);
+      } else {
+        o[c0 + 32 * u] = vi[u];  // bf16(0 + x) = x
       }
     }
   }
 }
 
-// With the inverse permutation: one warp owns token t and adds its top_k rows
-// in ascending row order into an fp32 accumulator started from out[t] (ACC)
-// or from zero.
+// With the inverse permutation: a warp owns a (token, chunk) item and adds
+// the token's top_k rows in ascending row order into an fp32 accumulator
+// started from out[t] (ACC) or from zero.
 template <bool ACC>
 __global__ void __launch_bounds__(kThreads) scatter_add_tokens_kernel(uint4* __restrict__ out,
                                                                       const uint4* __restrict__ in,
@@ -300,7 +556,11 @@ __global__ void __launch_bounds__(kThreads) scatter_add_tokens_kernel(uint4* __r
   int Tv = valid / k;
   if (Tv > T) Tv = T;
   const int lane = threadIdx.x & 31;
-  for (int t = global_warp(); t < Tv; t += num_warps()) {
+  const int chunks = (D8 + kChunk - 1) / kChunk;
+  const int64_t items = (int64_t)Tv * chunks;
+  for (int64_t it = global_warp(); it < items; it += num_warps()) {
+    const int t = (int)(it / chunks);
+    const int c0 = (int)(it - (int64_t)t * chunks) * kChunk + lane;
     int my_row = 0;
     bool bad = false;
     if (lane < k) {
@@ -312,113 +572,145 @@ __global__ void __launch_bounds__(kThreads) scatter_add_tokens_kernel(uint4* __r
       continue;
     }
     uint4* o = out + (int64_t)t * D8;
-    for (int c0 = lane; c0 < D8; c0 += 32 * 2) {
-      float acc[2][8];
+    float acc[kUnroll][8];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        if (ACC && c0 + 32 * u < D8) {
-          bf16x8_to_f32(o[c0 + 32 * u], acc[u]);
-        } else {
+    for (int u = 0; u < kUnroll; ++u) {
+      if (ACC && c0 + 32 * u < D8) {
+        bf16x8_to_f32(o[c0 + 32 * u], acc[u]);
+      } else {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
-        }
+        for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
       }
-      for (int j = 0; j < k; ++j) {
-        const int r = (j < 32) ? __shfl_sync(0xffffffffu, my_row, j) : __ldg(inv + (int64_t)t * k + j);
-        if ((unsigned)r >= (unsigned)a) {  // only reachable for top_k > 32
-          flag_error(err, MOE_DEVERR_BAD_INDEX);
-          continue;
-        }
-        const uint4* src = in + (int64_t)r * D8;
-#pragma unroll
-        for (int u = 0; u < 2; ++u)
-          if (c0 + 32 * u < D8) {
-            float fi[8];
-            bf16x8_to_f32(__ldg(src + c0 + 32 * u), fi);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[u][i] = __fadd_rn(acc[u][i], fi[i]);
-          }
-      }
-#pragma unroll
-      for (int u = 0; u < 2; ++u)
-        if (c0 + 32 * u < D8) o[c0 + 32 * u] = f32_to_bf16x8(acc[u]);
     }
+    for (int j = 0; j < k; ++j) {
+      const int r = (j < 32) ? __shfl_sync(0xffffffffu, my_row, j) : __ldg(inv + (int64_t)t * k + j);
+      if ((unsigned)r >= (unsigned)a) {  // only reachable for top_k > 32
+        flag_error(err, MOE_DEVERR_BAD_INDEX);
+        continue;
+      }
+      const uint4* src = in + (int64_t)r * D8;
+      uint4 v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        if (c0 + 32 * u < D8) v[u] = __ldg(src + c0 + 32 * u);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        if (c0 + 32 * u < D8) {
+          float fi[8];
+          bf16x8_to_f32(v[u], fi);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[u][i] = __fadd_rn(acc[u][i], fi[i]);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (c0 + 32 * u < D8) o[c0 + 32 * u] = f32_to_bf16x8(acc[u]);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_gather_scale(const GatherArgs& g, cudaStream_t s) {
-  const int grid = persistent_grid(g.a, kWarps);
+  const int grid =
+      persistent_grid(gather_scale_kernel, (int64_t)g.a * ((g.D / 8 + kGatherChunk - 1) / kGatherChunk), kWarps);
   gather_scale_kernel<<<grid, kThreads, 0, s>>>(static_cast<const uint4*>(g.x), g.T, g.D / 8, g.token_indices,
                                                 g.expert_indices, g.a, g.scores, g.dtype, g.stride_t, g.stride_e,
                                                 g.E, g.valid, static_cast<uint4*>(g.out), g.err);
   return cudaGetLastError();
 }
 
-#define MOE_GATHER_QUANT(VPT)                                                                                     \
-  gather_scale_quant_kernel<VPT><<<grid, kThreads, 0, s>>>(                                                      \
-      static_cast<const uint4*>(g.x), g.T, D8, g.token_indices, g.expert_indices, g.a, g.scores, g.dtype,         \
+// Row groups: the fewest warps per row (G) with at most 4 vectors (32 fp32) per
+// thread, 8 vectors only past 8 warps (D or H above 8192).
+inline int pick_group(int nvec) {
+  for (int g = 1; g < 8; g <<= 1)
+    if (nvec <= 32 * g * 4) return g;
+  return 8;
+}
+
+#define MOE_GATHER_QUANT(G, VPT)                                                                              \
+  gather_scale_quant_kernel<G, VPT><<<persistent_grid(gather_scale_quant_kernel<G, VPT>, g.a, kThreads / (32 * G)), \
+                                      kThreads, 0, s>>>(                                                     \
+      static_cast<const uint4*>(g.x), g.T, D8, g.token_indices, g.expert_indices, g.a, g.scores, g.dtype,     \
       g.stride_t, g.stride_e, g.E, g.valid, g.scale_ub, static_cast<uint2*>(g.out), g.out_scale, g.err)
 
 cudaError_t launch_gather_scale_quant(const GatherArgs& g, cudaStream_t s) {
   const int D8 = g.D / 8;
-  const int vpt = (D8 + kThreads - 1) / kThreads;
-  const int grid = persistent_grid(g.a, 1);
-  if (vpt <= 1) MOE_GATHER_QUANT(1);
-  else if (vpt <= 2) MOE_GATHER_QUANT(2);
-  else if (vpt <= 3) MOE_GATHER_QUANT(3);
-  else if (vpt <= 4) MOE_GATHER_QUANT(4);
-  else if (vpt <= 6) MOE_GATHER_QUANT(6);
-  else MOE_GATHER_QUANT(8);
+  {
+    // TMA-staged kernel: as many row slots per warp (2..4) as fit in 200 KB of shared memory.
+    const size_t row_bytes = (size_t)D8 * 16;
+    const int nb = (int)std::min<size_t>(4, (200u * 1024u) / (kStagedWarps * row_bytes));
+    if (nb >= 2) {
+      const size_t smem = (size_t)((kStagedWarps * nb * 16 + 127) / 128) * 128 + (size_t)kStagedWarps * nb * row_bytes;
+      cudaError_t e = cudaFuncSetAttribute(gather_scale_quant_staged_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      const int64_t need = (g.a + kStagedWarps - 1) / kStagedWarps;
+      const int grid = (int)std::min<int64_t>(need, device_sm_count());
+      gather_scale_quant_staged_kernel<<<grid, kStagedWarps * 32, smem, s>>>(
+          static_cast<const uint4*>(g.x), g.T, D8, g.token_indices, g.expert_indices, g.a, g.scores, g.dtype,
+          g.stride_t, g.stride_e, g.E, g.valid, g.scale_ub, static_cast<uint2*>(g.out), g.out_scale, nb, g.err);
+      return cudaGetLastError();
+    }
+  }
+  const int G = pick_group(D8);
+  const bool full = D8 > 32 * G * 4;  // 8 vectors per thread, else 4
+  switch (G * 2 + (full ? 1 : 0)) {
+    case 2: MOE_GATHER_QUANT(1, 4); break;
+    case 4: MOE_GATHER_QUANT(2, 4); break;
+    case 8: MOE_GATHER_QUANT(4, 4); break;
+    case 16: MOE_GATHER_QUANT(8, 4); break;
+    default: MOE_GATHER_QUANT(8, 8); break;  // rows past 8192 elements
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_rows(const float* w, int64_t rows, int cols, const float* ub, void* q, float* scale,
                                  cudaStream_t s) {
-  const int grid = persistent_grid(rows, 1);
+  const int grid = persistent_grid(quantize_rows_kernel, rows, 1);
   quantize_rows_kernel<<<grid, kThreads, 0, s>>>(reinterpret_cast<const float4*>(w), rows, cols / 4, ub,
                                                  static_cast<uint32_t*>(q), scale);
   return cudaGetLastError();
 }
 
 cudaError_t launch_silu_mul(const SiluArgs& g, cudaStream_t s) {
-  const int grid = persistent_grid(g.a, kWarps);
+  const int grid = persistent_grid(silu_mul_kernel, (int64_t)g.a * ((g.H / 8 + kChunk - 1) / kChunk), kWarps);
   silu_mul_kernel<<<grid, kThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(g.x0),
                                             static_cast<const __nv_bfloat16*>(g.x1), g.ld, g.a, g.H / 8, g.valid,
                                             static_cast<uint4*>(g.z), g.err);
   return cudaGetLastError();
 }
 
-#define MOE_SILU_QUANT(VPT)                                                                                        \
-  silu_mul_quant_kernel<VPT><<<grid, kThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(g.x0),                 \
-                                                       static_cast<const __nv_bfloat16*>(g.x1), g.ld, g.a, H8,    \
-                                                       g.valid, g.scale_ub, static_cast<uint2*>(g.z), g.z_scale, \
-                                                       g.err)
+#define MOE_SILU_QUANT(G, VPT)                                                                                  \
+  silu_mul_quant_kernel<G, VPT><<<persistent_grid(silu_mul_quant_kernel<G, VPT>, g.a, kThreads / (32 * G)),   \
+                                  kThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(g.x0),                   \
+                                                          static_cast<const __nv_bfloat16*>(g.x1), g.ld, g.a, H8, \
+                                                          g.valid, g.scale_ub, static_cast<uint2*>(g.z),          \
+                                                          g.z_scale, g.err)
 
 cudaError_t launch_silu_mul_quant(const SiluArgs& g, cudaStream_t s) {
   const int H8 = g.H / 8;
-  const int vpt = (H8 + kThreads - 1) / kThreads;
-  const int grid = persistent_grid(g.a, 1);
-  if (vpt <= 1) MOE_SILU_QUANT(1);
-  else if (vpt <= 2) MOE_SILU_QUANT(2);
-  else if (vpt <= 3) MOE_SILU_QUANT(3);
-  else if (vpt <= 4) MOE_SILU_QUANT(4);
-  else if (vpt <= 6) MOE_SILU_QUANT(6);
-  else MOE_SILU_QUANT(8);
+  const int G = pick_group(H8);
+  const bool full = H8 > 32 * G * 4;
+  switch (G * 2 + (full ? 1 : 0)) {
+    case 2: MOE_SILU_QUANT(1, 4); break;
+    case 4: MOE_SILU_QUANT(2, 4); break;
+    case 8: MOE_SILU_QUANT(4, 4); break;
+    case 16: MOE_SILU_QUANT(8, 4); break;
+    default: MOE_SILU_QUANT(8, 8); break;  // rows past 8192 elements
+  }
   return cudaGetLastError();
 }
 
 cudaError_t launch_scatter_add(const ScatterArgs& g, cudaStream_t s) {
   const int D8 = g.D / 8;
   if (g.inv) {
-    const int grid = persistent_grid(g.T, kWarps);
     auto k = g.accumulate ? scatter_add_tokens_kernel<true> : scatter_add_tokens_kernel<false>;
+    const int grid = persistent_grid(k, (int64_t)g.T * ((D8 + kChunk - 1) / kChunk), kWarps);
     k<<<grid, kThreads, 0, s>>>(static_cast<uint4*>(g.out), static_cast<const uint4*>(g.in), g.inv, g.top_k, g.a,
                                 g.T, D8, g.valid, g.err);
   } else {
-    const int grid = persistent_grid(g.a, kWarps);
     auto k = g.accumulate ? scatter_add_rows_kernel<true> : scatter_add_rows_kernel<false>;
+    const int grid = persistent_grid(k, (int64_t)g.a * ((D8 + kChunk - 1) / kChunk), kWarps);
     k<<<grid, kThreads, 0, s>>>(static_cast<uint4*>(g.out), static_cast<const uint4*>(g.in), g.token_indices, g.a,
                                 g.T, D8, g.valid, g.err);
   }
