@@ -324,8 +324,10 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
 
     # algorithmic work per stage (one launch each per step)
     gemm1 = "gemm_w13" if cfg.fp8 else "gemm_w13_silu"
+    mlp_bytes = (active * 3 * H * D * wb + a * D * wb + a * H * 2 * 2 + a * D * 2)
     work = {
         "route": ("hbm", cfg.valid_tokens * E * 2 + a * 12 + 8 * (E + 1)),
+        "expert_mlp": ("gemm", mlp_bytes, 2.0 * a * 3 * H * D),
         ("gather_quant" if cfg.fp8 else "gather"): ("hbm", cfg.valid_tokens * D * 2 + a * D * wb + a * (14 if cfg.fp8 else 10)),
         gemm1: ("gemm", active * 2 * H * D * wb + a * D * wb + a * (2 * H * 2 if cfg.fp8 else H * 2),
                 2.0 * a * 2 * H * D),
@@ -335,6 +337,7 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
     if cfg.fp8:
         work["silu_quant"] = ("hbm", a * 2 * H * 2 + a * H + a * 4)
     peak_t = peaks["bf16_tflops_sustained"] * (FP8_OVER_BF16 if cfg.fp8 else 1.0)
+    gemm_stages = [n for n in stage_ms if work[n][0] == "gemm"]
     stages = {}
     for name, t in stage_ms.items():
         kind, *w = work[name]
@@ -376,13 +379,13 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
                    "parallelism": "replicas" if world == 1 else f"{world} independent replicas (weak scaling)"},
         "roofline": roof,
         "stages": stages,
-        "gemm_tflops": round(sum(work[n][2] for n in (gemm1, "gemm_w2")) /
-                             (sum(stage_ms[n] for n in (gemm1, "gemm_w2")) * 1e-3) / 1e12, 1),
+        "gemm_tflops": round(sum(work[n][2] for n in gemm_stages) / (sum(stage_ms[n] for n in gemm_stages) * 1e-3)
+                             / 1e12, 1),
         "e2e": None if e2e_ms is None else {
             "value": round(job_tokens_per_s(cfg.valid_tokens, world, e2e_ms), 1), "unit": UNIT,
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": layer.kernel_launches() * args.steps,
+        "gpu_launches": layer.kernel_launches(cfg.T) * args.steps,
         "clocks": clocks,
     }
     return res

@@ -230,6 +230,24 @@ int moe_grouped_gemm_fp8_rowwise(const void* x, const void* w, const int32_t* co
                                  const float* x_scale, const float* w_scale, int E, int a_max,
                                  int N, int K, void* y, int epilogue, cudaStream_t stream);
 
+/*
+ * Both grouped GEMMs of the bf16 routed experts in one persistent launch:
+ * z = moe_grouped_gemm(x, w13, counts, MOE_EPILOGUE_SILU_MUL) followed by
+ * y = moe_grouped_gemm(z, w2, counts) (the two GEMMs of
+ * MetaShufflingMoE._routed_expert with silu_mul between them).  Results are
+ * bit-identical to the two separate calls.  Each CTA works through its w13
+ * tiles, then its w2 tiles; a w2 tile of expert e starts once every w13 tile
+ * of e has stored its z rows, so the w2 work fills the tail of the w13 work.
+ * x [a_max, D], w13 [E, 2H, D], w2 [E, D, H], z [a_max, H] (written: it is
+ * the intermediate), y [a_max, D]; all bf16.  counts [E] device int32.
+ * ws: device workspace of moe_expert_mlp_workspace_size(E) bytes (contents on
+ * entry do not matter).  All CTAs must be resident at once (a cooperative
+ * launch); MOE_ERR_CUDA if the device cannot host them.  D, H multiples of 16.
+ */
+int moe_expert_mlp_workspace_size(int E, size_t* bytes);
+int moe_expert_mlp(const void* x, const void* w13, const void* w2, const int32_t* counts, int E, int a_max,
+                   int D, int H, void* z, void* y, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- silu_mul */
 
 /*

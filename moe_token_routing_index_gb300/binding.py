@@ -51,6 +51,8 @@ def _load() -> ctypes.CDLL:
         "moe_gather_scale_quant": ([P, I, I, P, P, I, P, I, L, L, I, P, P, P, P, P], I),
         "moe_quantize_rows": ([P, L, I, P, P, P, P], I),
         "moe_grouped_gemm": ([P, P, P, I, I, I, I, P, I, P], I),
+        "moe_expert_mlp_workspace_size": ([I, ctypes.POINTER(S)], I),
+        "moe_expert_mlp": ([P, P, P, P, I, I, I, I, P, P, P, S, P], I),
         "moe_grouped_gemm_fp8_rowwise": ([P, P, P, P, P, I, I, I, I, P, I, P], I),
         "moe_silu_mul": ([P, P, L, I, I, P, P, P], I),
         "moe_silu_mul_quant": ([P, P, L, I, I, P, P, P, P, P], I),
@@ -224,6 +226,32 @@ def moe_grouped_gemm_fp8_rowwise(x, w, counts, x_scale, w_scale, *, epilogue: in
     st = _lib.moe_grouped_gemm_fp8_rowwise(_ptr(x), _ptr(w), _ptr(counts), _ptr(x_scale), _ptr(w_scale), E, a_max,
                                            N, K, _ptr(out), epilogue, _stream(stream))
     _check("moe_grouped_gemm_fp8_rowwise", st)
+    return out
+
+
+def moe_expert_mlp_workspace_size(E: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check("moe_expert_mlp_workspace_size", _lib.moe_expert_mlp_workspace_size(E, ctypes.byref(n)))
+    return n.value
+
+
+def moe_expert_mlp(x, w13, w2, counts, *, z=None, out=None, workspace=None, stream=None):
+    """Both bf16 grouped GEMMs in one launch: z = silu_mul(x w13^T), out = z w2^T per expert."""
+    a_max, D = x.shape
+    E, n2, D2 = w13.shape
+    H = n2 // 2
+    assert D == D2 and tuple(w2.shape) == (E, D, H)
+    for t, n in ((x, "x"), (w13, "w13"), (w2, "w2")):
+        _need(t, torch.bfloat16, n)
+    if z is None:
+        z = torch.empty(a_max, H, dtype=torch.bfloat16, device=x.device)
+    if out is None:
+        out = torch.empty(a_max, D, dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(moe_expert_mlp_workspace_size(E), dtype=torch.uint8, device=x.device)
+    st = _lib.moe_expert_mlp(_ptr(x), _ptr(w13), _ptr(w2), _ptr(counts), E, a_max, D, H, _ptr(z), _ptr(out),
+                             _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("moe_expert_mlp", st)
     return out
 
 

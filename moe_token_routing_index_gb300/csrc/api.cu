@@ -257,6 +257,33 @@ static int grouped_gemm_common(const void* x, const void* w, const int32_t* coun
   return finish(e);
 }
 
+int moe_expert_mlp_workspace_size(int E, size_t* bytes) {
+  if (!bytes || E < 1) return MOE_ERR_INVALID;
+  if (E > 1024) return MOE_ERR_UNSUPPORTED;
+  *bytes = moe::expert_mlp_workspace_bytes(E);
+  return MOE_OK;
+}
+
+int moe_expert_mlp(const void* x, const void* w13, const void* w2, const int32_t* counts, int E, int a_max, int D,
+                   int H, void* z, void* y, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  size_t need;
+  int rc = moe_expert_mlp_workspace_size(E, &need);
+  if (rc != MOE_OK) return rc;
+  if (a_max < 0 || D < 0 || H < 0) return MOE_ERR_INVALID;
+  if (a_max == 0 || D == 0 || H == 0) return MOE_OK;
+  if (!x || !w13 || !w2 || !counts || !z || !y || !ws) return MOE_ERR_INVALID;
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE;
+  if (D % 16 != 0 || H % 16 != 0) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(w13) || !aligned16(w2) || !aligned16(z) || !aligned16(y) || !aligned16(ws))
+    return MOE_ERR_UNSUPPORTED;
+  moe::MlpArgs g{x, w13, w2, counts, E, a_max, D, H, z, y, ws, nullptr};
+  rc = device_error_word(&g.err);
+  if (rc != MOE_OK) return rc;
+  cudaError_t e = moe::launch_expert_mlp(g, stream);
+  if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
+  return finish(e);
+}
+
 int moe_grouped_gemm(const void* x, const void* w, const int32_t* counts, int E, int a_max, int N, int K, void* y,
                      int epilogue, cudaStream_t stream) {
   return grouped_gemm_common(x, w, counts, nullptr, nullptr, E, a_max, N, K, y, epilogue, false, stream);

@@ -212,11 +212,40 @@ __device__ __forceinline__ Tile decode_tile(int tile, int E, int n_tiles, const 
 
 // ----------------------------------------------------------------- kernel
 
-template <bool FP8, int EPI>
+// One grouped GEMM of a launch.  A launch runs one phase, or two: the w13 GEMM
+// (SiLU*mul epilogue into z) and then the w2 GEMM reading z.
+struct Phase {
+  int N, K;           // GEMM output columns (2H for SILU_MUL) and reduction length
+  int epi;            // MOE_EPILOGUE_*
+  int n_out;          // stored columns: N, or N / 2 for SILU_MUL
+  int n_tile_cols;    // stored columns per tile
+  int n_tiles;        // tiles along N
+  int num_kb;         // K blocks
+  __nv_bfloat16* y;   // [a_max, n_out]
+  const float* x_scale;
+  const float* w_scale;
+};
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+template <bool FP8, int NPHASE>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
-    const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-    const int32_t* __restrict__ counts, const float* __restrict__ x_scale, const float* __restrict__ w_scale, int E,
-    int a_max, int N, int K, __nv_bfloat16* __restrict__ y, unsigned int* err) {
+    const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_b0,
+    const __grid_constant__ CUtensorMap map_a1, const __grid_constant__ CUtensorMap map_b1,
+    const int32_t* __restrict__ counts, const Phase p0, const Phase p1, int E, int a_max, int* done,
+    unsigned int* err) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -250,8 +279,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     *s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    tma_prefetch_desc(&map_a);
-    tma_prefetch_desc(&map_b);
+    tma_prefetch_desc(&map_a0);
+    tma_prefetch_desc(&map_b0);
+    if (NPHASE == 2) {
+      tma_prefetch_desc(&map_a1);
+      tma_prefetch_desc(&map_b1);
+    }
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(s_tmem)),
@@ -311,12 +344,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   tc_fence_after();
 
   const uint32_t tmem_base = *s_tmem;
-  const int n_out = (EPI == MOE_EPILOGUE_SILU_MUL) ? N / 2 : N;
-  const int n_tile_cols = (EPI == MOE_EPILOGUE_SILU_MUL) ? kBN / 2 : kBN;  // output columns per tile
-  const int n_tiles = (n_out + n_tile_cols - 1) / n_tile_cols;
-  const int total_tiles = *s_total * n_tiles;
+  const int tiles0 = *s_total * p0.n_tiles;
+  const int total_tiles = tiles0 + (NPHASE == 2 ? *s_total * p1.n_tiles : 0);
   const int elems_per_kb = FP8 ? kBKBytes : kBKBytes / 2;
-  const int num_kb = (K + elems_per_kb - 1) / elems_per_kb;
+  // (phase, tile within the phase) of a tile id: phase-0 tiles come first.
+  auto locate = [&](int tile, int* ph) {
+    *ph = (NPHASE == 2 && tile >= tiles0) ? 1 : 0;
+    const Phase& p = *ph ? p1 : p0;
+    return decode_tile(*ph ? tile - tiles0 : tile, E, p.n_tiles, tile_start, row_off, mtiles);
+  };
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
@@ -326,16 +362,34 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       uint32_t issued_mask = 0, issued_parity = 0;  // per stage: issued since start, parity of that issue
       bool ok = true;
       for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-        const Tile t = decode_tile(tile, E, n_tiles, tile_start, row_off, mtiles);
+        int ph;
+        const Tile t = locate(tile, &ph);
+        const Phase& p = ph ? p1 : p0;
+        const CUtensorMap* ma = ph ? &map_a1 : &map_a0;
+        const CUtensorMap* mb = ph ? &map_b1 : &map_b0;
+        if (NPHASE == 2 && ph == 1) {
+          // z rows of this expert come from phase-0 tiles of other CTAs: wait
+          // until all of them (4 epilogue warps x row tiles x N tiles) are stored.
+          const int target = 4 * mtiles[t.expert] * p0.n_tiles;
+          const uint64_t t0 = global_timer_ns();
+          for (uint32_t i = 0; ld_acquire(done + t.expert) < target; ++i) {
+            if ((i & 63) == 63 && (*s_abort || global_timer_ns() - t0 > kWaitTimeoutNs)) {
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) break;
+          fence_proxy_async_global();  // the TMA reads below observe those stores
+        }
         int b_row0, b_row1;
-        if (EPI == MOE_EPILOGUE_SILU_MUL) {
-          b_row0 = t.expert * N + t.n_idx * (kBN / 2);
-          b_row1 = b_row0 + N / 2;
+        if (p.epi == MOE_EPILOGUE_SILU_MUL) {
+          b_row0 = t.expert * p.N + t.n_idx * (kBN / 2);
+          b_row1 = b_row0 + p.N / 2;
         } else {
-          b_row0 = t.expert * N + t.n_idx * kBN;
+          b_row0 = t.expert * p.N + t.n_idx * kBN;
           b_row1 = b_row0 + kBN / 2;
         }
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(bar_empty(s), phase ^ 1u, s_abort)) {
             ok = false;
             break;
@@ -344,9 +398,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
           const uint32_t b_dst = sbase + SmemLayout::b + s * kBBytes;
           mbar_arrive_expect_tx(bar_full(s), kStageBytes);
           const int kc = kb * elems_per_kb;
-          tma_load_2d(a_dst, &map_a, bar_full(s), kc, t.row0);
-          tma_load_2d(b_dst, &map_b, bar_full(s), kc, b_row0);
-          tma_load_2d(b_dst + kBBytes / 2, &map_b, bar_full(s), kc, b_row1);
+          tma_load_2d(a_dst, ma, bar_full(s), kc, t.row0);
+          tma_load_2d(b_dst, mb, bar_full(s), kc, b_row0);
+          tma_load_2d(b_dst + kBBytes / 2, mb, bar_full(s), kc, b_row1);
           issued_mask |= 1u << s;
           issued_parity = (issued_parity & ~(1u << s)) | (phase << s);
           if (++s == kStages) {
@@ -373,6 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       uint32_t acc_phase = 0;
       bool ok = true, issued_any = false;
       for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+        const int num_kb = (NPHASE == 2 && tile >= tiles0) ? p1.num_kb : p0.num_kb;
         if (!mbar_wait(bar_tempty(acc), acc_phase ^ 1u, s_abort)) {
           ok = false;
           break;
@@ -422,7 +477,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-      const Tile t = decode_tile(tile, E, n_tiles, tile_start, row_off, mtiles);
+      int ph;
+      const Tile t = locate(tile, &ph);
+      const Phase& p = ph ? p1 : p0;
       if (!mbar_wait(bar_tfull(acc), acc_phase, s_abort)) {
         if (lane == 0) flag_error(err, MOE_DEVERR_TIMEOUT);
         *s_abort = 1;
@@ -432,13 +489,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * kBN);
       const bool row_ok = row_in_tile < t.rows;
       const int row = t.row0 + row_in_tile;
+      const int n_out = p.n_out;
       float xs = 1.0f;
-      if (FP8 && row_ok) xs = __ldg(x_scale + row);
-      __nv_bfloat16* yrow = y + (int64_t)row * n_out;
-      const int col0 = t.n_idx * n_tile_cols;
-      const float* wsc = FP8 ? w_scale + (int64_t)t.expert * N : nullptr;
-      if (EPI == MOE_EPILOGUE_SILU_MUL) {
-        const int H = N / 2;
+      if (FP8 && row_ok) xs = __ldg(p.x_scale + row);
+      __nv_bfloat16* yrow = p.y + (int64_t)row * n_out;
+      const int col0 = t.n_idx * p.n_tile_cols;
+      const float* wsc = FP8 ? p.w_scale + (int64_t)t.expert * p.N : nullptr;
+      if (p.epi == MOE_EPILOGUE_SILU_MUL) {
+        const int H = p.N / 2;
 #pragma unroll 1
         for (int c = 0; c < kBN / 2; c += 32) {
           float v0[32], v1[32];
@@ -486,6 +544,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
         }
       }
       tc_fence_before();
+      if (NPHASE == 2 && ph == 0) {
+        // publish this warp's share of the tile's z rows to the phase-1 producers
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+          fence_proxy_async_global();
+          red_release_add(done + t.expert, 1);
+        }
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_tempty(acc));
       if (++acc == kAccBufs) {
@@ -535,24 +602,52 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, bo
   return r == CUDA_SUCCESS;
 }
 
-template <bool FP8, int EPI>
-cudaError_t launch_impl(const GemmArgs& g, cudaStream_t s) {
-  CUtensorMap ma, mb;
-  if (!make_map(&ma, g.x, g.a_max, g.K, FP8) || !make_map(&mb, g.w, (int64_t)g.E * g.N, g.K, FP8))
-    return cudaErrorInvalidValue;
-  const int smem = SmemLayout::bytes_for(g.E) + 1024;
-  auto kern = grouped_gemm_kernel<FP8, EPI>;
+Phase make_phase(int N, int K, int epi, bool fp8, void* y, const float* xs, const float* ws) {
+  Phase p;
+  p.N = N;
+  p.K = K;
+  p.epi = epi;
+  p.n_out = epi == MOE_EPILOGUE_SILU_MUL ? N / 2 : N;
+  p.n_tile_cols = epi == MOE_EPILOGUE_SILU_MUL ? kBN / 2 : kBN;
+  p.n_tiles = (p.n_out + p.n_tile_cols - 1) / p.n_tile_cols;
+  const int elems = fp8 ? kBKBytes : kBKBytes / 2;
+  p.num_kb = (K + elems - 1) / elems;
+  p.y = static_cast<__nv_bfloat16*>(y);
+  p.x_scale = xs;
+  p.w_scale = ws;
+  return p;
+}
+
+template <bool FP8, int NPHASE>
+cudaError_t launch_phases(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1,
+                          const CUtensorMap& b1, const int32_t* counts, const Phase& p0, const Phase& p1, int E,
+                          int a_max, int* done, unsigned int* err, cudaStream_t s) {
+  const int smem = SmemLayout::bytes_for(E) + 1024;
+  auto kern = grouped_gemm_kernel<FP8, NPHASE>;
   // The attribute is per device; setting it on every call is cheap and keeps multi-device use correct.
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int n_out = (EPI == MOE_EPILOGUE_SILU_MUL) ? g.N / 2 : g.N;
-  const int n_tile_cols = (EPI == MOE_EPILOGUE_SILU_MUL) ? kBN / 2 : kBN;
-  const int64_t n_tiles = (n_out + n_tile_cols - 1) / n_tile_cols;
-  const int64_t tiles_ub = ((int64_t)(g.a_max + kBM - 1) / kBM + g.E) * n_tiles;
+  int64_t tiles_ub = 0;
+  const int64_t mt_ub = (int64_t)(a_max + kBM - 1) / kBM + E;
+  tiles_ub += mt_ub * p0.n_tiles;
+  if (NPHASE == 2) tiles_ub += mt_ub * p1.n_tiles;
   const int sms = device_sm_count();
   const int grid = (int)(tiles_ub < sms ? tiles_ub : sms);
-  kern<<<grid, kThreads, smem, s>>>(ma, mb, g.counts, g.x_scale, g.w_scale, g.E, g.a_max, g.N, g.K,
-                                    static_cast<__nv_bfloat16*>(g.y), g.err);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (NPHASE == 2) {
+    // phase-1 tiles wait on phase-0 tiles of other CTAs: all CTAs must be resident at once
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  e = cudaLaunchKernelEx(&cfg, kern, a0, b0, a1, b1, counts, p0, p1, E, a_max, done, err);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -560,12 +655,28 @@ cudaError_t launch_impl(const GemmArgs& g, cudaStream_t s) {
 
 cudaError_t launch_grouped_gemm(const GemmArgs& g, cudaStream_t s) {
   if (g.E > kMaxExperts) return cudaErrorNotSupported;
-  if (g.fp8) {
-    if (g.epilogue == MOE_EPILOGUE_SILU_MUL) return launch_impl<true, MOE_EPILOGUE_SILU_MUL>(g, s);
-    return launch_impl<true, MOE_EPILOGUE_NONE>(g, s);
-  }
-  if (g.epilogue == MOE_EPILOGUE_SILU_MUL) return launch_impl<false, MOE_EPILOGUE_SILU_MUL>(g, s);
-  return launch_impl<false, MOE_EPILOGUE_NONE>(g, s);
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, g.x, g.a_max, g.K, g.fp8) || !make_map(&mb, g.w, (int64_t)g.E * g.N, g.K, g.fp8))
+    return cudaErrorInvalidValue;
+  const Phase p = make_phase(g.N, g.K, g.epilogue, g.fp8, g.y, g.x_scale, g.w_scale);
+  if (g.fp8) return launch_phases<true, 1>(ma, mb, ma, mb, g.counts, p, p, g.E, g.a_max, nullptr, g.err, s);
+  return launch_phases<false, 1>(ma, mb, ma, mb, g.counts, p, p, g.E, g.a_max, nullptr, g.err, s);
+}
+
+size_t expert_mlp_workspace_bytes(int E) { return ((size_t)E * sizeof(int) + 255) / 256 * 256; }
+
+cudaError_t launch_expert_mlp(const MlpArgs& g, cudaStream_t s) {
+  if (g.E > kMaxExperts) return cudaErrorNotSupported;
+  CUtensorMap a0, b0, a1, b1;
+  if (!make_map(&a0, g.x, g.a_max, g.D, false) || !make_map(&b0, g.w13, (int64_t)g.E * 2 * g.H, g.D, false) ||
+      !make_map(&a1, g.z, g.a_max, g.H, false) || !make_map(&b1, g.w2, (int64_t)g.E * g.D, g.H, false))
+    return cudaErrorInvalidValue;
+  const Phase p0 = make_phase(2 * g.H, g.D, MOE_EPILOGUE_SILU_MUL, false, g.z, nullptr, nullptr);
+  const Phase p1 = make_phase(g.D, g.H, MOE_EPILOGUE_NONE, false, g.y, nullptr, nullptr);
+  int* done = static_cast<int*>(g.ws);
+  cudaError_t e = cudaMemsetAsync(done, 0, sizeof(int) * g.E, s);
+  if (e != cudaSuccess) return e;
+  return launch_phases<false, 2>(a0, b0, a1, b1, g.counts, p0, p1, g.E, g.a_max, done, g.err, s);
 }
 
 }  // namespace moe

@@ -91,6 +91,22 @@ struct GemmArgs {
 
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s);
 
+// Both grouped GEMMs of a bf16 expert MLP in one launch (w13 with SiLU*mul into z, then w2).
+struct MlpArgs {
+  const void* x;        // [a_max, D] bf16
+  const void* w13;      // [E, 2H, D]
+  const void* w2;       // [E, D, H]
+  const int32_t* counts;
+  int E, a_max, D, H;
+  void* z;              // [a_max, H] bf16
+  void* y;              // [a_max, D] bf16
+  void* ws;             // expert_mlp_workspace_bytes(E)
+  unsigned int* err;
+};
+
+size_t expert_mlp_workspace_bytes(int E);
+cudaError_t launch_expert_mlp(const MlpArgs& a, cudaStream_t s);
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 

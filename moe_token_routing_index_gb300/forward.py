@@ -4,7 +4,8 @@ Stage order of mslk/moe/layers.py, MetaShufflingMoE._no_comm_forward
 (routed experts, no shared expert):
 
   bf16:  route -> gather*score -> grouped GEMM w13 with the SiLU*mul epilogue
-         -> grouped GEMM w2 -> scatter-add
+         -> grouped GEMM w2 -> scatter-add (both GEMMs in one persistent launch,
+         moe_expert_mlp, when the layer streams its weights: T*top_k <= 128*E)
   FP8:   route -> gather*score -> e4m3 rows -> grouped GEMM w13 (FP8 rowwise)
          -> silu_mul_quant -> grouped GEMM w2 (FP8 rowwise) -> scatter-add
 
@@ -30,6 +31,7 @@ class _Buffers:
     T: int
     route: dict
     ws: torch.Tensor
+    mlp_ws: torch.Tensor
     xr: torch.Tensor              # routed rows: bf16 [T*k, D] or e4m3 [T*k, D]
     xs: torch.Tensor | None       # FP8: row scales [T*k]
     y: torch.Tensor | None        # FP8: GEMM1 output bf16 [T*k, 2H]
@@ -46,7 +48,8 @@ class MoELayer:
     """
 
     def __init__(self, top_k: int, w13: torch.Tensor, w2: torch.Tensor, w13_scale: torch.Tensor | None = None,
-                 w2_scale: torch.Tensor | None = None, scale_ub: float | None = None):
+                 w2_scale: torch.Tensor | None = None, scale_ub: float | None = None,
+                 fused_mlp: bool | None = None):
         self.E, n2, self.D = w13.shape
         self.H = n2 // 2
         assert w2.shape == (self.E, self.D, self.H), "w2 must be [E, D, H]"
@@ -59,17 +62,20 @@ class MoELayer:
         self.w2_scale = None if w2_scale is None else w2_scale.contiguous()
         dev = w13.device
         self.scale_ub = None if scale_ub is None else torch.tensor([scale_ub], dtype=torch.float32, device=dev)
+        # None: one launch for both bf16 GEMMs when the batch averages at most one
+        # 128-row tile per expert (weight-streaming, HBM-bound), else two launches.
+        self.fused_mlp = fused_mlp
         self._bufs: _Buffers | None = None
 
     @classmethod
-    def from_weights(cls, cfg: MoEConfig, w13: torch.Tensor, w2: torch.Tensor) -> "MoELayer":
+    def from_weights(cls, cfg: MoEConfig, w13: torch.Tensor, w2: torch.Tensor, **kw) -> "MoELayer":
         """bf16 weights as they are; fp32 weights of an FP8 layer are quantised
         per row on the device (moe_quantize_rows)."""
         if cfg.fp8:
             w13q, w13s = mb.moe_quantize_rows(w13.float().contiguous())
             w2q, w2s = mb.moe_quantize_rows(w2.float().contiguous())
-            return cls(cfg.top_k, w13q, w2q, w13s, w2s, scale_ub=cfg.scale_ub)
-        return cls(cfg.top_k, w13.to(torch.bfloat16), w2.to(torch.bfloat16), scale_ub=cfg.scale_ub)
+            return cls(cfg.top_k, w13q, w2q, w13s, w2s, scale_ub=cfg.scale_ub, **kw)
+        return cls(cfg.top_k, w13.to(torch.bfloat16), w2.to(torch.bfloat16), scale_ub=cfg.scale_ub, **kw)
 
     # ------------------------------------------------------------ buffers
     def buffers(self, T: int, device) -> _Buffers:
@@ -82,15 +88,16 @@ class MoELayer:
                      expert_indices=torch.zeros(a, **i32), token_indices=torch.zeros(a, **i32),
                      inv_rows=torch.zeros(a, **i32))
         ws = torch.empty(max(mb.moe_route_workspace_size(T, E, k), 256), dtype=torch.uint8, device=device)
+        mlp_ws = torch.empty(mb.moe_expert_mlp_workspace_size(E), dtype=torch.uint8, device=device)
         if self.fp8:
             e4 = dict(dtype=torch.float8_e4m3fn, device=device)
             f32 = dict(dtype=torch.float32, device=device)
-            b = _Buffers(T, route, ws, torch.empty(a, D, **e4), torch.empty(a, **f32),
+            b = _Buffers(T, route, ws, mlp_ws, torch.empty(a, D, **e4), torch.empty(a, **f32),
                          torch.empty(a, 2 * H, dtype=torch.bfloat16, device=device), torch.empty(a, H, **e4),
                          torch.empty(a, **f32), torch.empty(a, D, dtype=torch.bfloat16, device=device))
         else:
             bf = dict(dtype=torch.bfloat16, device=device)
-            b = _Buffers(T, route, ws, torch.empty(a, D, **bf), None, None, torch.empty(a, H, **bf), None,
+            b = _Buffers(T, route, ws, mlp_ws, torch.empty(a, D, **bf), None, None, torch.empty(a, H, **bf), None,
                          torch.empty(a, D, **bf))
         self._bufs = b
         return b
@@ -109,12 +116,16 @@ class MoELayer:
         k = self.top_k
         st = [("route", lambda: mb.moe_route(scores, k, num_valid_tokens, out=r, workspace=b.ws))]
         if not self.fp8:
-            st += [
-                ("gather", lambda: mb.moe_gather_scale(x, ti, ei, scores, valid, out=b.xr)),
-                ("gemm_w13_silu", lambda: mb.moe_grouped_gemm(b.xr, self.w13, counts,
-                                                              epilogue=mb.MOE_EPILOGUE_SILU_MUL, out=b.z)),
-                ("gemm_w2", lambda: mb.moe_grouped_gemm(b.z, self.w2, counts, out=b.o)),
-            ]
+            st.append(("gather", lambda: mb.moe_gather_scale(x, ti, ei, scores, valid, out=b.xr)))
+            if self.use_fused_mlp(T):
+                st.append(("expert_mlp", lambda: mb.moe_expert_mlp(b.xr, self.w13, self.w2, counts, z=b.z, out=b.o,
+                                                                   workspace=b.mlp_ws)))
+            else:
+                st += [
+                    ("gemm_w13_silu", lambda: mb.moe_grouped_gemm(b.xr, self.w13, counts,
+                                                                  epilogue=mb.MOE_EPILOGUE_SILU_MUL, out=b.z)),
+                    ("gemm_w2", lambda: mb.moe_grouped_gemm(b.z, self.w2, counts, out=b.o)),
+                ]
         else:
             st += [
                 ("gather_quant", lambda: mb.moe_gather_scale_quant(x, ti, ei, scores, self.scale_ub, valid,
@@ -140,6 +151,18 @@ class MoELayer:
             launch()
         return out
 
-    def kernel_launches(self) -> int:
-        """Kernels one forward launches (routing takes three)."""
-        return 7 if not self.fp8 else 8
+    def use_fused_mlp(self, T: int) -> bool:
+        if self.fp8:
+            return False
+        if self.fused_mlp is not None:
+            return self.fused_mlp
+        return T * self.top_k <= 128 * self.E
+
+    def kernel_launches(self, T: int | None = None) -> int:
+        """Kernels one forward launches: routing (1 for small batches, else 3),
+        gather, the GEMMs (1 fused, or 2), silu_mul_quant (FP8), scatter."""
+        T = self._bufs.T if T is None and self._bufs is not None else (T or 0)
+        route = 1 if (T <= 1024 and T * self.E <= 16384 and T * self.top_k <= 8192 and self.E <= 256) else 3
+        if self.fp8:
+            return route + 5
+        return route + 1 + (1 if self.use_fused_mlp(T) else 2) + 1

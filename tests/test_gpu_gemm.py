@@ -172,3 +172,44 @@ def test_grouped_gemm_bf16_workloads_sampled(name):
     assert torch.equal(z, mb.moe_silu_mul(y, cfg.H))
     o_ref = oracle.grouped_gemm_bf16(bits(z)[rows], w2_u, sub_cnt)
     _check_close(bits(o[rows]), o_ref, _abs_bound_bf16(bits(z)[rows], w2_u, sub_cnt))
+
+
+@pytest.mark.parametrize("E,counts,D,H,a_max", [(1, [128], 64, 128, None), (3, [5, 0, 130], 256, 512, None),
+                                                (5, [300, 17, 0, 64, 250], 272, 528, 700),
+                                                (16, [8] * 12 + [0] * 4, 512, 1024, 130)])
+def test_expert_mlp_one_launch_equals_two(E, counts, D, H, a_max):
+    """moe_expert_mlp (both GEMMs in one persistent launch) equals the two calls bit for bit."""
+    mb = _mb()
+    g = torch.Generator().manual_seed(D + H)
+    a = int(sum(counts))
+    a_max = a if a_max is None else a_max
+    x = torch.randn(a_max, D, generator=g).to(torch.bfloat16).cuda()
+    w13 = (torch.randn(E, 2 * H, D, generator=g) * 0.1).to(torch.bfloat16).cuda()
+    w2 = (torch.randn(E, D, H, generator=g) * 0.1).to(torch.bfloat16).cuda()
+    cd = torch.tensor(counts, dtype=torch.int32, device="cuda")
+    z_ref = mb.moe_grouped_gemm(x, w13, cd, epilogue=mb.MOE_EPILOGUE_SILU_MUL)
+    y_ref = mb.moe_grouped_gemm(z_ref, w2, cd)
+    y = sentinel_like((a_max, D), torch.bfloat16)
+    z = torch.empty(a_max, H, dtype=torch.bfloat16, device="cuda")
+    for _ in range(2):   # the workspace is reused as it is left
+        mb.moe_expert_mlp(x, w13, w2, cd, z=z, out=y)
+    assert mb.device_error() == 0
+    assert torch.equal(y[:a], y_ref[:a]) and torch.equal(z[:a], z_ref[:a])
+    assert is_sentinel(y[a:])
+
+
+@pytest.mark.parametrize("name", ["decode", "fine_grained"])
+def test_expert_mlp_workloads_equal_two_launches(name):
+    mb = _mb()
+    cfg = workloads.CONFIGS[name]
+    r = oracle.route(bits(workloads.make_scores(cfg)), cfg.top_k, cfg.valid_tokens)
+    cnt = torch.from_numpy(r["counts"][:cfg.E].copy()).cuda()
+    a = cfg.routed_rows
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(a, cfg.D, generator=g).to(torch.bfloat16).cuda()
+    w13, w2 = workloads.make_weights(cfg, device="cuda")
+    z_ref = mb.moe_grouped_gemm(x, w13, cnt, epilogue=mb.MOE_EPILOGUE_SILU_MUL)
+    y_ref = mb.moe_grouped_gemm(z_ref, w2, cnt)
+    y = mb.moe_expert_mlp(x, w13, w2, cnt)
+    assert mb.device_error() == 0
+    assert torch.equal(y, y_ref)
