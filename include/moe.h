@@ -214,9 +214,19 @@ int moe_quantize_rows(const float* w, int64_t rows, int cols, const float* scale
  * the number of routed rows; rows past it are not written).  Runs on the
  * tensor cores (tcgen05, accumulators in tensor memory, TMA-fed).
  * Requires N, K multiples of 16 (H a multiple of 16 for SILU_MUL), E <= 1024.
+ *
+ * scatter_indices (nullable; MOE_EPILOGUE_NONE only): the combine fused into
+ * the epilogue, grouped_gemm(..., _output_tensor=out,
+ * _scatter_add_indices=token_indices) of _routed_expert, for top_k = 1 where
+ * every token has exactly one routed row.  y is then out [T_out, N]; routed
+ * row r's bf16 result o goes to y[scatter_indices[r], :]: y = bf16(f32(y) +
+ * f32(o)) with accumulate != 0 (moe_scatter_add's arithmetic), y = o with
+ * accumulate == 0.  Rows of y that no routed row names are not touched; an
+ * index outside [0, T_out) is skipped and flagged.
  */
 int moe_grouped_gemm(const void* x, const void* w, const int32_t* counts, int E, int a_max, int N,
-                     int K, void* y, int epilogue, cudaStream_t stream);
+                     int K, void* y, int epilogue, const int32_t* scatter_indices, int T_out,
+                     int accumulate, cudaStream_t stream);
 
 /*
  * grouped_gemm_fp8_rowwise(x, w, counts, x_scale, w_scale) of
@@ -224,11 +234,12 @@ int moe_grouped_gemm(const void* x, const void* w, const int32_t* counts, int E,
  *   v[r, n] = (sum_k x[r, k] * w[e, n, k]) * x_scale[r] * w_scale[e * N + n]
  * (fp32; the dequantisation order of BaselineMoE._fake_quant).
  * x [a_max, K] e4m3, w [E, N, K] e4m3, x_scale [a_max] fp32, w_scale [E * N]
- * fp32.  Epilogues as in moe_grouped_gemm.
+ * fp32.  Epilogues and the fused combine as in moe_grouped_gemm.
  */
 int moe_grouped_gemm_fp8_rowwise(const void* x, const void* w, const int32_t* counts,
                                  const float* x_scale, const float* w_scale, int E, int a_max,
-                                 int N, int K, void* y, int epilogue, cudaStream_t stream);
+                                 int N, int K, void* y, int epilogue, const int32_t* scatter_indices,
+                                 int T_out, int accumulate, cudaStream_t stream);
 
 /*
  * Both grouped GEMMs of the bf16 routed experts in one persistent launch:
@@ -243,10 +254,13 @@ int moe_grouped_gemm_fp8_rowwise(const void* x, const void* w, const int32_t* co
  * ws: device workspace of moe_expert_mlp_workspace_size(E) bytes (contents on
  * entry do not matter).  All CTAs must be resident at once (a cooperative
  * launch); MOE_ERR_CUDA if the device cannot host them.  D, H multiples of 16.
+ * scatter_indices, T_out, accumulate: the fused top_k = 1 combine of the w2
+ * GEMM, as in moe_grouped_gemm (y is then out [T_out, D]).
  */
 int moe_expert_mlp_workspace_size(int E, size_t* bytes);
 int moe_expert_mlp(const void* x, const void* w13, const void* w2, const int32_t* counts, int E, int a_max,
-                   int D, int H, void* z, void* y, void* ws, size_t ws_bytes, cudaStream_t stream);
+                   int D, int H, void* z, void* y, const int32_t* scatter_indices, int T_out, int accumulate,
+                   void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* ---------------------------------------------------------------- silu_mul */
 

@@ -50,10 +50,10 @@ def _load() -> ctypes.CDLL:
         "moe_gather_scale": ([P, I, I, P, P, I, P, I, L, L, I, P, P, P], I),
         "moe_gather_scale_quant": ([P, I, I, P, P, I, P, I, L, L, I, P, P, P, P, P], I),
         "moe_quantize_rows": ([P, L, I, P, P, P, P], I),
-        "moe_grouped_gemm": ([P, P, P, I, I, I, I, P, I, P], I),
+        "moe_grouped_gemm": ([P, P, P, I, I, I, I, P, I, P, I, I, P], I),
         "moe_expert_mlp_workspace_size": ([I, ctypes.POINTER(S)], I),
-        "moe_expert_mlp": ([P, P, P, P, I, I, I, I, P, P, P, S, P], I),
-        "moe_grouped_gemm_fp8_rowwise": ([P, P, P, P, P, I, I, I, I, P, I, P], I),
+        "moe_expert_mlp": ([P, P, P, P, I, I, I, I, P, P, P, I, I, P, S, P], I),
+        "moe_grouped_gemm_fp8_rowwise": ([P, P, P, P, P, I, I, I, I, P, I, P, I, I, P], I),
         "moe_silu_mul": ([P, P, L, I, I, P, P, P], I),
         "moe_silu_mul_quant": ([P, P, L, I, I, P, P, P, P, P], I),
         "moe_scatter_add": ([P, P, P, P, I, I, I, I, P, I, P], I),
@@ -198,33 +198,46 @@ def moe_quantize_rows(w: torch.Tensor, scale_ub=None, *, out=None, out_scale=Non
 
 # ------------------------------------------------------------- grouped GEMM
 
-def moe_grouped_gemm(x, w, counts, *, epilogue: int = MOE_EPILOGUE_NONE, out=None, stream=None):
-    """x[a_max, K] bf16, w[E, N, K] bf16, counts[>= E] int32 -> y[a_max, N or N/2]."""
+def _scatter_args(scatter_indices, out, accumulate):
+    if scatter_indices is None:
+        return None, 0, 0
+    if out is None:
+        raise ValueError("the fused combine writes into a caller-provided out[T, N]")
+    return scatter_indices, out.shape[0], int(accumulate)
+
+
+def moe_grouped_gemm(x, w, counts, *, epilogue: int = MOE_EPILOGUE_NONE, out=None, scatter_indices=None,
+                     accumulate: bool = True, stream=None):
+    """x[a_max, K] bf16, w[E, N, K] bf16, counts[>= E] int32 -> y[a_max, N or N/2].
+    With scatter_indices (top_k = 1), routed row r lands in out[scatter_indices[r]]."""
     a_max, K = x.shape
     E, N, K2 = w.shape
     assert K == K2
     _need(x, torch.bfloat16, "x")
     _need(w, torch.bfloat16, "w")
     n_out = N // 2 if epilogue == MOE_EPILOGUE_SILU_MUL else N
+    si, t_out, acc = _scatter_args(scatter_indices, out, accumulate)
     if out is None:
         out = torch.empty(a_max, n_out, dtype=torch.bfloat16, device=x.device)
-    st = _lib.moe_grouped_gemm(_ptr(x), _ptr(w), _ptr(counts), E, a_max, N, K, _ptr(out), epilogue, _stream(stream))
+    st = _lib.moe_grouped_gemm(_ptr(x), _ptr(w), _ptr(counts), E, a_max, N, K, _ptr(out), epilogue, _ptr(si),
+                               t_out, acc, _stream(stream))
     _check("moe_grouped_gemm", st)
     return out
 
 
 def moe_grouped_gemm_fp8_rowwise(x, w, counts, x_scale, w_scale, *, epilogue: int = MOE_EPILOGUE_NONE, out=None,
-                                 stream=None):
+                                 scatter_indices=None, accumulate: bool = True, stream=None):
     a_max, K = x.shape
     E, N, K2 = w.shape
     assert K == K2
     _need(x, torch.float8_e4m3fn, "x")
     _need(w, torch.float8_e4m3fn, "w")
     n_out = N // 2 if epilogue == MOE_EPILOGUE_SILU_MUL else N
+    si, t_out, acc = _scatter_args(scatter_indices, out, accumulate)
     if out is None:
         out = torch.empty(a_max, n_out, dtype=torch.bfloat16, device=x.device)
     st = _lib.moe_grouped_gemm_fp8_rowwise(_ptr(x), _ptr(w), _ptr(counts), _ptr(x_scale), _ptr(w_scale), E, a_max,
-                                           N, K, _ptr(out), epilogue, _stream(stream))
+                                           N, K, _ptr(out), epilogue, _ptr(si), t_out, acc, _stream(stream))
     _check("moe_grouped_gemm_fp8_rowwise", st)
     return out
 
@@ -235,8 +248,10 @@ def moe_expert_mlp_workspace_size(E: int) -> int:
     return n.value
 
 
-def moe_expert_mlp(x, w13, w2, counts, *, z=None, out=None, workspace=None, stream=None):
-    """Both bf16 grouped GEMMs in one launch: z = silu_mul(x w13^T), out = z w2^T per expert."""
+def moe_expert_mlp(x, w13, w2, counts, *, z=None, out=None, scatter_indices=None, accumulate: bool = True,
+                   workspace=None, stream=None):
+    """Both bf16 grouped GEMMs in one launch: z = silu_mul(x w13^T), out = z w2^T per expert
+    (with scatter_indices, top_k = 1: row r lands in out[scatter_indices[r]])."""
     a_max, D = x.shape
     E, n2, D2 = w13.shape
     H = n2 // 2
@@ -245,12 +260,13 @@ def moe_expert_mlp(x, w13, w2, counts, *, z=None, out=None, workspace=None, stre
         _need(t, torch.bfloat16, n)
     if z is None:
         z = torch.empty(a_max, H, dtype=torch.bfloat16, device=x.device)
+    si, t_out, acc = _scatter_args(scatter_indices, out, accumulate)
     if out is None:
         out = torch.empty(a_max, D, dtype=torch.bfloat16, device=x.device)
     if workspace is None:
         workspace = torch.empty(moe_expert_mlp_workspace_size(E), dtype=torch.uint8, device=x.device)
     st = _lib.moe_expert_mlp(_ptr(x), _ptr(w13), _ptr(w2), _ptr(counts), E, a_max, D, H, _ptr(z), _ptr(out),
-                             _ptr(workspace), workspace.numel(), _stream(stream))
+                             _ptr(si), t_out, acc, _ptr(workspace), workspace.numel(), _stream(stream))
     _check("moe_expert_mlp", st)
     return out
 

@@ -239,7 +239,8 @@ int moe_scatter_add(void* out, const void* in, const int32_t* token_indices, con
 
 static int grouped_gemm_common(const void* x, const void* w, const int32_t* counts, const float* x_scale,
                                const float* w_scale, int E, int a_max, int N, int K, void* y, int epilogue,
-                               bool fp8, cudaStream_t stream) {
+                               const int32_t* scatter, int T_out, int accumulate, bool fp8,
+                               cudaStream_t stream) {
   if (E < 1 || a_max < 0 || N < 0 || K < 0) return MOE_ERR_INVALID;
   if (epilogue != MOE_EPILOGUE_NONE && epilogue != MOE_EPILOGUE_SILU_MUL) return MOE_ERR_INVALID;
   if (a_max == 0 || N == 0) return MOE_OK;
@@ -249,7 +250,9 @@ static int grouped_gemm_common(const void* x, const void* w, const int32_t* coun
   if (N % 16 != 0 || K % 16 != 0 || K == 0) return MOE_ERR_UNSUPPORTED;
   if (epilogue == MOE_EPILOGUE_SILU_MUL && (N % 32 != 0)) return MOE_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return MOE_ERR_UNSUPPORTED;
-  moe::GemmArgs g{x, w, counts, x_scale, w_scale, E, a_max, N, K, y, epilogue, fp8, nullptr};
+  if (scatter && (epilogue != MOE_EPILOGUE_NONE || T_out < 0)) return MOE_ERR_INVALID;
+  moe::GemmArgs g{x, w, counts, x_scale, w_scale, E, a_max, N, K, y, epilogue, fp8, scatter, T_out, accumulate,
+                  nullptr};
   int rc = device_error_word(&g.err);
   if (rc != MOE_OK) return rc;
   cudaError_t e = moe::launch_grouped_gemm(g, stream);
@@ -265,7 +268,8 @@ int moe_expert_mlp_workspace_size(int E, size_t* bytes) {
 }
 
 int moe_expert_mlp(const void* x, const void* w13, const void* w2, const int32_t* counts, int E, int a_max, int D,
-                   int H, void* z, void* y, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                   int H, void* z, void* y, const int32_t* scatter_indices, int T_out, int accumulate, void* ws,
+                   size_t ws_bytes, cudaStream_t stream) {
   size_t need;
   int rc = moe_expert_mlp_workspace_size(E, &need);
   if (rc != MOE_OK) return rc;
@@ -276,7 +280,8 @@ int moe_expert_mlp(const void* x, const void* w13, const void* w2, const int32_t
   if (D % 16 != 0 || H % 16 != 0) return MOE_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(w13) || !aligned16(w2) || !aligned16(z) || !aligned16(y) || !aligned16(ws))
     return MOE_ERR_UNSUPPORTED;
-  moe::MlpArgs g{x, w13, w2, counts, E, a_max, D, H, z, y, ws, nullptr};
+  if (scatter_indices && T_out < 0) return MOE_ERR_INVALID;
+  moe::MlpArgs g{x, w13, w2, counts, E, a_max, D, H, z, y, ws, scatter_indices, T_out, accumulate, nullptr};
   rc = device_error_word(&g.err);
   if (rc != MOE_OK) return rc;
   cudaError_t e = moe::launch_expert_mlp(g, stream);
@@ -285,14 +290,16 @@ int moe_expert_mlp(const void* x, const void* w13, const void* w2, const int32_t
 }
 
 int moe_grouped_gemm(const void* x, const void* w, const int32_t* counts, int E, int a_max, int N, int K, void* y,
-                     int epilogue, cudaStream_t stream) {
-  return grouped_gemm_common(x, w, counts, nullptr, nullptr, E, a_max, N, K, y, epilogue, false, stream);
+                     int epilogue, const int32_t* scatter_indices, int T_out, int accumulate, cudaStream_t stream) {
+  return grouped_gemm_common(x, w, counts, nullptr, nullptr, E, a_max, N, K, y, epilogue, scatter_indices, T_out,
+                             accumulate, false, stream);
 }
 
 int moe_grouped_gemm_fp8_rowwise(const void* x, const void* w, const int32_t* counts, const float* x_scale,
                                  const float* w_scale, int E, int a_max, int N, int K, void* y, int epilogue,
-                                 cudaStream_t stream) {
-  return grouped_gemm_common(x, w, counts, x_scale, w_scale, E, a_max, N, K, y, epilogue, true, stream);
+                                 const int32_t* scatter_indices, int T_out, int accumulate, cudaStream_t stream) {
+  return grouped_gemm_common(x, w, counts, x_scale, w_scale, E, a_max, N, K, y, epilogue, scatter_indices, T_out,
+                             accumulate, true, stream);
 }
 
 }  // extern "C"

@@ -221,9 +221,12 @@ struct Phase {
   int n_tile_cols;    // stored columns per tile
   int n_tiles;        // tiles along N
   int num_kb;         // K blocks
-  __nv_bfloat16* y;   // [a_max, n_out]
+  __nv_bfloat16* y;   // [a_max, n_out], or [T_out, n_out] when scattering
   const float* x_scale;
   const float* w_scale;
+  const int32_t* scatter;  // NONE epilogue only: row r goes to y[scatter[r]] (top_k = 1 combine)
+  int T_out;               // rows of y when scattering
+  int accumulate;          // scatter: add into y (fp32 add of the bf16 row, one rounding) or overwrite
 };
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -492,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       const int n_out = p.n_out;
       float xs = 1.0f;
       if (FP8 && row_ok) xs = __ldg(p.x_scale + row);
-      __nv_bfloat16* yrow = p.y + (int64_t)row * n_out;
+      __nv_bfloat16* yrow = p.y + (int64_t)row * n_out;  // (the scatter epilogue redirects it)
       const int col0 = t.n_idx * p.n_tile_cols;
       const float* wsc = FP8 ? p.w_scale + (int64_t)t.expert * p.N : nullptr;
       if (p.epi == MOE_EPILOGUE_SILU_MUL) {
@@ -524,11 +527,23 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
           }
         }
       } else {
+        // The combine fused in (top_k = 1): this row's destination is its token's row.
+        bool dst_ok = row_ok;
+        if (p.scatter && row_ok) {
+          const int tok = __ldg(p.scatter + row);
+          if ((unsigned)tok < (unsigned)p.T_out) {
+            yrow = p.y + (int64_t)tok * n_out;
+          } else {
+            dst_ok = false;
+            flag_error(err, MOE_DEVERR_BAD_INDEX);
+          }
+        }
+        const bool add = p.scatter && p.accumulate;
 #pragma unroll 1
         for (int c = 0; c < kBN; c += 32) {
           float v[32];
           tmem_ld32(tbase + c, v);
-          if (row_ok && col0 + c < n_out) {
+          if (dst_ok && col0 + c < n_out) {
             if (FP8) {
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
@@ -538,8 +553,19 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
             }
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              if (col0 + c + 8 * q < n_out)
-                *reinterpret_cast<uint4*>(yrow + col0 + c + 8 * q) = f32_to_bf16x8(v + 8 * q);
+              if (col0 + c + 8 * q < n_out) {
+                uint4* dst = reinterpret_cast<uint4*>(yrow + col0 + c + 8 * q);
+                uint4 o = f32_to_bf16x8(v + 8 * q);
+                if (add) {  // as moe_scatter_add on the bf16 GEMM output: fp32 add, one rounding
+                  float fo[8], fi[8];
+                  bf16x8_to_f32(*dst, fo);
+                  bf16x8_to_f32(o, fi);
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) fo[i] = __fadd_rn(fo[i], fi[i]);
+                  o = f32_to_bf16x8(fo);
+                }
+                *dst = o;
+              }
           }
         }
       }
@@ -615,6 +641,9 @@ Phase make_phase(int N, int K, int epi, bool fp8, void* y, const float* xs, cons
   p.y = static_cast<__nv_bfloat16*>(y);
   p.x_scale = xs;
   p.w_scale = ws;
+  p.scatter = nullptr;
+  p.T_out = 0;
+  p.accumulate = 0;
   return p;
 }
 
@@ -658,7 +687,10 @@ cudaError_t launch_grouped_gemm(const GemmArgs& g, cudaStream_t s) {
   CUtensorMap ma, mb;
   if (!make_map(&ma, g.x, g.a_max, g.K, g.fp8) || !make_map(&mb, g.w, (int64_t)g.E * g.N, g.K, g.fp8))
     return cudaErrorInvalidValue;
-  const Phase p = make_phase(g.N, g.K, g.epilogue, g.fp8, g.y, g.x_scale, g.w_scale);
+  Phase p = make_phase(g.N, g.K, g.epilogue, g.fp8, g.y, g.x_scale, g.w_scale);
+  p.scatter = g.scatter;
+  p.T_out = g.T_out;
+  p.accumulate = g.accumulate;
   if (g.fp8) return launch_phases<true, 1>(ma, mb, ma, mb, g.counts, p, p, g.E, g.a_max, nullptr, g.err, s);
   return launch_phases<false, 1>(ma, mb, ma, mb, g.counts, p, p, g.E, g.a_max, nullptr, g.err, s);
 }
@@ -672,7 +704,10 @@ cudaError_t launch_expert_mlp(const MlpArgs& g, cudaStream_t s) {
       !make_map(&a1, g.z, g.a_max, g.H, false) || !make_map(&b1, g.w2, (int64_t)g.E * g.D, g.H, false))
     return cudaErrorInvalidValue;
   const Phase p0 = make_phase(2 * g.H, g.D, MOE_EPILOGUE_SILU_MUL, false, g.z, nullptr, nullptr);
-  const Phase p1 = make_phase(g.D, g.H, MOE_EPILOGUE_NONE, false, g.y, nullptr, nullptr);
+  Phase p1 = make_phase(g.D, g.H, MOE_EPILOGUE_NONE, false, g.y, nullptr, nullptr);
+  p1.scatter = g.scatter;
+  p1.T_out = g.T_out;
+  p1.accumulate = g.accumulate;
   int* done = static_cast<int*>(g.ws);
   cudaError_t e = cudaMemsetAsync(done, 0, sizeof(int) * g.E, s);
   if (e != cudaSuccess) return e;

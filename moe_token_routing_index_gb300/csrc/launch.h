@@ -86,6 +86,9 @@ struct GemmArgs {
   void* y;
   int epilogue;
   bool fp8;
+  const int32_t* scatter;  // nullable: combine row r into y[scatter[r]] (top_k = 1)
+  int T_out;               // rows of y when scattering
+  int accumulate;
   unsigned int* err;
 };
 
@@ -99,8 +102,11 @@ struct MlpArgs {
   const int32_t* counts;
   int E, a_max, D, H;
   void* z;              // [a_max, H] bf16
-  void* y;              // [a_max, D] bf16
+  void* y;              // [a_max, D] bf16, or [T_out, D] when scattering
   void* ws;             // expert_mlp_workspace_bytes(E)
+  const int32_t* scatter;
+  int T_out;
+  int accumulate;
   unsigned int* err;
 };
 

@@ -9,6 +9,9 @@ Stage order of mslk/moe/layers.py, MetaShufflingMoE._no_comm_forward
   FP8:   route -> gather*score -> e4m3 rows -> grouped GEMM w13 (FP8 rowwise)
          -> silu_mul_quant -> grouped GEMM w2 (FP8 rowwise) -> scatter-add
 
+With top_k = 1 the scatter-add is fused into the w2 GEMM's epilogue (each
+routed row owns its token), as _routed_expert does with _scatter_add_indices.
+
 Weights stay resident on the device; every buffer of the pipeline is
 allocated once per token-buffer size, so a forward launches kernels only
 (no allocation), and the valid-row count flows on the device from the router
@@ -114,17 +117,20 @@ class MoELayer:
         ti, ei = r["token_indices"], r["expert_indices"]
         inv = r["inv_rows"] if self.top_k > 1 else None
         k = self.top_k
+        fuse_combine = k == 1
+        # the w2 GEMM writes either the routed rows o, or (top_k = 1) the tokens' rows of out
+        w2_out = dict(out=out, scatter_indices=ti, accumulate=accumulate) if fuse_combine else dict(out=b.o)
         st = [("route", lambda: mb.moe_route(scores, k, num_valid_tokens, out=r, workspace=b.ws))]
         if not self.fp8:
             st.append(("gather", lambda: mb.moe_gather_scale(x, ti, ei, scores, valid, out=b.xr)))
             if self.use_fused_mlp(T):
-                st.append(("expert_mlp", lambda: mb.moe_expert_mlp(b.xr, self.w13, self.w2, counts, z=b.z, out=b.o,
-                                                                   workspace=b.mlp_ws)))
+                st.append(("expert_mlp", lambda: mb.moe_expert_mlp(b.xr, self.w13, self.w2, counts, z=b.z,
+                                                                   workspace=b.mlp_ws, **w2_out)))
             else:
                 st += [
                     ("gemm_w13_silu", lambda: mb.moe_grouped_gemm(b.xr, self.w13, counts,
                                                                   epilogue=mb.MOE_EPILOGUE_SILU_MUL, out=b.z)),
-                    ("gemm_w2", lambda: mb.moe_grouped_gemm(b.z, self.w2, counts, out=b.o)),
+                    ("gemm_w2", lambda: mb.moe_grouped_gemm(b.z, self.w2, counts, **w2_out)),
                 ]
         else:
             st += [
@@ -135,9 +141,10 @@ class MoELayer:
                 ("silu_quant", lambda: mb.moe_silu_mul_quant(b.y, self.H, self.scale_ub, valid, out=b.z,
                                                              out_scale=b.zs)),
                 ("gemm_w2", lambda: mb.moe_grouped_gemm_fp8_rowwise(b.z, self.w2, counts, b.zs, self.w2_scale,
-                                                                    out=b.o)),
+                                                                    **w2_out)),
             ]
-        st.append(("scatter", lambda: mb.moe_scatter_add(out, b.o, ti, inv, k, valid, accumulate=accumulate)))
+        if not fuse_combine:
+            st.append(("scatter", lambda: mb.moe_scatter_add(out, b.o, ti, inv, k, valid, accumulate=accumulate)))
         return st
 
     def __call__(self, x: torch.Tensor, scores: torch.Tensor, num_valid_tokens: torch.Tensor | None = None,
@@ -163,6 +170,7 @@ class MoELayer:
         gather, the GEMMs (1 fused, or 2), silu_mul_quant (FP8), scatter."""
         T = self._bufs.T if T is None and self._bufs is not None else (T or 0)
         route = 1 if (T <= 1024 and T * self.E <= 16384 and T * self.top_k <= 8192 and self.E <= 256) else 3
+        scatter = 0 if self.top_k == 1 else 1
         if self.fp8:
-            return route + 5
-        return route + 1 + (1 if self.use_fused_mlp(T) else 2) + 1
+            return route + 4 + scatter
+        return route + 1 + (1 if self.use_fused_mlp(T) else 2) + scatter

@@ -64,8 +64,15 @@ def test_host_side_validation_without_gpu(lib):
     # silu: misaligned row stride
     assert L.moe_silu_mul(fake, fake, 36, 4, 32, None, fake, None) == lib.MOE_ERR_UNSUPPORTED
     # grouped GEMM: N not a multiple of 16, unknown epilogue, too many experts
-    assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 24, 64, fake, 0, None) == lib.MOE_ERR_UNSUPPORTED
-    assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 32, 64, fake, 9, None) == lib.MOE_ERR_INVALID
-    assert L.moe_grouped_gemm(fake, fake, fake, 2048, 64, 32, 64, fake, 0, None) == lib.MOE_ERR_UNSUPPORTED
-    assert L.moe_grouped_gemm_fp8_rowwise(fake, fake, fake, None, fake, 4, 64, 32, 64, fake, 0, None) \
+    assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 24, 64, fake, 0, None, 0, 0, None) == lib.MOE_ERR_UNSUPPORTED
+    assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 32, 64, fake, 9, None, 0, 0, None) == lib.MOE_ERR_INVALID
+    assert L.moe_grouped_gemm(fake, fake, fake, 2048, 64, 32, 64, fake, 0, None, 0, 0, None) \
+        == lib.MOE_ERR_UNSUPPORTED
+    assert L.moe_grouped_gemm_fp8_rowwise(fake, fake, fake, None, fake, 4, 64, 32, 64, fake, 0, None, 0, 0, None) \
         == lib.MOE_ERR_INVALID
+    # the fused combine only goes with the plain epilogue
+    assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 32, 64, fake, 1, fake, 8, 1, None) == lib.MOE_ERR_INVALID
+    n = ctypes.c_size_t(0)
+    assert L.moe_expert_mlp_workspace_size(0, ctypes.byref(n)) == lib.MOE_ERR_INVALID
+    assert L.moe_expert_mlp(fake, fake, fake, fake, 4, 64, 32, 32, fake, fake, None, 0, 0, fake, 0, None) \
+        == lib.MOE_ERR_WORKSPACE

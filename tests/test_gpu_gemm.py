@@ -213,3 +213,47 @@ def test_expert_mlp_workloads_equal_two_launches(name):
     y = mb.moe_expert_mlp(x, w13, w2, cnt)
     assert mb.device_error() == 0
     assert torch.equal(y, y_ref)
+
+
+@pytest.mark.parametrize("accumulate", [True, False])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_fused_combine_equals_gemm_then_scatter(accumulate, fp8):
+    """top_k = 1: the w2 GEMM writing out[token] directly equals GEMM + moe_scatter_add bit for bit."""
+    mb = _mb()
+    E, counts, N, K, T = 5, [70, 0, 33, 129, 1], 272, 192, 300
+    x, w, cnt, a = _problem(E, counts, N, K, None, seed=77)
+    perm = torch.randperm(T, generator=torch.Generator().manual_seed(1))[:a].to(torch.int32).cuda()  # token of each row
+    cd = torch.from_numpy(cnt).cuda()
+    init = torch.randn(T, N, generator=torch.Generator().manual_seed(2)).to(torch.bfloat16).cuda()
+    if fp8:
+        xq, xs = mb.moe_quantize_rows(x.float().cuda())
+        wq, ws = mb.moe_quantize_rows(w.float().cuda())
+        gemm = lambda **kw: mb.moe_grouped_gemm_fp8_rowwise(xq, wq, cd, xs, ws, **kw)
+    else:
+        gemm = lambda **kw: mb.moe_grouped_gemm(x.cuda(), w.cuda(), cd, **kw)
+    o = gemm()
+    ref = init.clone()
+    mb.moe_scatter_add(ref, o, perm, None, 1, accumulate=accumulate)
+    got = init.clone()
+    gemm(out=got, scatter_indices=perm, accumulate=accumulate)
+    assert mb.device_error() == 0
+    assert torch.equal(got, ref)
+
+
+def test_expert_mlp_fused_combine_equals_unfused():
+    mb = _mb()
+    E, counts, D, H, T = 4, [40, 0, 90, 17], 256, 384, 200
+    g = torch.Generator().manual_seed(9)
+    a = sum(counts)
+    x = torch.randn(a, D, generator=g).to(torch.bfloat16).cuda()
+    w13 = (torch.randn(E, 2 * H, D, generator=g) * 0.1).to(torch.bfloat16).cuda()
+    w2 = (torch.randn(E, D, H, generator=g) * 0.1).to(torch.bfloat16).cuda()
+    cd = torch.tensor(counts, dtype=torch.int32, device="cuda")
+    perm = torch.randperm(T, generator=g)[:a].to(torch.int32).cuda()
+    o = mb.moe_expert_mlp(x, w13, w2, cd)
+    ref = sentinel_like((T, D), torch.bfloat16)
+    mb.moe_scatter_add(ref, o, perm, None, 1, accumulate=False)
+    got = sentinel_like((T, D), torch.bfloat16)
+    mb.moe_expert_mlp(x, w13, w2, cd, out=got, scatter_indices=perm, accumulate=False)
+    assert mb.device_error() == 0
+    assert torch.equal(got, ref)
