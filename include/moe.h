@@ -166,11 +166,15 @@ int moe_route_no_alloc(const void* scores, int scores_dtype, int64_t stride_t, i
  * moe_route (E experts); valid_token_count: device int32 count of ROUTED ROWS
  * (NULL: a), e.g. &counts[E] from moe_route.  Rows i >= valid are not written.
  * out [a, D] bf16.  a == 0 or D == 0 is a no-op.
+ * inv_rows (nullable) and top_k: moe_route's inverse permutation.  With it
+ * (and top_k > 1) the rows are produced token by token, each x row read from
+ * HBM once for its top_k routed rows; valid_token_count must then be
+ * Tv * top_k.  The output is the same either way.
  */
 int moe_gather_scale(const void* x, int T, int D, const int32_t* token_indices,
                      const int32_t* expert_indices, int a, const void* scores, int scores_dtype,
                      int64_t stride_t, int64_t stride_e, int E, const int32_t* valid_token_count,
-                     void* out, cudaStream_t stream);
+                     const int32_t* inv_rows, int top_k, void* out, cudaStream_t stream);
 
 /*
  * gather_scale_quant_dense_tokens (mslk/moe/gather_scatter.py,
@@ -182,12 +186,13 @@ int moe_gather_scale(const void* x, int T, int D, const int32_t* token_indices,
  *   out[i, j] = e4m3( clamp(v_j * s, -448, 448) ), round to nearest even.
  * All arithmetic is IEEE fp32 (correctly rounded division and reciprocal).
  * out [a, D] e4m3, out_scale [a] fp32.  Rows i >= valid are not written.
+ * inv_rows, top_k: as in moe_gather_scale.
  */
 int moe_gather_scale_quant(const void* x, int T, int D, const int32_t* token_indices,
                            const int32_t* expert_indices, int a, const void* scores,
                            int scores_dtype, int64_t stride_t, int64_t stride_e, int E,
-                           const int32_t* valid_token_count, const float* scale_ub, void* out,
-                           float* out_scale, cudaStream_t stream);
+                           const int32_t* valid_token_count, const int32_t* inv_rows, int top_k,
+                           const float* scale_ub, void* out, float* out_scale, cudaStream_t stream);
 
 /*
  * Per-row FP8 quantisation of an fp32 matrix w [rows, cols] with the rule of

@@ -47,8 +47,8 @@ def _load() -> ctypes.CDLL:
         "moe_route_workspace_size": ([I, I, I, ctypes.POINTER(S)], I),
         "moe_route": ([P, I, L, L, I, I, I, P, P, P, P, P, P, P, S, P], I),
         "moe_route_no_alloc": ([P, I, L, L, I, I, I, P, P, P, P, P, P, P], I),
-        "moe_gather_scale": ([P, I, I, P, P, I, P, I, L, L, I, P, P, P], I),
-        "moe_gather_scale_quant": ([P, I, I, P, P, I, P, I, L, L, I, P, P, P, P, P], I),
+        "moe_gather_scale": ([P, I, I, P, P, I, P, I, L, L, I, P, P, I, P, P], I),
+        "moe_gather_scale_quant": ([P, I, I, P, P, I, P, I, L, L, I, P, P, I, P, P, P, P], I),
         "moe_quantize_rows": ([P, L, I, P, P, P, P], I),
         "moe_grouped_gemm": ([P, P, P, I, I, I, I, P, I, P, I, I, P], I),
         "moe_expert_mlp_workspace_size": ([I, ctypes.POINTER(S)], I),
@@ -152,7 +152,8 @@ def moe_route(scores: torch.Tensor, top_k: int, num_valid_tokens: torch.Tensor |
 
 # ------------------------------------------------------------------- gather
 
-def moe_gather_scale(x, token_indices, expert_indices, scores, valid_token_count=None, *, out=None, stream=None):
+def moe_gather_scale(x, token_indices, expert_indices, scores, valid_token_count=None, *, inv_rows=None,
+                     top_k: int = 1, out=None, stream=None):
     T, D = x.shape
     a = token_indices.shape[0]
     _need(x, torch.bfloat16, "x")
@@ -160,13 +161,13 @@ def moe_gather_scale(x, token_indices, expert_indices, scores, valid_token_count
         out = torch.empty(a, D, dtype=x.dtype, device=x.device)
     st = _lib.moe_gather_scale(_ptr(x), T, D, _ptr(token_indices), _ptr(expert_indices), a, _ptr(scores),
                                _dtype_code(scores), scores.stride(0), scores.stride(1), scores.shape[1],
-                               _ptr(valid_token_count), _ptr(out), _stream(stream))
+                               _ptr(valid_token_count), _ptr(inv_rows), top_k, _ptr(out), _stream(stream))
     _check("moe_gather_scale", st)
     return out
 
 
 def moe_gather_scale_quant(x, token_indices, expert_indices, scores, scale_ub=None, valid_token_count=None, *,
-                           out=None, out_scale=None, stream=None):
+                           inv_rows=None, top_k: int = 1, out=None, out_scale=None, stream=None):
     T, D = x.shape
     a = token_indices.shape[0]
     _need(x, torch.bfloat16, "x")
@@ -176,8 +177,8 @@ def moe_gather_scale_quant(x, token_indices, expert_indices, scores, scale_ub=No
         out_scale = torch.empty(a, dtype=torch.float32, device=x.device)
     st = _lib.moe_gather_scale_quant(_ptr(x), T, D, _ptr(token_indices), _ptr(expert_indices), a, _ptr(scores),
                                      _dtype_code(scores), scores.stride(0), scores.stride(1), scores.shape[1],
-                                     _ptr(valid_token_count), _ptr(scale_ub), _ptr(out), _ptr(out_scale),
-                                     _stream(stream))
+                                     _ptr(valid_token_count), _ptr(inv_rows), top_k, _ptr(scale_ub), _ptr(out),
+                                     _ptr(out_scale), _stream(stream))
     _check("moe_gather_scale_quant", st)
     return out, out_scale
 

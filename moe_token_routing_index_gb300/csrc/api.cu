@@ -159,11 +159,13 @@ static int check_gather(const void* x, int T, int D, const int32_t* ti, const in
 
 int moe_gather_scale(const void* x, int T, int D, const int32_t* token_indices, const int32_t* expert_indices, int a,
                      const void* scores, int scores_dtype, int64_t stride_t, int64_t stride_e, int E,
-                     const int32_t* valid_token_count, void* out, cudaStream_t stream) {
+                     const int32_t* valid_token_count, const int32_t* inv_rows, int top_k, void* out,
+                     cudaStream_t stream) {
   int rc = check_gather(x, T, D, token_indices, expert_indices, a, scores, scores_dtype, E, out);
   if (rc != MOE_OK || a == 0 || D == 0) return rc;
+  if (inv_rows && top_k < 1) return MOE_ERR_INVALID;
   moe::GatherArgs g{x, T, D, token_indices, expert_indices, a, scores, scores_dtype, stride_t, stride_e, E,
-                    valid_token_count, nullptr, out, nullptr, nullptr};
+                    valid_token_count, nullptr, out, nullptr, inv_rows, inv_rows ? top_k : 1, nullptr};
   rc = device_error_word(&g.err);
   if (rc != MOE_OK) return rc;
   return finish(moe::launch_gather_scale(g, stream));
@@ -171,14 +173,15 @@ int moe_gather_scale(const void* x, int T, int D, const int32_t* token_indices, 
 
 int moe_gather_scale_quant(const void* x, int T, int D, const int32_t* token_indices, const int32_t* expert_indices,
                            int a, const void* scores, int scores_dtype, int64_t stride_t, int64_t stride_e, int E,
-                           const int32_t* valid_token_count, const float* scale_ub, void* out, float* out_scale,
-                           cudaStream_t stream) {
+                           const int32_t* valid_token_count, const int32_t* inv_rows, int top_k,
+                           const float* scale_ub, void* out, float* out_scale, cudaStream_t stream) {
   int rc = check_gather(x, T, D, token_indices, expert_indices, a, scores, scores_dtype, E, out);
   if (rc != MOE_OK || a == 0 || D == 0) return rc;
   if (!out_scale) return MOE_ERR_INVALID;
+  if (inv_rows && top_k < 1) return MOE_ERR_INVALID;
   if (D > 16384) return MOE_ERR_UNSUPPORTED;
   moe::GatherArgs g{x, T, D, token_indices, expert_indices, a, scores, scores_dtype, stride_t, stride_e, E,
-                    valid_token_count, scale_ub, out, out_scale, nullptr};
+                    valid_token_count, scale_ub, out, out_scale, inv_rows, inv_rows ? top_k : 1, nullptr};
   rc = device_error_word(&g.err);
   if (rc != MOE_OK) return rc;
   return finish(moe::launch_gather_scale_quant(g, stream));

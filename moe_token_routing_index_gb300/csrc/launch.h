@@ -40,6 +40,8 @@ struct GatherArgs {
   const float* scale_ub;  // quantising variant only
   void* out;
   float* out_scale;       // quantising variant only
+  const int32_t* inv;     // nullable: rows of each token (token-major gather)
+  int top_k;
   unsigned int* err;
 };
 

@@ -276,18 +276,45 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 
 constexpr int kStagedWarps = 8;
 
-__global__ void __launch_bounds__(kStagedWarps * 32, 1) gather_scale_quant_staged_kernel(
+// Largest |bf16| of 8 packed values, as bf16 magnitude bits (the magnitude
+// bits of a bf16 order like its absolute value), folded into `m`.
+__device__ __forceinline__ uint32_t absmax_bits8(const uint4& v, uint32_t m) {
+  uint32_t a = __vmaxu2(v.x & 0x7fff7fffu, v.y & 0x7fff7fffu);
+  uint32_t b = __vmaxu2(v.z & 0x7fff7fffu, v.w & 0x7fff7fffu);
+  a = __vmaxu2(a, b);
+  return max(m, max(a & 0xffffu, a >> 16));
+}
+
+// Items of the staged gather: row-major (item = routed row r, its token
+// ti[r], one output row) or token-major (item = valid token t, its top_k
+// routed rows inv[t*k .. t*k+k), so the staged x row serves all of them).
+//
+// Per warp: a ring of NB slots, each holding one staged x row (one bulk copy,
+// completion on the slot's mbarrier).  The routed rows' metadata (row index
+// and score) is loaded for 32 rows at a time, one row per lane, so the
+// dependent index loads cost one round trip per 32 rows.  For the FP8 output
+// the row max uses max |RN(x * s)| = RN(max |x| * |s|) (rounding is
+// monotone), taken as an integer max over the packed bf16 magnitudes; the
+// clamp to +-448 is the saturation of the e4m3 conversion itself.
+template <bool QUANT>
+__global__ void __launch_bounds__(kStagedWarps * 32, 1) gather_staged_kernel(
     const uint4* __restrict__ x, int T, int D8, const int32_t* __restrict__ ti, const int32_t* __restrict__ ei,
-    int a, const void* __restrict__ scores, int dtype, int64_t st, int64_t se, int E,
-    const int32_t* __restrict__ valid_p, const float* __restrict__ ub, uint2* __restrict__ out,
+    const int32_t* __restrict__ inv, int k, int a, const void* __restrict__ scores, int dtype, int64_t st,
+    int64_t se, int E, const int32_t* __restrict__ valid_p, const float* __restrict__ ub, void* __restrict__ out,
     float* __restrict__ out_scale, int NB, unsigned int* err) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t row_bytes = (uint32_t)D8 * 16u;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);                      // [warps][NB]
-  int2* s_idx = reinterpret_cast<int2*>(smem + kStagedWarps * NB * 8);     // [warps][NB]: token, expert
+  int* s_tok = reinterpret_cast<int*>(smem + kStagedWarps * NB * 8);       // [warps][NB]: staged token or -1
   uint8_t* slots = smem + ((kStagedWarps * NB * 16 + 127) / 128) * 128;    // [warps][NB][row_bytes]
   const int valid = read_count(valid_p, a, err);
+  const int nrows = inv ? k : 1;  // routed rows per item
+  int items = valid;
+  if (inv) {
+    if (valid % k != 0 && blockIdx.x == 0 && threadIdx.x == 0) flag_error(err, MOE_DEVERR_BAD_COUNT);
+    items = min(valid / k, T);
+  }
   const int gw = blockIdx.x * kStagedWarps + warp, nw = gridDim.x * kStagedWarps;
   auto bar_addr = [&](int b) { return (uint32_t)__cvta_generic_to_shared(&bars[warp * NB + b]); };
   auto slot = [&](int b) { return slots + (size_t)(warp * NB + b) * row_bytes; };
@@ -295,76 +322,141 @@ __global__ void __launch_bounds__(kStagedWarps * 32, 1) gather_scale_quant_stage
     for (int b = 0; b < NB; ++b) bar_init(bar_addr(b), 1);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncwarp();
-  // lane 0: read the indices of routed row r and start its copy into slot b
-  auto issue = [&](int r, int b) {
-    const int t = __ldg(ti + r), e = __ldg(ei + r);
-    const bool ok = (unsigned)t < (unsigned)T && (unsigned)e < (unsigned)E;
-    s_idx[warp * NB + b] = make_int2(ok ? t : -1, e);
+  // lane 0: the token of `item`, and one bulk copy of its x row into slot b
+  auto issue = [&](int item, int b) {
+    const int t = inv ? item : __ldg(ti + item);
+    const bool ok = (unsigned)t < (unsigned)T;
+    s_tok[warp * NB + b] = ok ? t : -1;
     if (ok) bulk_load((uint32_t)__cvta_generic_to_shared(slot(b)), x + (int64_t)t * D8, row_bytes, bar_addr(b));
   };
   if (lane == 0)
     for (int b = 0; b < NB; ++b)
-      if (gw + b * nw < valid) issue(gw + b * nw, b);
+      if (gw + b * nw < items) issue(gw + b * nw, b);
   __syncwarp();
+  // metadata of routed-row number q of this warp (item q / nrows, its row q % nrows): lane L holds q = base + L
+  int meta_base = -32;
+  int m_row = -1;
+  float m_s = 0.0f;
+  auto load_meta = [&](int base) {
+    meta_base = base;
+    const int q = base + lane;
+    const int i = q / nrows, j = q - (q / nrows) * nrows;
+    const int item = gw + i * nw;
+    m_row = -1;
+    if (item < items) {
+      const int r = inv ? __ldg(inv + (int64_t)item * k + j) : item;
+      const int t = inv ? item : __ldg(ti + item);
+      const int e = (unsigned)r < (unsigned)a ? __ldg(ei + r) : -1;
+      if ((unsigned)r < (unsigned)a && (unsigned)e < (unsigned)E && (unsigned)t < (unsigned)T) {
+        m_row = r;
+        m_s = load_score(scores, dtype, (int64_t)t * st + (int64_t)e * se);
+      }
+    }
+  };
   uint32_t phase = 0;  // bit b: parity of the next completion of slot b
   int i = 0;
   bool timed_out = false;
   for (;; ++i) {
-    const int r = gw + i * nw;
-    if (r >= valid) break;
+    const int item = gw + i * nw;
+    if (item >= items) break;
     const int b = i % NB;
-    const int2 te = s_idx[warp * NB + b];
-    if (te.x >= 0) {
+    const int t = s_tok[warp * NB + b];
+    if (t >= 0) {
       if (!bar_wait(bar_addr(b), (phase >> b) & 1u)) {
         timed_out = true;
         break;
       }
       phase ^= 1u << b;
-      const float s = load_score(scores, dtype, (int64_t)te.x * st + (int64_t)te.y * se);
       const uint4* row = reinterpret_cast<const uint4*>(slot(b));
-      float m = 0.0f;
-      for (int c = lane; c < D8; c += 32) {
-        float f[8];
-        bf16x8_to_f32(row[c], f);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) m = fmaxf(m, fabsf(__fmul_rn(f[q], s)));
+      uint32_t mx = 0;
+      if (QUANT) {  // the row's largest |x|, shared by all of its routed rows
+        for (int c = lane; c < D8; c += 32) mx = absmax_bits8(row[c], mx);
+        mx = __reduce_max_sync(0xffffffffu, mx);
       }
-      m = warp_max_nonneg(m);
-      float inv;
-      const float sc = fp8_row_scale(m, ub, &inv);
-      if (lane == 0) out_scale[r] = inv;
-      uint2* dst = out + (int64_t)r * D8;
-      for (int c = lane; c < D8; c += 32) {
-        float f[8];
-        bf16x8_to_f32(row[c], f);
+      for (int j = 0; j < nrows; ++j) {
+        const int q = i * nrows + j;
+        if (q >= meta_base + 32) load_meta(q);
+        const int r = __shfl_sync(0xffffffffu, m_row, q - meta_base);
+        const float s = __shfl_sync(0xffffffffu, m_s, q - meta_base);
+        if (r < 0) {
+          if (lane == 0) flag_error(err, MOE_DEVERR_BAD_INDEX);
+          continue;
+        }
+        if constexpr (QUANT) {
+          const float m = __fmul_rn(__uint_as_float(mx << 16), fabsf(s));  // = max_j |x_j * s|
+          float inv_s;
+          const float sc = fp8_row_scale(m, ub, &inv_s);
+          if (lane == 0) out_scale[r] = inv_s;
+          uint2* dst = static_cast<uint2*>(out) + (int64_t)r * D8;
+#pragma unroll 2
+          for (int c = lane; c < D8; c += 32) {
+            float f[8];
+            bf16x8_to_f32(row[c], f);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) f[q] = fp8_scaled_clamped(__fmul_rn(f[q], s), sc);
-        dst[c] = e4m3x8(f);
+            for (int q8 = 0; q8 < 8; ++q8) f[q8] = __fmul_rn(__fmul_rn(f[q8], s), sc);
+            dst[c] = e4m3x8(f);  // saturating conversion = the clamp to +-448
+          }
+        } else {
+          uint4* dst = static_cast<uint4*>(out) + (int64_t)r * D8;
+#pragma unroll 2
+          for (int c = lane; c < D8; c += 32) {
+            float f[8];
+            bf16x8_to_f32(row[c], f);
+#pragma unroll
+            for (int q8 = 0; q8 < 8; ++q8) f[q8] = __fmul_rn(f[q8], s);
+            dst[c] = f32_to_bf16x8(f);
+          }
+        }
       }
-    } else if (lane == 0) {
-      flag_error(err, MOE_DEVERR_BAD_INDEX);
+    } else {
+      if (lane == 0) flag_error(err, MOE_DEVERR_BAD_INDEX);
+      for (int j = 0; j < nrows; ++j)  // keep the metadata window in step
+        if (i * nrows + j >= meta_base + 32) load_meta(i * nrows + j);
     }
     // the slot's reads (generic proxy) finish before the next bulk copy (async proxy) writes it
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
-    if (lane == 0 && r + NB * nw < valid) issue(r + NB * nw, b);
+    if (lane == 0 && item + NB * nw < items) issue(item + NB * nw, b);
     __syncwarp();
   }
   // On a normal exit every issued copy has been consumed (a copy is issued only
-  // for a row below `valid`, and the loop waits on every such row).  After a
+  // for an item below `items`, and the loop waits on every such item).  After a
   // timeout, the copies of iterations i .. i+NB-1 may still be in flight: wait
   // for them (bounded) so none lands after the block has exited.
   if (timed_out && lane == 0) {
     flag_error(err, MOE_DEVERR_TIMEOUT);
     for (int j = i; j < i + NB; ++j) {
       const int b = j % NB;
-      if (gw + j * nw < valid && s_idx[warp * NB + b].x >= 0) {
+      if (gw + j * nw < items && s_tok[warp * NB + b] >= 0) {
         const uint64_t t0 = global_timer_ns_rw();
         while (!bar_try_wait(bar_addr(b), (phase >> b) & 1u) && global_timer_ns_rw() - t0 < 100000000ull) {
         }
       }
     }
   }
+}
+
+// Slots per warp of the staged gather (0: the row does not fit twice in 200 KB).
+inline int staged_slots(int D8) {
+  const size_t row_bytes = (size_t)D8 * 16;
+  return (int)std::min<size_t>(4, (200u * 1024u) / (kStagedWarps * row_bytes));
+}
+
+template <bool QUANT>
+cudaError_t launch_staged(const GatherArgs& g, int nb, cudaStream_t s) {
+  const int D8 = g.D / 8;
+  const size_t row_bytes = (size_t)D8 * 16;
+  const size_t smem = (size_t)((kStagedWarps * nb * 16 + 127) / 128) * 128 + (size_t)kStagedWarps * nb * row_bytes;
+  auto kern = gather_staged_kernel<QUANT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int64_t items = g.inv ? std::min<int64_t>(g.a / g.top_k, g.T) : g.a;
+  const int64_t need = (items + kStagedWarps - 1) / kStagedWarps;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(need, device_sm_count()));
+  kern<<<grid, kStagedWarps * 32, smem, s>>>(static_cast<const uint4*>(g.x), g.T, D8, g.token_indices,
+                                             g.expert_indices, g.inv, g.top_k, g.a, g.scores, g.dtype, g.stride_t,
+                                             g.stride_e, g.E, g.valid, g.scale_ub, g.out, g.out_scale, nb, g.err);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------- weight rows -> FP8 (2 pass)
@@ -611,6 +703,10 @@ __global__ void __launch_bounds__(kThreads) scatter_add_tokens_kernel(uint4* __r
 }  // namespace
 
 cudaError_t launch_gather_scale(const GatherArgs& g, cudaStream_t s) {
+  if (g.inv && g.top_k > 1) {  // token-major: each x row is read once for its top_k rows
+    const int nb = staged_slots(g.D / 8);
+    if (nb >= 2) return launch_staged<false>(g, nb, s);
+  }
   const int grid =
       persistent_grid(gather_scale_kernel, (int64_t)g.a * ((g.D / 8 + kGatherChunk - 1) / kGatherChunk), kWarps);
   gather_scale_kernel<<<grid, kThreads, 0, s>>>(static_cast<const uint4*>(g.x), g.T, g.D / 8, g.token_indices,
@@ -635,23 +731,10 @@ inline int pick_group(int nvec) {
 
 cudaError_t launch_gather_scale_quant(const GatherArgs& g, cudaStream_t s) {
   const int D8 = g.D / 8;
-  {
-    // TMA-staged kernel: as many row slots per warp (2..4) as fit in 200 KB of shared memory.
-    const size_t row_bytes = (size_t)D8 * 16;
-    const int nb = (int)std::min<size_t>(4, (200u * 1024u) / (kStagedWarps * row_bytes));
-    if (nb >= 2) {
-      const size_t smem = (size_t)((kStagedWarps * nb * 16 + 127) / 128) * 128 + (size_t)kStagedWarps * nb * row_bytes;
-      cudaError_t e = cudaFuncSetAttribute(gather_scale_quant_staged_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      const int64_t need = (g.a + kStagedWarps - 1) / kStagedWarps;
-      const int grid = (int)std::min<int64_t>(need, device_sm_count());
-      gather_scale_quant_staged_kernel<<<grid, kStagedWarps * 32, smem, s>>>(
-          static_cast<const uint4*>(g.x), g.T, D8, g.token_indices, g.expert_indices, g.a, g.scores, g.dtype,
-          g.stride_t, g.stride_e, g.E, g.valid, g.scale_ub, static_cast<uint2*>(g.out), g.out_scale, nb, g.err);
-      return cudaGetLastError();
-    }
-  }
+  // TMA-staged rows (token-major with the inverse permutation) when two row
+  // slots per warp fit in shared memory, else rows held in registers.
+  const int nb = staged_slots(D8);
+  if (nb >= 2) return launch_staged<true>(g, nb, s);
   const int G = pick_group(D8);
   const bool full = D8 > 32 * G * 4;  // 8 vectors per thread, else 4
   switch (G * 2 + (full ? 1 : 0)) {

@@ -122,7 +122,8 @@ class MoELayer:
         w2_out = dict(out=out, scatter_indices=ti, accumulate=accumulate) if fuse_combine else dict(out=b.o)
         st = [("route", lambda: mb.moe_route(scores, k, num_valid_tokens, out=r, workspace=b.ws))]
         if not self.fp8:
-            st.append(("gather", lambda: mb.moe_gather_scale(x, ti, ei, scores, valid, out=b.xr)))
+            st.append(("gather", lambda: mb.moe_gather_scale(x, ti, ei, scores, valid, inv_rows=inv, top_k=k,
+                                                             out=b.xr)))
             if self.use_fused_mlp(T):
                 st.append(("expert_mlp", lambda: mb.moe_expert_mlp(b.xr, self.w13, self.w2, counts, z=b.z,
                                                                    workspace=b.mlp_ws, **w2_out)))
@@ -135,7 +136,8 @@ class MoELayer:
         else:
             st += [
                 ("gather_quant", lambda: mb.moe_gather_scale_quant(x, ti, ei, scores, self.scale_ub, valid,
-                                                                   out=b.xr, out_scale=b.xs)),
+                                                                   inv_rows=inv, top_k=k, out=b.xr,
+                                                                   out_scale=b.xs)),
                 ("gemm_w13", lambda: mb.moe_grouped_gemm_fp8_rowwise(b.xr, self.w13, counts, b.xs, self.w13_scale,
                                                                      out=b.y)),
                 ("silu_quant", lambda: mb.moe_silu_mul_quant(b.y, self.H, self.scale_ub, valid, out=b.z,

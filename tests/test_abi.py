@@ -51,14 +51,17 @@ def test_host_side_validation_without_gpu(lib):
     assert L.moe_route(fake, 0, 8, 1, 64, 8, 2, None, None, fake, fake, fake, None, fake, 1 << 20, None) \
         == lib.MOE_ERR_INVALID
     # gather: D not a multiple of 16; empty is a no-op
-    assert L.moe_gather_scale(fake, 4, 24, fake, fake, 4, fake, 0, 8, 1, 8, None, fake, None) \
+    assert L.moe_gather_scale(fake, 4, 24, fake, fake, 4, fake, 0, 8, 1, 8, None, None, 1, fake, None) \
         == lib.MOE_ERR_UNSUPPORTED
-    assert L.moe_gather_scale(None, 4, 32, None, None, 0, None, 0, 8, 1, 8, None, None, None) == lib.MOE_OK
-    # gather: bad score dtype
-    assert L.moe_gather_scale(fake, 4, 32, fake, fake, 4, fake, 7, 8, 1, 8, None, fake, None) == lib.MOE_ERR_INVALID
-    # quantising gather needs out_scale
-    assert L.moe_gather_scale_quant(fake, 4, 32, fake, fake, 4, fake, 0, 8, 1, 8, None, None, fake, None, None) \
+    assert L.moe_gather_scale(None, 4, 32, None, None, 0, None, 0, 8, 1, 8, None, None, 1, None, None) == lib.MOE_OK
+    # gather: bad score dtype; inverse permutation without a valid top_k
+    assert L.moe_gather_scale(fake, 4, 32, fake, fake, 4, fake, 7, 8, 1, 8, None, None, 1, fake, None) \
         == lib.MOE_ERR_INVALID
+    assert L.moe_gather_scale(fake, 4, 32, fake, fake, 4, fake, 0, 8, 1, 8, None, fake, 0, fake, None) \
+        == lib.MOE_ERR_INVALID
+    # quantising gather needs out_scale
+    assert L.moe_gather_scale_quant(fake, 4, 32, fake, fake, 4, fake, 0, 8, 1, 8, None, None, 1, None, fake, None,
+                                    None) == lib.MOE_ERR_INVALID
     # scatter: top_k > 1 needs the inverse permutation
     assert L.moe_scatter_add(fake, fake, fake, None, 2, 8, 4, 32, None, 1, None) == lib.MOE_ERR_INVALID
     # silu: misaligned row stride
