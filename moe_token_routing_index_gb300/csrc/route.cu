@@ -2,18 +2,21 @@
 // mslk/moe/layers.py, MetaShufflingMoE._route; selection as torch.topk in
 // BaselineMoE._forward, ties to the lower expert index).
 //
-// Small problems (the decode batch) run in one block, all in shared memory;
-// larger ones take three launches over blocks of 32 tokens:
+// Small problems (the decode batch) run in one block, all in shared memory.
+// Larger ones run as one cooperative launch in three phases over 32-token
+// chunks, separated by grid-wide barriers:
 //   select : one warp per token; each lane holds the order keys of experts
 //            lane, lane+32, ...; top_k rounds of a warp arg-max (redux.sync max
 //            on the key, then min on the expert index among the winners).
-//            Writes the chosen experts and a per-block expert histogram.
+//            Writes the chosen experts and a per-chunk expert histogram.
 //   scan   : one block per expert; exclusive scan of that expert's histogram
-//            over the token blocks (the block's base row within the expert)
-//            and the expert's count.
-//   emit   : per token block, a 32-bit bitmap per expert marks which of the
-//            block's tokens chose it, so a token's rank within the expert is a
-//            popcount; row = expert offset + block base + rank.
+//            over the chunks (the chunk's base row within the expert) and the
+//            expert's count.
+//   emit   : per chunk, a 32-bit bitmap per expert marks which of the chunk's
+//            tokens chose it, so a token's rank within the expert is a
+//            popcount; row = expert offset + chunk base + rank.
+// The barrier is an arrival counter in the workspace (zeroed before the
+// launch) with a bounded wait; the cooperative launch keeps every block resident.
 #include "common.cuh"
 #include "launch.h"
 
@@ -21,7 +24,7 @@ namespace moe {
 namespace {
 
 constexpr int kTokBlock = 32;     // tokens per block (one bitmap word per expert)
-constexpr int kRouteThreads = 256;
+constexpr int kRouteThreads = 1024;  // 32 warps: one token of a 32-token chunk per warp
 constexpr int kWarps = kRouteThreads / 32;
 
 // Monotone map of a float to uint32 (larger float -> larger key), -0 folded onto +0.
@@ -31,18 +34,15 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-template <int EPL>  // experts per lane: ceil(E / 32) rounded up to the instantiated size
-__global__ void __launch_bounds__(kRouteThreads) route_select_kernel(
-    const void* __restrict__ scores, int dtype, int64_t st, int64_t se, int T, int E, int k,
-    const int32_t* __restrict__ num_valid, int32_t* __restrict__ chosen, int32_t* __restrict__ hist_t,
-    int nblk, unsigned int* err) {
-  __shared__ int s_hist[1024];
-  const int Tv = read_count(num_valid, T, err);
+// Phase 1 for chunk c: select the top_k experts of its valid tokens.
+template <int EPL>
+__device__ void route_select_chunk(int c, const void* __restrict__ scores, int dtype, int64_t st, int64_t se, int E,
+                                   int k, int Tv, int32_t* __restrict__ chosen, int32_t* __restrict__ hist_t, int nblk,
+                                   int* s_hist) {
   for (int e = threadIdx.x; e < E; e += kRouteThreads) s_hist[e] = 0;
   __syncthreads();
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t0 = blockIdx.x * kTokBlock;
+  const int t0 = c * kTokBlock;
   for (int t = t0 + warp; t < t0 + kTokBlock && t < Tv; t += kWarps) {
     uint32_t key[EPL];
     uint32_t live = 0;  // bit i: expert lane + 32 i exists and is not yet chosen
@@ -75,100 +75,161 @@ __global__ void __launch_bounds__(kRouteThreads) route_select_kernel(
     }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += kRouteThreads) hist_t[(int64_t)e * nblk + blockIdx.x] = s_hist[e];
+  for (int e = threadIdx.x; e < E; e += kRouteThreads) hist_t[(int64_t)e * nblk + c] = s_hist[e];
+  __syncthreads();
 }
 
-// Block e: exclusive scan of hist_t[e, 0..nblk) in place; counts[e] = total.
-__global__ void __launch_bounds__(kRouteThreads) route_scan_kernel(int32_t* __restrict__ hist_t, int nblk,
-                                                                   int32_t* __restrict__ counts) {
-  __shared__ int s_part[kRouteThreads];
-  const int e = blockIdx.x;
+// Block-wide exclusive scan of one value per thread; returns the thread's
+// exclusive prefix, and the total in *total.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* s_part, int* total) {
+  s_part[threadIdx.x] = v;
+  __syncthreads();
+  for (int o = 1; o < kRouteThreads; o <<= 1) {  // Hillis-Steele inclusive scan
+    const int u = threadIdx.x >= o ? s_part[threadIdx.x - o] : 0;
+    __syncthreads();
+    s_part[threadIdx.x] += u;
+    __syncthreads();
+  }
+  const int incl = s_part[threadIdx.x];
+  *total = s_part[kRouteThreads - 1];
+  __syncthreads();
+  return incl - v;
+}
+
+// Phase 2 for expert e: exclusive scan of hist_t[e, 0..nblk) in place; counts[e] = total.
+__device__ void route_scan_expert(int e, int32_t* __restrict__ hist_t, int nblk, int32_t* __restrict__ counts,
+                                  int* s_part) {
   int32_t* h = hist_t + (int64_t)e * nblk;
   const int per = (nblk + kRouteThreads - 1) / kRouteThreads;
   const int b0 = threadIdx.x * per;
   int sum = 0;
-  for (int b = b0; b < b0 + per && b < nblk; ++b) sum += h[b];
-  s_part[threadIdx.x] = sum;
-  __syncthreads();
-  // Hillis-Steele inclusive scan of the per-thread sums.
-  for (int o = 1; o < kRouteThreads; o <<= 1) {
-    int v = threadIdx.x >= o ? s_part[threadIdx.x - o] : 0;
-    __syncthreads();
-    s_part[threadIdx.x] += v;
-    __syncthreads();
-  }
-  int run = s_part[threadIdx.x] - sum;
+  // data written by other blocks before a grid barrier is read at L2 (.cg), past any stale L1 line
+  for (int b = b0; b < b0 + per && b < nblk; ++b) sum += __ldcg(h + b);
+  int total;
+  int run = block_exclusive_scan(sum, s_part, &total);
   for (int b = b0; b < b0 + per && b < nblk; ++b) {
-    const int v = h[b];
+    const int v = __ldcg(h + b);
     h[b] = run;
     run += v;
   }
-  if (threadIdx.x == kRouteThreads - 1) counts[e] = s_part[kRouteThreads - 1];
+  if (threadIdx.x == 0) counts[e] = total;
 }
 
-__global__ void __launch_bounds__(kRouteThreads) route_emit_kernel(
-    int T, int E, int k, const int32_t* __restrict__ num_valid, const int32_t* __restrict__ chosen,
-    const int32_t* __restrict__ hist_t, int nblk, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-    int32_t* __restrict__ expert_indices, int32_t* __restrict__ token_indices, int32_t* __restrict__ inv,
-    unsigned int* err) {
-  __shared__ int s_off[1024];
-  __shared__ unsigned int s_bits[1024];
-  __shared__ int s_scan[kRouteThreads];
-  const int Tv = read_count(num_valid, T, nullptr);  // already flagged by select
+// Phase 3 for chunk c: rows of its tokens.  s_off holds the expert offsets.
+__device__ void route_emit_chunk(int c, int E, int k, int Tv, const int32_t* __restrict__ chosen,
+                                 const int32_t* __restrict__ hist_t, int nblk, const int* s_off, unsigned int* s_bits,
+                                 int32_t* __restrict__ expert_indices, int32_t* __restrict__ token_indices,
+                                 int32_t* __restrict__ inv) {
   const int tid = threadIdx.x;
-
-  // Exclusive scan of counts[0..E) -> expert offsets (each block recomputes it).
-  const int per = (E + kRouteThreads - 1) / kRouteThreads;
-  int sum = 0;
-  for (int e = tid * per; e < (tid + 1) * per && e < E; ++e) sum += counts[e];
-  s_scan[tid] = sum;
+  const int t0 = c * kTokBlock;
+  const int nt = min(kTokBlock, Tv - t0);
   for (int e = tid; e < E; e += kRouteThreads) s_bits[e] = 0u;
   __syncthreads();
-  for (int o = 1; o < kRouteThreads; o <<= 1) {
-    int v = tid >= o ? s_scan[tid - o] : 0;
-    __syncthreads();
-    s_scan[tid] += v;
-    __syncthreads();
-  }
-  int run = s_scan[tid] - sum;
-  for (int e = tid * per; e < (tid + 1) * per && e < E; ++e) {
-    s_off[e] = run;
-    run += counts[e];
-  }
-  const int total = s_scan[kRouteThreads - 1];
-  if (blockIdx.x == 0) {
-    for (int e = tid; e < E; e += kRouteThreads) offsets[e] = s_off[e];
-    if (tid == 0) {
-      counts[E] = total;
-      offsets[E] = total;
-      if (total != Tv * k) flag_error(err, MOE_DEVERR_BAD_COUNT);
-    }
-  }
-
-  const int t0 = blockIdx.x * kTokBlock;
-  const int nt = min(kTokBlock, Tv - t0);
-  if (nt <= 0) return;
-  // Mark which tokens of the block chose each expert.
-  for (int p = tid; p < nt * k; p += kRouteThreads) {
+  for (int p = tid; p < nt * k; p += kRouteThreads) {  // mark which tokens of the chunk chose each expert
     const int tl = p / k;
-    const int e = chosen[(int64_t)(t0 + tl) * k + (p % k)];
+    const int e = __ldcg(chosen + (int64_t)(t0 + tl) * k + (p % k));
     atomicOr(&s_bits[e], 1u << tl);
   }
   __syncthreads();
   for (int p = tid; p < nt * k; p += kRouteThreads) {
     const int tl = p / k, j = p % k, t = t0 + tl;
     const int32_t* ch = chosen + (int64_t)t * k;
-    const int e = ch[j];
+    const int e = __ldcg(ch + j);
     const int rank = __popc(s_bits[e] & ((1u << tl) - 1u));
-    const int row = s_off[e] + hist_t[(int64_t)e * nblk + blockIdx.x] + rank;
+    const int row = s_off[e] + __ldcg(hist_t + (int64_t)e * nblk + c) + rank;
     expert_indices[row] = e;
     token_indices[row] = t;
     if (inv) {
       int pos = 0;  // rows of t ascend with the expert index
-      for (int jj = 0; jj < k; ++jj) pos += ch[jj] < e;
+      for (int jj = 0; jj < k; ++jj) pos += __ldcg(ch + jj) < e;
       inv[(int64_t)t * k + pos] = row;
     }
   }
+  __syncthreads();
+}
+
+// Grid-wide barrier of a cooperative launch: every block arrives once per
+// barrier on a counter that starts at 0, so barrier n completes at n * grid
+// arrivals.  The wait is bounded (1 s); false means it gave up.
+__device__ bool grid_barrier(unsigned int* counter, unsigned int target) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(counter, 1u);
+    uint64_t t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    int ok = 1;
+    for (uint32_t i = 0;; ++i) {
+      unsigned int v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+      if (v >= target) break;
+      if ((i & 63) == 63) {
+        uint64_t t1;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+        if (t1 - t0 > 1000000000ull) {
+          ok = 0;
+          break;
+        }
+      }
+    }
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(kRouteThreads) route_coop_kernel(
+    const void* __restrict__ scores, int dtype, int64_t st, int64_t se, int T, int E, int k,
+    const int32_t* __restrict__ num_valid, int32_t* __restrict__ chosen, int32_t* __restrict__ hist_t, int nblk,
+    unsigned int* barrier, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ expert_indices, int32_t* __restrict__ token_indices, int32_t* __restrict__ inv,
+    unsigned int* err) {
+  __shared__ int s_a[1024];          // select: histogram; emit: expert offsets
+  __shared__ unsigned int s_bits[1024];
+  __shared__ int s_part[kRouteThreads];
+  const int Tv = read_count(num_valid, T, err);
+  const int nchunks = (Tv + kTokBlock - 1) / kTokBlock;
+  // chunks past the valid tokens still publish an empty histogram
+  for (int c = blockIdx.x; c < nblk; c += gridDim.x) {
+    if (c < nchunks) {
+      route_select_chunk<EPL>(c, scores, dtype, st, se, E, k, Tv, chosen, hist_t, nblk, s_a);
+    } else {
+      for (int e = threadIdx.x; e < E; e += kRouteThreads) hist_t[(int64_t)e * nblk + c] = 0;
+    }
+  }
+  if (!grid_barrier(barrier, gridDim.x)) {
+    if (threadIdx.x == 0) flag_error(err, MOE_DEVERR_TIMEOUT);
+    return;
+  }
+  for (int e = blockIdx.x; e < E; e += gridDim.x) route_scan_expert(e, hist_t, nblk, counts, s_part);
+  if (!grid_barrier(barrier, 2u * gridDim.x)) {
+    if (threadIdx.x == 0) flag_error(err, MOE_DEVERR_TIMEOUT);
+    return;
+  }
+  // expert offsets (every block recomputes them from the counts)
+  const int per = (E + kRouteThreads - 1) / kRouteThreads;
+  int sum = 0;
+  for (int e = threadIdx.x * per; e < (threadIdx.x + 1) * per && e < E; ++e) sum += __ldcg(counts + e);
+  int total;
+  int run = block_exclusive_scan(sum, s_part, &total);
+  for (int e = threadIdx.x * per; e < (threadIdx.x + 1) * per && e < E; ++e) {
+    s_a[e] = run;
+    run += __ldcg(counts + e);
+  }
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int e = threadIdx.x; e < E; e += kRouteThreads) offsets[e] = s_a[e];
+    if (threadIdx.x == 0) {
+      counts[E] = total;
+      offsets[E] = total;
+      if (total != Tv * k) flag_error(err, MOE_DEVERR_BAD_COUNT);
+    }
+  }
+  for (int c = blockIdx.x; c < nchunks; c += gridDim.x)
+    route_emit_chunk(c, E, k, Tv, chosen, hist_t, nblk, s_a, s_bits, expert_indices, token_indices, inv);
 }
 
 // ---------------------------------------------------------------------------
@@ -306,17 +367,36 @@ cudaError_t launch_small(const RouteArgs& a, cudaStream_t s) {
 }
 
 template <int EPL>
-void launch_select(const RouteArgs& a, int32_t* chosen, int32_t* hist_t, int nblk, cudaStream_t s) {
-  route_select_kernel<EPL><<<nblk, kRouteThreads, 0, s>>>(a.scores, a.dtype, a.stride_t, a.stride_e, a.T, a.E,
-                                                          a.top_k, a.num_valid, chosen, hist_t, nblk, a.err);
+cudaError_t launch_coop(const RouteArgs& a, int32_t* chosen, int32_t* hist_t, int nblk, unsigned int* barrier,
+                        cudaStream_t s) {
+  auto kern = route_coop_kernel<EPL>;
+  const int cap = device_sm_count() * resident_blocks_per_sm(reinterpret_cast<const void*>(kern), kRouteThreads);
+  const int grid = nblk < cap ? nblk : cap;
+  cudaError_t e = cudaMemsetAsync(barrier, 0, sizeof(unsigned int), s);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kRouteThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // the grid barriers need every block resident
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, a.scores, a.dtype, a.stride_t, a.stride_e, a.T, a.E, a.top_k, a.num_valid,
+                         chosen, hist_t, nblk, barrier, a.counts, a.offsets, a.expert_indices, a.token_indices,
+                         a.inv, a.err);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 }  // namespace
 
+// Workspace: [barrier counter | pad to 256] [chosen experts T*k] [histogram E x chunks]
 size_t route_workspace_bytes(int T, int E, int top_k) {
   const size_t nblk = (size_t)(T + kTokBlock - 1) / kTokBlock;
   const size_t chosen = ((size_t)T * top_k * 4 + 255) / 256 * 256;
-  return chosen + nblk * (size_t)E * 4 + 256;
+  return 256 + chosen + nblk * (size_t)E * 4 + 256;
 }
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
@@ -335,20 +415,16 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
     return launch_small<8>(a, s);
   }
   char* ws = static_cast<char*>(a.ws);
-  int32_t* chosen = reinterpret_cast<int32_t*>(ws);
-  int32_t* hist_t = reinterpret_cast<int32_t*>(ws + ((size_t)a.T * a.top_k * 4 + 255) / 256 * 256);
+  unsigned int* barrier = reinterpret_cast<unsigned int*>(ws);
+  int32_t* chosen = reinterpret_cast<int32_t*>(ws + 256);
+  int32_t* hist_t = reinterpret_cast<int32_t*>(ws + 256 + ((size_t)a.T * a.top_k * 4 + 255) / 256 * 256);
   const int epl = (a.E + 31) / 32;
-  if (epl <= 1) launch_select<1>(a, chosen, hist_t, nblk, s);
-  else if (epl <= 2) launch_select<2>(a, chosen, hist_t, nblk, s);
-  else if (epl <= 4) launch_select<4>(a, chosen, hist_t, nblk, s);
-  else if (epl <= 8) launch_select<8>(a, chosen, hist_t, nblk, s);
-  else if (epl <= 16) launch_select<16>(a, chosen, hist_t, nblk, s);
-  else launch_select<32>(a, chosen, hist_t, nblk, s);
-  route_scan_kernel<<<a.E, kRouteThreads, 0, s>>>(hist_t, nblk, a.counts);
-  route_emit_kernel<<<nblk, kRouteThreads, 0, s>>>(a.T, a.E, a.top_k, a.num_valid, chosen, hist_t, nblk,
-                                                   a.counts, a.offsets, a.expert_indices, a.token_indices,
-                                                   a.inv, a.err);
-  return cudaGetLastError();
+  if (epl <= 1) return launch_coop<1>(a, chosen, hist_t, nblk, barrier, s);
+  if (epl <= 2) return launch_coop<2>(a, chosen, hist_t, nblk, barrier, s);
+  if (epl <= 4) return launch_coop<4>(a, chosen, hist_t, nblk, barrier, s);
+  if (epl <= 8) return launch_coop<8>(a, chosen, hist_t, nblk, barrier, s);
+  if (epl <= 16) return launch_coop<16>(a, chosen, hist_t, nblk, barrier, s);
+  return launch_coop<32>(a, chosen, hist_t, nblk, barrier, s);
 }
 
 }  // namespace moe
