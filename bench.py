@@ -395,8 +395,9 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
 # summarised under profiles/, with the hash of the kernel sources they were taken
 # on: when those sources change the figure no longer applies and is reported as null.
 TRAFFIC: dict = {
-    ("decode", "gemm_w13_silu"): (2_689_735_000 + 5_240_320, "grouped_gemm.cu", "17e071b8aa3f"),
-    ("prefill_fp8", "gemm_w13"): (1_386_018_000 + 249_785_600, "grouped_gemm.cu", "17e071b8aa3f"),
+    ("decode", "expert_mlp"): (4_037_536_000 + 6_564_096, "grouped_gemm.cu", "dbbc561c7cec"),
+    ("prefill_fp8", "gemm_w13"): (1_385_705_000 + 249_711_616, "grouped_gemm.cu", "dbbc561c7cec"),
+    ("padded_fp8", "gather_quant"): (93_180_672 + 118_366_720, "rowwise.cu", "d196775be574"),
 }
 
 
