@@ -207,7 +207,8 @@ def run_ours(args, cfg):
     x = workloads.make_tokens(cfg, seed=rank).to(dev)
     s = workloads.make_scores(cfg, seed=rank).to(dev)
     w13, w2 = workloads.make_weights(cfg, seed=0, device=dev)
-    layer = MoELayer.from_weights(cfg, w13, w2)
+    pairs = {"auto": None, "on": True, "off": False}[args.cta_pairs]
+    layer = MoELayer.from_weights(cfg, w13, w2, cta_pairs=pairs)
     if args.no_cpu_baseline or world > 1 or rank != 0:
         # only the oracle baseline needs the source weights (fp32 for FP8 layers)
         del w13, w2
@@ -490,6 +491,8 @@ def main(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU-baseline leg")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work of the oracle baseline sample")
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
+    p.add_argument("--cta-pairs", choices=["auto", "on", "off"], default="auto",
+                   help="256-row GEMM tiles on CTA pairs (default: when the batch has >= 256 rows per expert)")
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be at least 3")

@@ -61,6 +61,11 @@ extern "C" {
 /* Grouped-GEMM epilogues. */
 #define MOE_EPILOGUE_NONE 0     /* y[r, n] = (x_r . w_e[n]) (times the two scales for FP8), bf16 */
 #define MOE_EPILOGUE_SILU_MUL 1 /* with N = 2H: y[r, j] = silu(v_j) * v_{H+j}, j < H, bf16 */
+/* OR-ed into `epilogue` of the grouped GEMMs: compute 256-row x 256-column tiles on
+ * pairs of SMs (a 2-CTA cluster, tcgen05 cta_group::2).  Same results; faster when
+ * experts hold many rows; an expert whose rows end mid-tile still pays for the
+ * whole 256-row tile. */
+#define MOE_GEMM_CTA_PAIRS 0x100
 
 /* Device-side error bits (moe_device_error). */
 #define MOE_DEVERR_BAD_INDEX 0x1   /* a token or expert index outside its range was skipped */

@@ -22,6 +22,7 @@ HEADER = _PKG.parent / "include" / "moe.h"
 MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_WORKSPACE = 0, -1, -2, -3, -4
 MOE_DTYPE_BF16, MOE_DTYPE_F32, MOE_DTYPE_E4M3 = 0, 1, 2
 MOE_EPILOGUE_NONE, MOE_EPILOGUE_SILU_MUL = 0, 1
+MOE_GEMM_CTA_PAIRS = 0x100
 MOE_DEVERR_BAD_INDEX, MOE_DEVERR_BAD_COUNT, MOE_DEVERR_TIMEOUT = 1, 2, 4
 
 
@@ -216,7 +217,7 @@ def moe_grouped_gemm(x, w, counts, *, epilogue: int = MOE_EPILOGUE_NONE, out=Non
     assert K == K2
     _need(x, torch.bfloat16, "x")
     _need(w, torch.bfloat16, "w")
-    n_out = N // 2 if epilogue == MOE_EPILOGUE_SILU_MUL else N
+    n_out = N // 2 if (epilogue & 0xFF) == MOE_EPILOGUE_SILU_MUL else N
     si, t_out, acc = _scatter_args(scatter_indices, out, accumulate)
     if out is None:
         out = torch.empty(a_max, n_out, dtype=torch.bfloat16, device=x.device)
@@ -233,7 +234,7 @@ def moe_grouped_gemm_fp8_rowwise(x, w, counts, x_scale, w_scale, *, epilogue: in
     assert K == K2
     _need(x, torch.float8_e4m3fn, "x")
     _need(w, torch.float8_e4m3fn, "w")
-    n_out = N // 2 if epilogue == MOE_EPILOGUE_SILU_MUL else N
+    n_out = N // 2 if (epilogue & 0xFF) == MOE_EPILOGUE_SILU_MUL else N
     si, t_out, acc = _scatter_args(scatter_indices, out, accumulate)
     if out is None:
         out = torch.empty(a_max, n_out, dtype=torch.bfloat16, device=x.device)

@@ -245,6 +245,8 @@ static int grouped_gemm_common(const void* x, const void* w, const int32_t* coun
                                const int32_t* scatter, int T_out, int accumulate, bool fp8,
                                cudaStream_t stream) {
   if (E < 1 || a_max < 0 || N < 0 || K < 0) return MOE_ERR_INVALID;
+  const bool pairs = (epilogue & MOE_GEMM_CTA_PAIRS) != 0;
+  epilogue &= ~MOE_GEMM_CTA_PAIRS;
   if (epilogue != MOE_EPILOGUE_NONE && epilogue != MOE_EPILOGUE_SILU_MUL) return MOE_ERR_INVALID;
   if (a_max == 0 || N == 0) return MOE_OK;
   if (!x || !w || !counts || !y) return MOE_ERR_INVALID;
@@ -254,8 +256,8 @@ static int grouped_gemm_common(const void* x, const void* w, const int32_t* coun
   if (epilogue == MOE_EPILOGUE_SILU_MUL && (N % 32 != 0)) return MOE_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return MOE_ERR_UNSUPPORTED;
   if (scatter && (epilogue != MOE_EPILOGUE_NONE || T_out < 0)) return MOE_ERR_INVALID;
-  moe::GemmArgs g{x, w, counts, x_scale, w_scale, E, a_max, N, K, y, epilogue, fp8, scatter, T_out, accumulate,
-                  nullptr};
+  moe::GemmArgs g{x, w, counts, x_scale, w_scale, E, a_max, N, K, y, epilogue, fp8, pairs, scatter, T_out,
+                  accumulate, nullptr};
   int rc = device_error_word(&g.err);
   if (rc != MOE_OK) return rc;
   cudaError_t e = moe::launch_grouped_gemm(g, stream);

@@ -243,6 +243,93 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Epilogue of one accumulator tile for the calling thread: TMEM lane = the
+// thread's row of the tile (row_in_tile), columns of the phase's N tile.
+// FP8 scales, the SiLU*mul of the two halves or the fused combine, bf16 stores.
+template <bool FP8>
+__device__ __forceinline__ void epilogue_tile(const Phase& p, const Tile& t, int row_in_tile, uint32_t tbase,
+                                              unsigned int* err) {
+  const bool row_ok = row_in_tile < t.rows;
+  const int row = t.row0 + row_in_tile;
+  const int n_out = p.n_out;
+  float xs = 1.0f;
+  if (FP8 && row_ok) xs = __ldg(p.x_scale + row);
+  __nv_bfloat16* yrow = p.y + (int64_t)row * n_out;  // (the scatter epilogue redirects it)
+  const int col0 = t.n_idx * p.n_tile_cols;
+  const float* wsc = FP8 ? p.w_scale + (int64_t)t.expert * p.N : nullptr;
+  if (p.epi == MOE_EPILOGUE_SILU_MUL) {
+    const int H = p.N / 2;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 2; c += 32) {
+      float v0[32], v1[32];
+      tmem_ld32(tbase + c, v0);
+      tmem_ld32(tbase + kBN / 2 + c, v1);
+      if (row_ok && col0 + c < n_out) {
+        float z[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float a0 = v0[i], a1 = v1[i];
+          if (FP8) {
+            const int col = col0 + c + i < H ? col0 + c + i : H - 1;
+            a0 = __fmul_rn(__fmul_rn(a0, xs), __ldg(wsc + col));
+            a1 = __fmul_rn(__fmul_rn(a1, xs), __ldg(wsc + H + col));
+          }
+          // the unfused pipeline rounds the GEMM output to bf16 before silu_mul
+          a0 = __bfloat162float(__float2bfloat16_rn(a0));
+          a1 = __bfloat162float(__float2bfloat16_rn(a1));
+          z[i] = silu_mul_f32(a0, a1);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (col0 + c + 8 * q < n_out)
+            *reinterpret_cast<uint4*>(yrow + col0 + c + 8 * q) = f32_to_bf16x8(z + 8 * q);
+      }
+    }
+  } else {
+    // The combine fused in (top_k = 1): this row's destination is its token's row.
+    bool dst_ok = row_ok;
+    if (p.scatter && row_ok) {
+      const int tok = __ldg(p.scatter + row);
+      if ((unsigned)tok < (unsigned)p.T_out) {
+        yrow = p.y + (int64_t)tok * n_out;
+      } else {
+        dst_ok = false;
+        flag_error(err, MOE_DEVERR_BAD_INDEX);
+      }
+    }
+    const bool add = p.scatter && p.accumulate;
+#pragma unroll 1
+    for (int c = 0; c < kBN; c += 32) {
+      float v[32];
+      tmem_ld32(tbase + c, v);
+      if (dst_ok && col0 + c < n_out) {
+        if (FP8) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int col = col0 + c + i < n_out ? col0 + c + i : n_out - 1;
+            v[i] = __fmul_rn(__fmul_rn(v[i], xs), __ldg(wsc + col));
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (col0 + c + 8 * q < n_out) {
+            uint4* dst = reinterpret_cast<uint4*>(yrow + col0 + c + 8 * q);
+            uint4 o = f32_to_bf16x8(v + 8 * q);
+            if (add) {  // as moe_scatter_add on the bf16 GEMM output: fp32 add, one rounding
+              float fo[8], fi[8];
+              bf16x8_to_f32(*dst, fo);
+              bf16x8_to_f32(o, fi);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) fo[i] = __fadd_rn(fo[i], fi[i]);
+              o = f32_to_bf16x8(fo);
+            }
+            *dst = o;
+          }
+      }
+    }
+  }
+}
+
 template <bool FP8, int NPHASE>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_b0,
@@ -490,85 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       }
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * kBN);
-      const bool row_ok = row_in_tile < t.rows;
-      const int row = t.row0 + row_in_tile;
-      const int n_out = p.n_out;
-      float xs = 1.0f;
-      if (FP8 && row_ok) xs = __ldg(p.x_scale + row);
-      __nv_bfloat16* yrow = p.y + (int64_t)row * n_out;  // (the scatter epilogue redirects it)
-      const int col0 = t.n_idx * p.n_tile_cols;
-      const float* wsc = FP8 ? p.w_scale + (int64_t)t.expert * p.N : nullptr;
-      if (p.epi == MOE_EPILOGUE_SILU_MUL) {
-        const int H = p.N / 2;
-#pragma unroll 1
-        for (int c = 0; c < kBN / 2; c += 32) {
-          float v0[32], v1[32];
-          tmem_ld32(tbase + c, v0);
-          tmem_ld32(tbase + kBN / 2 + c, v1);
-          if (row_ok && col0 + c < n_out) {
-            float z[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              float a0 = v0[i], a1 = v1[i];
-              if (FP8) {
-                const int col = col0 + c + i < H ? col0 + c + i : H - 1;
-                a0 = __fmul_rn(__fmul_rn(a0, xs), __ldg(wsc + col));
-                a1 = __fmul_rn(__fmul_rn(a1, xs), __ldg(wsc + H + col));
-              }
-              // the unfused pipeline rounds the GEMM output to bf16 before silu_mul
-              a0 = __bfloat162float(__float2bfloat16_rn(a0));
-              a1 = __bfloat162float(__float2bfloat16_rn(a1));
-              z[i] = silu_mul_f32(a0, a1);
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              if (col0 + c + 8 * q < n_out)
-                *reinterpret_cast<uint4*>(yrow + col0 + c + 8 * q) = f32_to_bf16x8(z + 8 * q);
-          }
-        }
-      } else {
-        // The combine fused in (top_k = 1): this row's destination is its token's row.
-        bool dst_ok = row_ok;
-        if (p.scatter && row_ok) {
-          const int tok = __ldg(p.scatter + row);
-          if ((unsigned)tok < (unsigned)p.T_out) {
-            yrow = p.y + (int64_t)tok * n_out;
-          } else {
-            dst_ok = false;
-            flag_error(err, MOE_DEVERR_BAD_INDEX);
-          }
-        }
-        const bool add = p.scatter && p.accumulate;
-#pragma unroll 1
-        for (int c = 0; c < kBN; c += 32) {
-          float v[32];
-          tmem_ld32(tbase + c, v);
-          if (dst_ok && col0 + c < n_out) {
-            if (FP8) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const int col = col0 + c + i < n_out ? col0 + c + i : n_out - 1;
-                v[i] = __fmul_rn(__fmul_rn(v[i], xs), __ldg(wsc + col));
-              }
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              if (col0 + c + 8 * q < n_out) {
-                uint4* dst = reinterpret_cast<uint4*>(yrow + col0 + c + 8 * q);
-                uint4 o = f32_to_bf16x8(v + 8 * q);
-                if (add) {  // as moe_scatter_add on the bf16 GEMM output: fp32 add, one rounding
-                  float fo[8], fi[8];
-                  bf16x8_to_f32(*dst, fo);
-                  bf16x8_to_f32(o, fi);
-#pragma unroll
-                  for (int i = 0; i < 8; ++i) fo[i] = __fadd_rn(fo[i], fi[i]);
-                  o = f32_to_bf16x8(fo);
-                }
-                *dst = o;
-              }
-          }
-        }
-      }
+      epilogue_tile<FP8>(p, t, row_in_tile, tbase, err);
       tc_fence_before();
       if (NPHASE == 2 && ph == 0) {
         // publish this warp's share of the tile's z rows to the phase-1 producers
@@ -594,6 +603,362 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   tc_fence_after();
   if (warp == 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols) : "memory");
+}
+
+// ------------------------------------------------- CTA-pair kernel (2 SMs)
+//
+// A cluster of two CTAs computes one 256 x 256 tile with tcgen05.mma.cta_group::2:
+// CTA r holds rows [128 r, 128 r + 128) of the A tile and weight rows
+// [128 r, 128 r + 128) of the 256-row B tile (for SiLU*mul: CTA 0 the w_in block,
+// CTA 1 the gate block); the leader (rank 0) issues the M = 256, N = 256 MMAs,
+// which read both CTAs' shared memory and leave each CTA's 128 rows x 256
+// columns in its own tensor memory.  Per CTA a K block moves 32 KB (A 16 + B 16)
+// instead of 48, and six stages fit.
+//   - TMEM is allocated and freed collectively by the pair (cta_group::2).
+//   - Both CTAs' TMA loads complete on the leader's full barrier, whose single
+//     arrival (expect_tx of both CTAs' bytes) comes from the leader's producer.
+//   - The leader's commits are multicast to the empty and tensor-full barriers
+//     of both CTAs; both CTAs' epilogue warps arrive on the leader's
+//     tensor-empty barrier (8 arrivals).
+//   - Before exit each producer waits until its last stages were consumed, then
+//     the pair meets at a cluster barrier and frees TMEM together.
+constexpr int kPairStages = 6;
+constexpr int kPairBM = 2 * kBM;                           // rows of a pair tile
+constexpr int kPairABytes = kBM * kBKBytes;                // 16 KB: this CTA's A rows
+constexpr int kPairBBytes = (kBN / 2) * kBKBytes;          // 16 KB: this CTA's half of B
+constexpr int kPairStageBytes = kPairABytes + kPairBBytes;  // 32 KB
+
+struct PairSmem {
+  static constexpr int a = 0;
+  static constexpr int b = a + kPairStages * kPairABytes;
+  static constexpr int bars = b + kPairStages * kPairBBytes;  // full[S], empty[S], tfull[2], tempty[2], drain
+  static constexpr int nbars = 2 * kPairStages + 2 * kAccBufs + 1;
+  static constexpr int misc = bars + nbars * 8;
+  static constexpr int sched = misc + 16;
+  static constexpr int bytes_for(int E) { return sched + (3 * E + 2) * 4; }
+};
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// The shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// TMA load into this CTA's shared memory, completing on an mbarrier of either CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster, int c0,
+                                                 int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+template <bool FP8>
+__device__ __forceinline__ uint32_t instr_desc_pair() {
+  const uint32_t fmt = FP8 ? 0u : 1u;
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kPairBM >> 4) << 24);
+}
+
+template <bool FP8>
+__device__ __forceinline__ void mma_issue_pair(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if constexpr (FP8) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+  }
+}
+
+// Arrive on the barrier at this shared-memory offset in both CTAs of the pair once
+// the leader's MMAs issued so far have completed.
+__device__ __forceinline__ void mma_commit_pair_both(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)0x3)
+      : "memory");
+}
+
+__device__ __forceinline__ void spin_ns(uint64_t ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (global_timer_ns() - t0 < ns) {
+  }
+}
+
+template <bool FP8>
+__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
+    const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+    const int32_t* __restrict__ counts, const Phase p, int E, int a_max, unsigned int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  const uint32_t sbase = smem_u32(smem);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank() & 1u;
+  const bool leader = rank == 0;
+  const int cid = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + PairSmem::bars);
+  auto bar_full = [&](int s) { return smem_u32(&bars[s]); };
+  auto bar_empty = [&](int s) { return smem_u32(&bars[kPairStages + s]); };
+  auto bar_tfull = [&](int b) { return smem_u32(&bars[2 * kPairStages + b]); };
+  auto bar_tempty = [&](int b) { return smem_u32(&bars[2 * kPairStages + kAccBufs + b]); };
+  const uint32_t bar_drain = smem_u32(&bars[2 * kPairStages + 2 * kAccBufs]);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + PairSmem::misc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + PairSmem::misc + 4);
+  int* s_total = reinterpret_cast<int*>(smem + PairSmem::misc + 8);
+  int* tile_start = reinterpret_cast<int*>(smem + PairSmem::sched);  // [E + 1]
+  int* row_off = tile_start + (E + 1);                                // [E + 1]
+  int* mtiles = row_off + (E + 1);                                    // [E]
+
+  if (warp == 0 && lane == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    for (int b = 0; b < kAccBufs; ++b) {
+      mbar_init(bar_tfull(b), 1);
+      mbar_init(bar_tempty(b), 8);  // 4 epilogue warps in each CTA of the pair
+    }
+    mbar_init(bar_drain, 1);
+    *s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tma_prefetch_desc(&map_a);
+    tma_prefetch_desc(&map_b);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(s_tmem)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  if (warp == 2) {
+    // 256-row pair tiles per expert (the same scan as the single-CTA kernel).
+    int run_rows = 0, run_tiles = 0;
+    bool bad = false;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      int c = e < E ? counts[e] : 0;
+      if (c < 0) {
+        c = 0;
+        bad = true;
+      }
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int start = run_rows + incl - c;
+      if (start > a_max) start = a_max;
+      int end = run_rows + incl;
+      if (end > a_max) {
+        end = a_max;
+        bad = true;
+      }
+      const int mt = (end - start + kPairBM - 1) / kPairBM;
+      int tincl = mt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, tincl, o);
+        if (lane >= o) tincl += v;
+      }
+      if (e < E) {
+        row_off[e] = start;
+        tile_start[e] = run_tiles + tincl - mt;
+        mtiles[e] = mt;
+      }
+      run_rows = min(__shfl_sync(0xffffffffu, run_rows + incl, 31), a_max);
+      run_tiles += __shfl_sync(0xffffffffu, tincl, 31);
+    }
+    if (lane == 0) {
+      row_off[E] = run_rows;
+      tile_start[E] = run_tiles;
+      *s_total = run_tiles;
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0 && blockIdx.x == 0) flag_error(err, MOE_DEVERR_BAD_COUNT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers exist before any cross-CTA arrival
+  tc_fence_after();
+
+  const uint32_t tmem_base = *s_tmem;
+  const int total_tiles = *s_total * p.n_tiles;
+  const int elems_per_kb = FP8 ? kBKBytes : kBKBytes / 2;
+  // decode_tile works in 128-row units; a pair tile is decoded in 256-row units
+  auto locate = [&](int tile) {
+    const int mt_global = tile / p.n_tiles;
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tile_start[mid] <= mt_global) lo = mid;
+      else hi = mid - 1;
+    }
+    const int e = lo;
+    const int local = tile - tile_start[e] * p.n_tiles;
+    Tile t;
+    t.expert = e;
+    t.n_idx = local / mtiles[e];
+    t.row0 = row_off[e] + (local % mtiles[e]) * kPairBM;
+    const int rows_left = row_off[e + 1] - t.row0;
+    t.rows = rows_left < kPairBM ? rows_left : kPairBM;
+    return t;
+  };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint32_t full_leader0 = map_to_rank(bar_full(0), 0);
+      int s = 0;
+      uint32_t phase = 0;
+      uint32_t issued_mask = 0, issued_parity = 0;
+      bool ok = true;
+      for (int tile = cid; tile < total_tiles && ok; tile += nclusters) {
+        const Tile t = locate(tile);
+        int b_row;
+        if (p.epi == MOE_EPILOGUE_SILU_MUL)
+          b_row = t.expert * p.N + (int)rank * (p.N / 2) + t.n_idx * (kBN / 2);
+        else
+          b_row = t.expert * p.N + t.n_idx * kBN + (int)rank * (kBN / 2);
+        const int a_row = t.row0 + (int)rank * kBM;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(bar_empty(s), phase ^ 1u, s_abort)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(bar_full(s), 2 * kPairStageBytes);
+          const uint32_t full_leader = full_leader0 + (uint32_t)(s * 8);
+          const int kc = kb * elems_per_kb;
+          tma_load_2d_pair(sbase + PairSmem::a + s * kPairABytes, &map_a, full_leader, kc, a_row);
+          tma_load_2d_pair(sbase + PairSmem::b + s * kPairBBytes, &map_b, full_leader, kc, b_row);
+          issued_mask |= 1u << s;
+          issued_parity = (issued_parity & ~(1u << s)) | (phase << s);
+          if (++s == kPairStages) {
+            s = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (ok) {
+        // every stage this CTA filled has been consumed by the pair's MMAs
+        for (int i = 0; i < kPairStages; ++i)
+          if ((issued_mask >> i) & 1u && !mbar_wait(bar_empty(i), (issued_parity >> i) & 1u, s_abort)) ok = false;
+      }
+      if (!ok) {
+        flag_error(err, MOE_DEVERR_TIMEOUT);
+        *s_abort = 1;
+        spin_ns(kDrainTimeoutNs);  // copies in flight complete on the leader's barrier: give them time to land
+      }
+    }
+  } else if (warp == 1) {
+    // --------------------------------------------------------------- MMA (leader)
+    if (lane == 0 && leader) {
+      const uint32_t idesc = instr_desc_pair<FP8>();
+      int s = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true, issued_any = false;
+      for (int tile = cid; tile < total_tiles && ok; tile += nclusters) {
+        if (!mbar_wait(bar_tempty(acc), acc_phase ^ 1u, s_abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * kBN);
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(bar_full(s), phase, s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = sbase + PairSmem::a + s * kPairABytes;
+          const uint32_t b_addr = sbase + PairSmem::b + s * kPairBBytes;
+#pragma unroll
+          for (int kk = 0; kk < kBKBytes / 32; ++kk)
+            mma_issue_pair<FP8>(d, smem_desc_sw128(a_addr + kk * 32), smem_desc_sw128(b_addr + kk * 32), idesc,
+                                (kb | kk) != 0);
+          issued_any = true;
+          mma_commit_pair_both(bar_empty(s));
+          if (++s == kPairStages) {
+            s = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_pair_both(bar_tfull(acc));
+        if (++acc == kAccBufs) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        flag_error(err, MOE_DEVERR_TIMEOUT);
+        *s_abort = 1;
+        if (issued_any) {  // the MMAs in flight finish before tensor memory is freed
+          mma_commit_pair_both(bar_drain);
+          mbar_wait(bar_drain, 0, nullptr, kDrainTimeoutNs);
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue (both CTAs)
+    const int sub = warp & 3;
+    const int row_in_tile = (int)rank * kBM + sub * 32 + lane;
+    const uint32_t tempty_leader0 = map_to_rank(bar_tempty(0), 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = cid; tile < total_tiles; tile += nclusters) {
+      const Tile t = locate(tile);
+      if (!mbar_wait(bar_tfull(acc), acc_phase, s_abort)) {
+        if (lane == 0) flag_error(err, MOE_DEVERR_TIMEOUT);
+        *s_abort = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * kBN);
+      epilogue_tile<FP8>(p, t, row_in_tile, tbase, err);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty_leader0 + (uint32_t)(acc * 8));
+      if (++acc == kAccBufs) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  // ---- teardown: the pair meets, then frees its tensor memory together
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  tc_fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols) : "memory");
 }
 
 // ------------------------------------------------------------------- host
@@ -680,6 +1045,37 @@ cudaError_t launch_phases(const CUtensorMap& a0, const CUtensorMap& b0, const CU
   return cudaGetLastError();
 }
 
+template <bool FP8>
+cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const int32_t* counts, const Phase& p, int E,
+                        int a_max, unsigned int* err, cudaStream_t s) {
+  const int smem = PairSmem::bytes_for(E) + 1024;
+  auto kern = grouped_gemm_pair_kernel<FP8>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(2 * (device_sm_count() / 2));
+  int max_clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg);
+  if (e != cudaSuccess) return e;
+  if (max_clusters < 1) return cudaErrorNotSupported;
+  const int64_t tiles_ub = ((int64_t)(a_max + kPairBM - 1) / kPairBM + E) * p.n_tiles;
+  const int nclusters = (int)(tiles_ub < max_clusters ? tiles_ub : max_clusters);
+  cfg.gridDim = dim3(2 * nclusters);
+  e = cudaLaunchKernelEx(&cfg, kern, a, b, counts, p, E, a_max, err);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_grouped_gemm(const GemmArgs& g, cudaStream_t s) {
@@ -691,6 +1087,10 @@ cudaError_t launch_grouped_gemm(const GemmArgs& g, cudaStream_t s) {
   p.scatter = g.scatter;
   p.T_out = g.T_out;
   p.accumulate = g.accumulate;
+  if (g.pairs) {
+    if (g.fp8) return launch_pair<true>(ma, mb, g.counts, p, g.E, g.a_max, g.err, s);
+    return launch_pair<false>(ma, mb, g.counts, p, g.E, g.a_max, g.err, s);
+  }
   if (g.fp8) return launch_phases<true, 1>(ma, mb, ma, mb, g.counts, p, p, g.E, g.a_max, nullptr, g.err, s);
   return launch_phases<false, 1>(ma, mb, ma, mb, g.counts, p, p, g.E, g.a_max, nullptr, g.err, s);
 }

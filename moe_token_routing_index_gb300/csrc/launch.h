@@ -88,6 +88,7 @@ struct GemmArgs {
   void* y;
   int epilogue;
   bool fp8;
+  bool pairs;              // 256-row tiles on CTA pairs (cta_group::2)
   const int32_t* scatter;  // nullable: combine row r into y[scatter[r]] (top_k = 1)
   int T_out;               // rows of y when scattering
   int accumulate;

@@ -52,7 +52,7 @@ class MoELayer:
 
     def __init__(self, top_k: int, w13: torch.Tensor, w2: torch.Tensor, w13_scale: torch.Tensor | None = None,
                  w2_scale: torch.Tensor | None = None, scale_ub: float | None = None,
-                 fused_mlp: bool | None = None):
+                 fused_mlp: bool | None = None, cta_pairs: bool | None = None):
         self.E, n2, self.D = w13.shape
         self.H = n2 // 2
         assert w2.shape == (self.E, self.D, self.H), "w2 must be [E, D, H]"
@@ -68,6 +68,11 @@ class MoELayer:
         # None: one launch for both bf16 GEMMs when the batch averages at most one
         # 128-row tile per expert (weight-streaming, HBM-bound), else two launches.
         self.fused_mlp = fused_mlp
+        # None: 256-row tiles on CTA pairs for the bf16 GEMMs when the batch averages
+        # at least one such tile per expert; 128-row tiles otherwise.  The FP8 GEMMs
+        # keep 128-row tiles: on GB300 their pair tiles measured slower (prefill,
+        # 512 rows per expert) or padded more rows (344 rows per expert).
+        self.cta_pairs = cta_pairs
         self._bufs: _Buffers | None = None
 
     @classmethod
@@ -118,6 +123,7 @@ class MoELayer:
         inv = r["inv_rows"] if self.top_k > 1 else None
         k = self.top_k
         fuse_combine = k == 1
+        pairs = mb.MOE_GEMM_CTA_PAIRS if self.use_cta_pairs(T) else 0
         # the w2 GEMM writes either the routed rows o, or (top_k = 1) the tokens' rows of out
         w2_out = dict(out=out, scatter_indices=ti, accumulate=accumulate) if fuse_combine else dict(out=b.o)
         st = [("route", lambda: mb.moe_route(scores, k, num_valid_tokens, out=r, workspace=b.ws))]
@@ -130,8 +136,9 @@ class MoELayer:
             else:
                 st += [
                     ("gemm_w13_silu", lambda: mb.moe_grouped_gemm(b.xr, self.w13, counts,
-                                                                  epilogue=mb.MOE_EPILOGUE_SILU_MUL, out=b.z)),
-                    ("gemm_w2", lambda: mb.moe_grouped_gemm(b.z, self.w2, counts, **w2_out)),
+                                                                  epilogue=mb.MOE_EPILOGUE_SILU_MUL | pairs,
+                                                                  out=b.z)),
+                    ("gemm_w2", lambda: mb.moe_grouped_gemm(b.z, self.w2, counts, epilogue=pairs, **w2_out)),
                 ]
         else:
             st += [
@@ -139,11 +146,11 @@ class MoELayer:
                                                                    inv_rows=inv, top_k=k, out=b.xr,
                                                                    out_scale=b.xs)),
                 ("gemm_w13", lambda: mb.moe_grouped_gemm_fp8_rowwise(b.xr, self.w13, counts, b.xs, self.w13_scale,
-                                                                     out=b.y)),
+                                                                     epilogue=pairs, out=b.y)),
                 ("silu_quant", lambda: mb.moe_silu_mul_quant(b.y, self.H, self.scale_ub, valid, out=b.z,
                                                              out_scale=b.zs)),
                 ("gemm_w2", lambda: mb.moe_grouped_gemm_fp8_rowwise(b.z, self.w2, counts, b.zs, self.w2_scale,
-                                                                    **w2_out)),
+                                                                    epilogue=pairs, **w2_out)),
             ]
         if not fuse_combine:
             st.append(("scatter", lambda: mb.moe_scatter_add(out, b.o, ti, inv, k, valid, accumulate=accumulate)))
@@ -166,6 +173,11 @@ class MoELayer:
         if self.fused_mlp is not None:
             return self.fused_mlp
         return T * self.top_k <= 128 * self.E
+
+    def use_cta_pairs(self, T: int) -> bool:
+        if self.cta_pairs is not None:
+            return self.cta_pairs
+        return not self.fp8 and T * self.top_k >= 256 * self.E
 
     def kernel_launches(self, T: int | None = None) -> int:
         """Kernels one forward launches: routing (1 for small batches, else 3),

@@ -110,3 +110,23 @@ def test_forward_is_deterministic():
     o1 = layer(x, s).clone()
     o2 = layer(x, s)
     assert torch.equal(o1, o2)
+
+
+@pytest.mark.parametrize("name", ["fine_grained", "tiny", "prefill_fp8"])
+def test_forward_cta_pair_tiles_change_no_bit(name):
+    """256-row tiles on CTA pairs accumulate each output element in the same order
+    as 128-row tiles, so the whole forward is identical either way."""
+    from moe_token_routing_index_gb300 import binding as mb
+    from moe_token_routing_index_gb300.forward import MoELayer
+
+    cfg = workloads.CONFIGS[name]
+    x = workloads.make_tokens(cfg).cuda()
+    s = workloads.make_scores(cfg).cuda()
+    w13, w2 = workloads.make_weights(cfg, device="cuda")
+    outs = []
+    for pairs in (False, True):
+        layer = MoELayer.from_weights(cfg, w13, w2, cta_pairs=pairs, fused_mlp=False)
+        outs.append(layer(x, s).clone())
+    torch.cuda.synchronize()
+    assert mb.device_error() == 0
+    assert torch.equal(outs[0], outs[1])

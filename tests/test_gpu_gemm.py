@@ -257,3 +257,57 @@ def test_expert_mlp_fused_combine_equals_unfused():
     mb.moe_expert_mlp(x, w13, w2, cd, out=got, scatter_indices=perm, accumulate=False)
     assert mb.device_error() == 0
     assert torch.equal(got, ref)
+
+
+PAIR_SHAPES = [
+    # E, counts, N, K, a_max: row tiles of 256 on CTA pairs; odd 128-row tile counts, empty experts
+    (1, [256], 256, 64, None),
+    (2, [512, 256], 512, 320, None),
+    (3, [5, 0, 130], 256, 64, None),
+    (4, [1, 0, 0, 383], 48, 80, 500),
+    (5, [300, 17, 0, 640, 250], 1040, 272, 1300),
+]
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("E,counts,N,K,a_max", PAIR_SHAPES)
+def test_grouped_gemm_cta_pairs(E, counts, N, K, a_max, fp8):
+    """256-row tiles on CTA pairs (cta_group::2): within the oracle bound, bit-identical to the
+    single-CTA tiles (the same per-element accumulation), and the SiLU*mul epilogue equal to
+    silu_mul of the plain output."""
+    mb = _mb()
+    x, w, cnt, a = _problem(E, counts, N, K, a_max, seed=7 * N + K)
+    cd = torch.from_numpy(cnt).cuda()
+    y = sentinel_like((x.shape[0], N), torch.bfloat16)
+    if fp8:
+        xq, xs = mb.moe_quantize_rows(x.float().cuda())
+        wq, ws = mb.moe_quantize_rows(w.float().cuda())
+        gemm = lambda **kw: mb.moe_grouped_gemm_fp8_rowwise(xq, wq, cd, xs, ws, **kw)
+    else:
+        gemm = lambda **kw: mb.moe_grouped_gemm(x.cuda(), w.cuda(), cd, **kw)
+    gemm(epilogue=mb.MOE_GEMM_CTA_PAIRS, out=y)
+    assert mb.device_error() == 0
+    assert is_sentinel(y[a:])
+    y1 = gemm()   # single-CTA tiles
+    if fp8:
+        ref = oracle.grouped_gemm_fp8(bits(xq.cpu())[:a], bits(wq.cpu()), cnt, xs.cpu().numpy()[:a],
+                                      ws.cpu().numpy())
+        dx = oracle.e4m3_decode(bits(xq.cpu())[:a]).astype(np.float64)
+        dw = oracle.e4m3_decode(bits(wq.cpu())).astype(np.float64)
+        bound = np.zeros((a, N))
+        off = 0
+        for e, c in enumerate(cnt):
+            bound[off:off + c] = ((np.abs(dx[off:off + c]) @ np.abs(dw[e]).T) * xs.cpu().numpy()[off:off + c, None]
+                                  * ws.cpu().numpy()[e][None, :])
+            off += c
+        _check_close(bits(y[:a]), ref, 2.0 ** -20 * bound)
+    else:
+        ref = oracle.grouped_gemm_bf16(bits(x[:a]), bits(w), cnt)
+        _check_close(bits(y[:a]), ref, _abs_bound_bf16(bits(x[:a]), bits(w), cnt))
+    assert torch.equal(y[:a], y1[:a])
+    if N % 32 == 0:
+        z = sentinel_like((x.shape[0], N // 2), torch.bfloat16)
+        gemm(epilogue=mb.MOE_EPILOGUE_SILU_MUL | mb.MOE_GEMM_CTA_PAIRS, out=z)
+        assert mb.device_error() == 0
+        assert torch.equal(z[:a], mb.moe_silu_mul(y[:a].contiguous(), N // 2))
+        assert is_sentinel(z[a:])
