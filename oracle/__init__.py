@@ -14,6 +14,10 @@ _combine_outputs:
           -> grouped GEMM with w13 -> silu_mul (or silu_mul_quant)
           -> grouped GEMM with w2  -> scatter-add into the output.
 
+The whole layer of _no_comm_forward adds the router scores
+sigmoid(tokens @ router_DE) in front and the shared expert, whose output the
+routed rows are added into.
+
 bf16 values travel as ``numpy.uint16`` bit patterns, e4m3 as ``numpy.uint8``.
 """
 from __future__ import annotations
@@ -74,6 +78,7 @@ def _load():
             "oracle_silu_mul": ([P, P, L, I, I, P], None),
             "oracle_silu_mul_quant": ([P, P, L, I, I, P, P, P], None),
             "oracle_scatter_add": ([P, I, I, P, P, I], None),
+            "oracle_router_scores": ([P, P, I, I, I, I, P, P], None),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -248,6 +253,26 @@ def scatter_add(out, rows, token_indices, valid_rows: int | None = None):
     return out
 
 
+# ------------------------------------------------------------ router scores
+
+def router_scores(x, w_router, valid_tokens: int | None = None, logits: bool = False):
+    """x[T, D] bf16 bits, w_router[E, D] bf16 bits (router_DE transposed).
+
+    Returns scores[T, E] bf16 bits (rows >= valid_tokens are zero), and the
+    bf16 logits as well when ``logits``.
+    """
+    x = _c(x, np.uint16)
+    w = _c(w_router, np.uint16)
+    T, D = x.shape
+    E = w.shape[0]
+    assert w.shape[1] == D
+    v = T if valid_tokens is None else int(valid_tokens)
+    sc = np.zeros((T, E), np.uint16)
+    lg = np.zeros((T, E), np.uint16) if logits else None
+    _load().oracle_router_scores(_p(x), _p(w), T, D, E, v, _p(sc), _p(lg))
+    return (sc, lg) if logits else sc
+
+
 # ------------------------------------------------------------------- forward
 
 def moe_forward(x, scores, top_k: int, weights, *, fp8: bool, valid_tokens: int | None = None,
@@ -310,4 +335,64 @@ def moe_forward_tokens(tokens, x, scores, top_k: int, weights, *, fp8: bool, out
     ss = np.ascontiguousarray(scores[tokens])
     oi = None if out_init is None else np.ascontiguousarray(out_init[tokens])
     res = moe_forward(xs, ss, top_k, weights, fp8=fp8, out_init=oi, scale_ub=scale_ub)
+    return res["out"], res
+
+
+# ------------------------------------------------------------ shared expert
+
+def shared_expert(x, w13, w2, *, fp8: bool, scale_ub: float | None = None, valid_tokens: int | None = None):
+    """The shared expert of MetaShufflingMoE._shared_expert_part1 / _part2 on
+    the valid token rows: y = x @ w13.T, z = silu_mul(y0, y1), out = z @ w2.T.
+
+    w13[2H, D], w2[D, H]: bf16 bits, or fp32 when ``fp8``.  On the FP8-rowwise
+    path the weights are quantised per row here, x per row with the gathers'
+    row rule at unit score (bound ``scale_ub``), and z by silu_mul_quant.
+    Returns out[T, D] bf16 bits; rows >= valid_tokens stay zero.
+    """
+    T, D = x.shape
+    v = T if valid_tokens is None else int(valid_tokens)
+    out = np.zeros((T, D), np.uint16)
+    if v == 0:
+        return out
+    counts = np.array([v], np.int32)
+    H = w2.shape[-1]
+    if not fp8:
+        y = grouped_gemm_bf16(x[:v], np.asarray(w13)[None], counts)
+        z = silu_mul(y, H)
+        out[:v] = grouped_gemm_bf16(z, np.asarray(w2)[None], counts)
+    else:
+        w13q, w13s = quantize_rows(w13)
+        w2q, w2s = quantize_rows(w2)
+        xq, xs = quantize_rows(bf16_to_f32(x[:v]), scale_ub)
+        y = grouped_gemm_fp8(xq, w13q[None], counts, xs, w13s)
+        zq, zs = silu_mul_quant(y, H, scale_ub)
+        out[:v] = grouped_gemm_fp8(zq, w2q[None], counts, zs, w2s)
+    return out
+
+
+def moe_layer_forward(x, w_router, top_k: int, weights, *, fp8: bool, shared=None,
+                      valid_tokens: int | None = None, scale_ub: float | None = None):
+    """The whole MoE layer of MetaShufflingMoE._no_comm_forward on one GPU:
+    router scores, the shared expert (``shared`` = (w13, w2), or None for a
+    layer without one), and the routed experts added into its output.
+    Returns the routed forward's dict plus ``scores`` and ``shared_out``.
+    """
+    scores = router_scores(x, w_router, valid_tokens)
+    base = None
+    if shared is not None:
+        base = shared_expert(x, shared[0], shared[1], fp8=fp8, scale_ub=scale_ub, valid_tokens=valid_tokens)
+    res = moe_forward(x, scores, top_k, weights, fp8=fp8, valid_tokens=valid_tokens, out_init=base,
+                      scale_ub=scale_ub)
+    res["scores"] = scores
+    res["shared_out"] = base
+    return res
+
+
+def moe_layer_forward_tokens(tokens, x, w_router, top_k: int, weights, *, fp8: bool, shared=None,
+                             scale_ub: float | None = None):
+    """moe_layer_forward's output rows for a sample of valid tokens: every stage,
+    the router and the shared expert included, works token by token."""
+    tokens = np.asarray(tokens, np.int64)
+    res = moe_layer_forward(np.ascontiguousarray(x[tokens]), w_router, top_k, weights, fp8=fp8, shared=shared,
+                            scale_ub=scale_ub)
     return res["out"], res

@@ -11,7 +11,9 @@
  *     gather + FP8-rowwise quantise and scatter-add kernels;
  *   - "mslk/moe/layers.py" (same wheel): RoutedExperts.build (weight layout),
  *     BaselineMoE._forward / _fake_quant (the dense definition of the forward),
- *     MetaShufflingMoE._route / _routed_expert / _combine_outputs (stage order).
+ *     MetaShufflingMoE._route / _routed_expert / _combine_outputs (stage order),
+ *     the router scores of _route and the shared expert of
+ *     _shared_expert_part1 / _shared_expert_part2.
  *
  * Precision: fp32 where the pages fix it (the gather and quantise kernels
  * upcast to fp32 and do their arithmetic there); fp64 for the GEMM dot
@@ -344,6 +346,36 @@ void oracle_grouped_gemm_fp8(const uint8_t* x, const uint8_t* w, const int32_t* 
             }
         }
         off += cnt;
+    }
+}
+
+/* ---------------------------------------------------------- router scores */
+
+/*
+ * Router scores of MetaShufflingMoE._route (the same two steps open
+ * BaselineMoE._forward): scores = sigmoid(linear(tokens, router_DE.T)), both
+ * in the model dtype, bf16.  The weight comes transposed, w[e, d] =
+ * router_DE[d, e].  For each token t < valid_tokens and expert e:
+ *   logit = bf16( sum_d x[t, d] * w[e, d] )      fp64 over ascending d
+ *   score = bf16( 1 / (1 + e^-logit) )           fp64, from the bf16 logit
+ * Rows t >= valid_tokens are not written.  `logits` may be NULL.
+ */
+void oracle_router_scores(const uint16_t* x, const uint16_t* w, int T, int D, int E, int valid_tokens,
+                          uint16_t* scores, uint16_t* logits) {
+    (void)T;
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < valid_tokens; ++t) {
+        for (int e = 0; e < E; ++e) {
+            const uint16_t* xr = x + (int64_t)t * D;
+            const uint16_t* wr = w + (int64_t)e * D;
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d)
+                acc += (double)bf16_to_f32(xr[d]) * (double)bf16_to_f32(wr[d]);
+            const uint16_t l = f32_to_bf16((float)acc);
+            const double lv = (double)bf16_to_f32(l);
+            scores[(int64_t)t * E + e] = f32_to_bf16((float)(1.0 / (1.0 + exp(-lv))));
+            if (logits) logits[(int64_t)t * E + e] = l;
+        }
     }
 }
 
