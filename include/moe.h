@@ -5,6 +5,7 @@
  * entry points are the stages of the single-GPU forward of
  * mslk/moe/layers.py, MetaShufflingMoE._no_comm_forward:
  *
+ *   moe_router_scores         router scores sigmoid(tokens @ router_DE), bf16
  *   moe_route                 top-k routing into per-expert counts and a
  *                             by-expert token permutation (index_shuffling)
  *   moe_gather_scale          gather token rows and multiply by the score
@@ -83,6 +84,41 @@ int moe_last_cuda_error(void);
  * Synchronises `stream`.  *bits receives an OR of MOE_DEVERR_* (0 = none).
  */
 int moe_device_error(unsigned int* bits, cudaStream_t stream);
+
+/* ------------------------------------------------------------ router scores */
+
+/*
+ * Bytes of device workspace moe_router_scores needs (host call, no GPU use).
+ */
+int moe_router_workspace_size(int T, int D, int E, size_t* bytes);
+
+/*
+ * Router scores of mslk/moe/layers.py, MetaShufflingMoE._route (the same two
+ * steps open BaselineMoE._forward): scores = sigmoid(linear(tokens,
+ * router_DE.T)), both steps in bf16.  For every token t < Tv and expert e:
+ *   logit        = bf16( sum_d x[t, d] * w_router[e, d] )   fp32 accumulation
+ *   scores[t, e] = bf16( 1 / (1 + exp(-logit)) )            fp32
+ *
+ * x                bf16 [T, D], row-major, 16-byte aligned.
+ * w_router         bf16 [E, D], row-major, 16-byte aligned: router_DE [D, E]
+ *                  transposed (the caller keeps this copy resident).
+ * num_valid_tokens device int32 scalar Tv, or NULL for T.  A value outside
+ *                  [0, T] is clamped and flagged (MOE_DEVERR_BAD_COUNT).
+ * scores           bf16 [T, E], row-major (row stride E).  Rows t >= Tv are
+ *                  not written.  Pass it to moe_route with stride_t = E,
+ *                  stride_e = 1.
+ * ws, ws_bytes     device workspace of at least moe_router_workspace_size
+ *                  bytes, 256-byte aligned, owned by the caller; contents need
+ *                  not survive between calls.  Too small: MOE_ERR_WORKSPACE.
+ *
+ * Supports 1 <= E <= 256 and D a positive multiple of 16
+ * (MOE_ERR_UNSUPPORTED otherwise).  T = 0 is a no-op.  The sum over d may be
+ * split across CTAs; the partial sums are always added in the same order, so
+ * identical inputs on the same device give identical bytes.
+ */
+int moe_router_scores(const void* x, int T, int D, const void* w_router, int E,
+                      const int32_t* num_valid_tokens, void* scores, void* ws, size_t ws_bytes,
+                      cudaStream_t stream);
 
 /* ------------------------------------------------------------------ routing */
 

@@ -45,6 +45,8 @@ def _load() -> ctypes.CDLL:
         "moe_status_string": ([I], ctypes.c_char_p),
         "moe_last_cuda_error": ([], I),
         "moe_device_error": ([U, P], I),
+        "moe_router_workspace_size": ([I, I, I, ctypes.POINTER(S)], I),
+        "moe_router_scores": ([P, I, I, P, I, P, P, P, S, P], I),
         "moe_route_workspace_size": ([I, I, I, ctypes.POINTER(S)], I),
         "moe_route": ([P, I, L, L, I, I, I, P, P, P, P, P, P, P, S, P], I),
         "moe_route_no_alloc": ([P, I, L, L, I, I, I, P, P, P, P, P, P, P], I),
@@ -115,6 +117,32 @@ def device_error(stream=None) -> int:
 
 
 # ------------------------------------------------------------------ routing
+
+def moe_router_workspace_size(T: int, D: int, E: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check("moe_router_workspace_size", _lib.moe_router_workspace_size(T, D, E, ctypes.byref(n)))
+    return n.value
+
+
+def moe_router_scores(x: torch.Tensor, w_router: torch.Tensor, num_valid_tokens: torch.Tensor | None = None, *,
+                      out: torch.Tensor | None = None, workspace: torch.Tensor | None = None, stream=None):
+    """scores[T, E] = bf16(sigmoid(bf16(x @ w_router.T))) for x[T, D] and w_router[E, D] (bf16)."""
+    T, D = x.shape
+    E = w_router.shape[0]
+    _need(x, torch.bfloat16, "x")
+    _need(w_router, torch.bfloat16, "w_router")
+    if num_valid_tokens is not None:
+        _need(num_valid_tokens, torch.int32, "num_valid_tokens")
+    if out is None:
+        out = torch.empty(T, E, dtype=torch.bfloat16, device=x.device)
+    ws_bytes = moe_router_workspace_size(T, D, E)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=x.device)
+    st = _lib.moe_router_scores(_ptr(x), T, D, _ptr(w_router), E, _ptr(num_valid_tokens), _ptr(out),
+                                _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("moe_router_scores", st)
+    return out
+
 
 def moe_route_workspace_size(T: int, E: int, top_k: int) -> int:
     n = ctypes.c_size_t(0)

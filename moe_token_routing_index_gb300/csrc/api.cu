@@ -146,6 +146,29 @@ int moe_route(const void* scores, int scores_dtype, int64_t stride_t, int64_t st
   return finish(moe::launch_route(a, stream));
 }
 
+int moe_router_workspace_size(int T, int D, int E, size_t* bytes) {
+  if (!bytes || T < 0 || D < 1 || E < 1) return MOE_ERR_INVALID;
+  if (E > 256 || D % 16 != 0) return MOE_ERR_UNSUPPORTED;
+  *bytes = moe::router_workspace_bytes(T, D, E);
+  return MOE_OK;
+}
+
+int moe_router_scores(const void* x, int T, int D, const void* w_router, int E, const int32_t* num_valid_tokens,
+                      void* scores, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  size_t need;
+  int rc = moe_router_workspace_size(T, D, E, &need);
+  if (rc != MOE_OK) return rc;
+  if (T == 0) return MOE_OK;
+  if (!x || !w_router || !scores || !ws) return MOE_ERR_INVALID;
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(w_router) || (reinterpret_cast<uintptr_t>(scores) & 1u)) return MOE_ERR_UNSUPPORTED;
+  moe::RouterArgs a{x, T, D, w_router, E, num_valid_tokens, scores, ws, nullptr};
+  rc = device_error_word(&a.err);
+  if (rc != MOE_OK) return rc;
+  return finish(moe::launch_router_scores(a, stream));
+}
+
 static int check_gather(const void* x, int T, int D, const int32_t* ti, const int32_t* ei, int a,
                         const void* scores, int dtype, int E, const void* out) {
   if (T < 0 || D < 0 || a < 0) return MOE_ERR_INVALID;

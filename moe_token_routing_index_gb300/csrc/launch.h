@@ -26,6 +26,20 @@ struct RouteArgs {
 size_t route_workspace_bytes(int T, int E, int top_k);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 
+struct RouterArgs {
+  const void* x;       // bf16 [T, D]
+  int T, D;
+  const void* w;       // bf16 [E, D]
+  int E;
+  const int32_t* num_valid;
+  void* scores;        // bf16 [T, E]
+  void* ws;
+  unsigned int* err;
+};
+
+size_t router_workspace_bytes(int T, int D, int E);
+cudaError_t launch_router_scores(const RouterArgs& a, cudaStream_t s);
+
 struct GatherArgs {
   const void* x;
   int T, D;

@@ -24,7 +24,7 @@ import numpy as np
 import torch
 
 __all__ = ["MoEConfig", "CONFIGS", "make_tokens", "make_logits", "make_scores",
-           "make_weights", "tensor_seed"]
+           "make_weights", "make_router", "make_shared_weights", "tensor_seed"]
 
 
 @dataclass(frozen=True)
@@ -87,13 +87,15 @@ CONFIGS: dict[str, MoEConfig] = {
                             fp8=True, Tv=11000),
 }
 
-# Stream indices inside the SeedSequence spawn.
-_STREAM_TOKENS, _STREAM_LOGITS, _STREAM_W13, _STREAM_W2, _STREAM_BIAS = range(5)
+# Stream indices inside the SeedSequence spawn (child i does not depend on how many are spawned).
+(_STREAM_TOKENS, _STREAM_LOGITS, _STREAM_W13, _STREAM_W2, _STREAM_BIAS, _STREAM_ROUTER, _STREAM_SHARED13,
+ _STREAM_SHARED2) = range(8)
+_NSTREAMS = 8
 
 
 def tensor_seed(seed: int, stream: int) -> int:
     """A 63-bit seed for one tensor's stream, derived from the workload seed."""
-    child = np.random.SeedSequence(seed).spawn(_STREAM_BIAS + 1)[stream]
+    child = np.random.SeedSequence(seed).spawn(_NSTREAMS)[stream]
     return int(child.generate_state(2, dtype=np.uint64)[0] >> np.uint64(1))
 
 
@@ -114,7 +116,7 @@ def make_logits(cfg: MoEConfig, seed: int = 0) -> torch.Tensor:
     g = _cpu_gen(seed, _STREAM_LOGITS)
     logits = torch.randn(cfg.T, cfg.E, generator=g, dtype=torch.float32)
     if cfg.skew == "zipf":
-        ss = np.random.SeedSequence(seed).spawn(_STREAM_BIAS + 1)[_STREAM_BIAS]
+        ss = np.random.SeedSequence(seed).spawn(_NSTREAMS)[_STREAM_BIAS]
         k = np.random.Generator(np.random.PCG64(ss)).zipf(1.1, cfg.E)
         logits += torch.from_numpy(np.log(k.astype(np.float64))).to(torch.float32)[None, :]
     elif cfg.skew == "zero_experts":
@@ -155,4 +157,27 @@ def make_weights(cfg: MoEConfig, seed: int = 0, device: str | torch.device = "cp
         w13[i] = (torch.randn(2 * cfg.H, cfg.D, generator=g, device=dev) * cfg.weight_std).to(dtype)
         g.manual_seed((base2 + 0x9E3779B97F4A7C15 * (e + 1)) & mask)
         w2[i] = (torch.randn(cfg.D, cfg.H, generator=g, device=dev) * cfg.weight_std).to(dtype)
+    return w13, w2
+
+
+def make_router(cfg: MoEConfig, seed: int = 0, device: str | torch.device = "cpu") -> torch.Tensor:
+    """Router weight, transposed: w_router[E, D] = router_DE[D, E], bf16 with
+    entries N(0, 1/D), so that with N(0, 1) tokens the logits are about N(0, 1)
+    (the logit distribution of the uniform workloads).  Drawn on the CPU."""
+    g = _cpu_gen(seed, _STREAM_ROUTER)
+    w = torch.randn(cfg.E, cfg.D, generator=g, dtype=torch.float32) / float(np.sqrt(cfg.D))
+    return w.to(torch.bfloat16).to(device)
+
+
+def make_shared_weights(cfg: MoEConfig, seed: int = 0,
+                        device: str | torch.device = "cpu") -> tuple[torch.Tensor, torch.Tensor]:
+    """Shared-expert weights (w13[2H, D], w2[D, H]) with entries N(0, weight_std):
+    bf16, or fp32 for FP8 workloads.  Drawn on ``device``."""
+    dev = torch.device(device)
+    dtype = torch.float32 if cfg.fp8 else torch.bfloat16
+    g = torch.Generator(device=dev)
+    g.manual_seed(tensor_seed(seed, _STREAM_SHARED13))
+    w13 = (torch.randn(2 * cfg.H, cfg.D, generator=g, device=dev) * cfg.weight_std).to(dtype)
+    g.manual_seed(tensor_seed(seed, _STREAM_SHARED2))
+    w2 = (torch.randn(cfg.D, cfg.H, generator=g, device=dev) * cfg.weight_std).to(dtype)
     return w13, w2

@@ -79,3 +79,12 @@ def test_host_side_validation_without_gpu(lib):
     assert L.moe_expert_mlp_workspace_size(0, ctypes.byref(n)) == lib.MOE_ERR_INVALID
     assert L.moe_expert_mlp(fake, fake, fake, fake, 4, 64, 32, 32, fake, fake, None, 0, 0, fake, 0, None) \
         == lib.MOE_ERR_WORKSPACE
+    # router scores: shape limits, workspace, empty batch
+    assert L.moe_router_workspace_size(-1, 64, 8, ctypes.byref(n)) == lib.MOE_ERR_INVALID
+    assert L.moe_router_workspace_size(64, 64, 300, ctypes.byref(n)) == lib.MOE_ERR_UNSUPPORTED
+    assert L.moe_router_workspace_size(64, 24, 8, ctypes.byref(n)) == lib.MOE_ERR_UNSUPPORTED
+    assert L.moe_router_workspace_size(0, 64, 8, ctypes.byref(n)) == lib.MOE_OK and n.value == 0
+    assert L.moe_router_workspace_size(8192, 5120, 16, ctypes.byref(n)) == lib.MOE_OK and n.value > 0
+    assert L.moe_router_scores(fake, 8192, 5120, fake, 16, None, fake, fake, 16, None) == lib.MOE_ERR_WORKSPACE
+    assert L.moe_router_scores(None, 0, 64, None, 8, None, None, None, 0, None) == lib.MOE_OK
+    assert L.moe_router_scores(None, 4, 64, fake, 8, None, fake, fake, 1 << 30, None) == lib.MOE_ERR_INVALID
