@@ -121,11 +121,24 @@ def _host_bits(t):
     return t.numpy()
 
 
-def oracle_tokens_per_s(cfg, x, s, w13, w2, seconds: float, max_tokens: int | None = None):
+def _layer_weights_host(cfg, router, shared):
+    """Router bits and shared-expert arrays (bf16 bits, or fp32 for FP8 layers) for the oracle."""
+    if router is None:
+        return None
+    sh = None
+    if shared is not None:
+        conv = (lambda t: t.float().cpu().numpy()) if cfg.fp8 else _host_bits
+        sh = (conv(shared[0]), conv(shared[1]))
+    return _host_bits(router), sh
+
+
+def oracle_tokens_per_s(cfg, x, s, w13, w2, seconds: float, max_tokens: int | None = None, layer=None):
     """Time the oracle's forward (as it stands) on a bounded sample of tokens.
 
     Returns (tokens/s, tokens in the sample, threads, wall seconds).  The
     sample is the first n valid tokens, n grown until about `seconds` of work.
+    layer: (router bits, shared-expert arrays) to time the whole layer
+    (router, shared expert and routed experts) instead of the routed forward.
     """
     import numpy as np
 
@@ -134,6 +147,13 @@ def oracle_tokens_per_s(cfg, x, s, w13, w2, seconds: float, max_tokens: int | No
     xb, sb = _host_bits(x), _host_bits(s)
     Tv = cfg.valid_tokens
     cache = {}
+
+    def forward(toks):
+        if layer is None:
+            oracle.moe_forward_tokens(toks, xb, sb, cfg.top_k, weights, fp8=cfg.fp8, scale_ub=cfg.scale_ub)
+        else:
+            oracle.moe_layer_forward_tokens(toks, xb, layer[0], cfg.top_k, weights, fp8=cfg.fp8, shared=layer[1],
+                                            scale_ub=cfg.scale_ub)
 
     def weights(ids):
         missing = [e for e in ids if e not in cache]
@@ -152,7 +172,7 @@ def oracle_tokens_per_s(cfg, x, s, w13, w2, seconds: float, max_tokens: int | No
         toks = np.arange(n)
         weights(sorted(set(oracle.route(sb[toks], cfg.top_k)["expert_indices"].tolist())))  # warm the copy
         t0 = time.perf_counter()
-        oracle.moe_forward_tokens(toks, xb, sb, cfg.top_k, weights, fp8=cfg.fp8, scale_ub=cfg.scale_ub)
+        forward(toks)
         dt = time.perf_counter() - t0
         if dt >= 0.3 * seconds or n >= limit:
             break
@@ -160,7 +180,7 @@ def oracle_tokens_per_s(cfg, x, s, w13, w2, seconds: float, max_tokens: int | No
     done, total = n, dt
     while total < 0.8 * seconds:          # a small workload is repeated until the sample is long enough
         t0 = time.perf_counter()
-        oracle.moe_forward_tokens(toks, xb, sb, cfg.top_k, weights, fp8=cfg.fp8, scale_ub=cfg.scale_ub)
+        forward(toks)
         total += time.perf_counter() - t0
         done += n
     return done / total, n, oracle.num_threads(), total
@@ -208,7 +228,13 @@ def run_ours(args, cfg):
     s = workloads.make_scores(cfg, seed=rank).to(dev)
     w13, w2 = workloads.make_weights(cfg, seed=0, device=dev)
     pairs = {"auto": None, "on": True, "off": False}[args.cta_pairs]
-    layer = MoELayer.from_weights(cfg, w13, w2, cta_pairs=pairs)
+    full = args.layer == "full"
+    router = shared = None
+    if full:
+        router = workloads.make_router(cfg, device=dev)
+        shared = workloads.make_shared_weights(cfg, device=dev)
+    layer = MoELayer.from_weights(cfg, w13, w2, cta_pairs=pairs, router=router, shared=shared,
+                                  overlap_shared=not args.no_overlap)
     if args.no_cpu_baseline or world > 1 or rank != 0:
         # only the oracle baseline needs the source weights (fp32 for FP8 layers)
         del w13, w2
@@ -216,16 +242,11 @@ def run_ours(args, cfg):
         torch.cuda.empty_cache()
     nv = None if cfg.Tv is None else torch.tensor([cfg.Tv], dtype=torch.int32, device=dev)
     out = torch.zeros(cfg.T, cfg.D, dtype=torch.bfloat16, device=dev)
-    stages = layer.stages(x, s, nv, out, accumulate=False)
-    names = [n for n, _ in stages]
+    stages = layer.stages(x, None if full else s, nv, out, accumulate=False)
+    names = [n for n, _, _ in stages]
 
     def step(ev=None):
-        for i, (_, launch) in enumerate(stages):
-            if ev is not None:
-                ev[i][0].record()
-            launch()
-            if ev is not None:
-                ev[i][1].record()
+        layer.run(stages, events=ev)
 
     for _ in range(args.warmup):
         step()
@@ -235,7 +256,8 @@ def run_ours(args, cfg):
     counts = layer.buffers(cfg.T, dev).route["counts"].cpu().tolist()
 
     K = args.steps
-    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in stages] for _ in range(K)]
+    ev = [{n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for n in names}
+          for _ in range(K)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
@@ -251,19 +273,20 @@ def run_ours(args, cfg):
     if world > 1:
         dist.barrier()
     ms = t_start.elapsed_time(t_end) / K
-    stage_ms = {n: statistics.fmean(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(K))
-                for i, n in enumerate(names)}
+    stage_ms = {n: statistics.fmean(ev[k][n][0].elapsed_time(ev[k][n][1]) for k in range(K)) for n in names}
     ms = max_over_ranks(ms, dev)
     if mb.device_error() != 0:
         raise RuntimeError("device-side error during the timed steps")
 
-    e2e_ms, h2d, d2h = (None, 0, 0) if args.no_e2e else run_e2e(args, cfg, layer, x, s, nv, out, world)
+    e2e_ms, h2d, d2h = (None, 0, 0) if args.no_e2e else run_e2e(args, cfg, layer, x, None if full else s, nv,
+                                                                 out, world)
 
     result = None
     if rank == 0:
-        result = report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, layer)
+        result = report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, layer, names)
         if not args.no_cpu_baseline and world == 1:
-            tps, n, cores, dt = oracle_tokens_per_s(cfg, x, s, w13, w2, args.cpu_seconds)
+            tps, n, cores, dt = oracle_tokens_per_s(cfg, x, s, w13, w2, args.cpu_seconds,
+                                                    layer=_layer_weights_host(cfg, router, shared))
             result["cpu_baseline"] = {"value": round(tps, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
                                       "sample": f"first {n} valid tokens of the workload (repeated to {dt:.1f} s of wall time)"}
         print(json.dumps(result), flush=True)
@@ -281,16 +304,17 @@ def run_e2e(args, cfg, layer, x, s, nv, out, world):
 
     K = args.steps
     xh = x.cpu().pin_memory()
-    sh = s.cpu().pin_memory()
+    sh = None if s is None else s.cpu().pin_memory()     # the whole layer computes its own scores
     nvh = None if nv is None else nv.cpu().pin_memory()
     outh = torch.empty(cfg.T, cfg.D, dtype=torch.bfloat16).pin_memory()
-    xd, sd = torch.empty_like(x), torch.empty_like(s)
+    xd, sd = torch.empty_like(x), None if s is None else torch.empty_like(s)
     nvd = None if nv is None else torch.empty_like(nv)
     outd = torch.zeros_like(out)
 
     def e2e_step():
         xd.copy_(xh, non_blocking=True)
-        sd.copy_(sh, non_blocking=True)
+        if sd is not None:
+            sd.copy_(sh, non_blocking=True)
         if nvd is not None:
             nvd.copy_(nvh, non_blocking=True)
         layer(xd, sd, nvd, out=outd)
@@ -309,12 +333,13 @@ def run_e2e(args, cfg, layer, x, s, nv, out, world):
     torch.cuda.synchronize()
     e2e_ms = e_start.elapsed_time(e_end) / K
     e2e_ms = max_over_ranks(e2e_ms, x.device)
-    h2d = xh.numel() * xh.element_size() + sh.numel() * sh.element_size() + (0 if nvh is None else 4)
+    h2d = xh.numel() * xh.element_size() + (0 if sh is None else sh.numel() * sh.element_size()) + \
+        (0 if nvh is None else 4)
     d2h = outh.numel() * outh.element_size()
     return e2e_ms, h2d, d2h
 
 
-def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, layer):
+def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, layer, names):
     peaks, peak_kind = load_peaks()
     E, D, H, k = cfg.E, cfg.D, cfg.H, cfg.top_k
     a = cfg.routed_rows
@@ -337,6 +362,22 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
     }
     if cfg.fp8:
         work["silu_quant"] = ("hbm", a * 2 * H * 2 + a * H + a * 4)
+    full = args.layer == "full"
+    if full:
+        Tv = cfg.valid_tokens
+        Hs = layer.Hs
+        work["router"] = ("hbm", Tv * D * 2 + E * D * 2 + Tv * E * 2)
+        work["shared_mlp"] = ("gemm", 3 * Hs * D * 2 + Tv * D * 2 + Tv * Hs * 2 * 2 + Tv * D * 2,
+                              2.0 * Tv * 3 * Hs * D)
+        work["shared_w13_silu"] = ("gemm", 2 * Hs * D * 2 + Tv * D * 2 + Tv * Hs * 2, 2.0 * Tv * 2 * Hs * D)
+        work["shared_quant"] = ("hbm", Tv * D * 2 + Tv * D + Tv * 16)
+        work["shared_w13"] = ("gemm", 2 * Hs * D + Tv * D + Tv * 2 * Hs * 2, 2.0 * Tv * 2 * Hs * D)
+        work["shared_silu_quant"] = ("hbm", Tv * 2 * Hs * 2 + Tv * Hs + Tv * 4)
+        work["shared_w2"] = ("gemm", D * Hs * wb + Tv * Hs * wb + Tv * D * 2, 2.0 * Tv * D * Hs)
+        # the routed combine adds into the shared expert's output: one more read of it
+        comb = layer.combine_stage(names)
+        kind, *w = work[comb]
+        work[comb] = (kind, w[0] + Tv * D * 2, *w[1:])
     peak_t = peaks["bf16_tflops_sustained"] * (FP8_OVER_BF16 if cfg.fp8 else 1.0)
     gemm_stages = [n for n in stage_ms if work[n][0] == "gemm"]
     stages = {}
@@ -372,8 +413,12 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3" if cfg.fp8 else "bf16",
-        "data": "synthetic, seeded: x~N(0,1), scores=bf16(sigmoid(N(0,1) logits)), expert weights N(0,0.02) random init",
-        "config": {"workload": workload_desc(cfg), "T": cfg.T, "valid_tokens": cfg.valid_tokens, "D": D, "H": H,
+        "data": ("synthetic, seeded: x~N(0,1), router N(0,1/D) (logits ~N(0,1)), routed and shared expert "
+                 "weights N(0,0.02) random init") if full else
+                "synthetic, seeded: x~N(0,1), scores=bf16(sigmoid(N(0,1) logits)), expert weights N(0,0.02) random init",
+        "config": {"workload": workload_desc(cfg) + (" + router + shared expert" if full else ""),
+                   "layer": "router + shared expert + routed experts" if full else "routed experts",
+                   "T": cfg.T, "valid_tokens": cfg.valid_tokens, "D": D, "H": H,
                    "E": E, "top_k": k, "routed_rows": a, "active_experts": active,
                    "l2": "inputs larger than L2: each step streams the active experts' weights "
                          f"({(active * 3 * H * D * wb) / 1e9:.2f} GB) from HBM",
@@ -386,7 +431,7 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
             "value": round(job_tokens_per_s(cfg.valid_tokens, world, e2e_ms), 1), "unit": UNIT,
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": layer.kernel_launches(cfg.T) * args.steps,
+        "gpu_launches": layer.kernel_launches(cfg.T, with_router=full) * args.steps,
         "clocks": clocks,
     }
     return res
@@ -434,10 +479,15 @@ def run_reference(args, cfg):
 
     x = workloads.make_tokens(cfg)
     s = workloads.make_scores(cfg)
-    w13, w2 = workloads.make_weights(cfg, device="cuda" if torch.cuda.is_available() else "cpu")
+    wdev = "cuda" if torch.cuda.is_available() else "cpu"   # the device the GPU arm draws its weights on
+    w13, w2 = workloads.make_weights(cfg, device=wdev)
+    layer = None
+    if args.layer == "full":
+        layer = _layer_weights_host(cfg, workloads.make_router(cfg), workloads.make_shared_weights(cfg, device=wdev))
     budget = 150.0                                  # seconds for the whole --steps/--warmup run
     # calibrate the per-token cost, then size each step's sample to the budget
-    tps, n, cores, dt = oracle_tokens_per_s(cfg, x, s, w13, w2, min(3.0, budget / (args.steps + args.warmup)))
+    tps, n, cores, dt = oracle_tokens_per_s(cfg, x, s, w13, w2, min(3.0, budget / (args.steps + args.warmup)),
+                                            layer=layer)
     per_tok = dt / n
     n_step = int(max(1, min(cfg.valid_tokens, budget / (args.steps + args.warmup) / per_tok)))
     xb, sb = _host_bits(x), _host_bits(s)
@@ -457,9 +507,13 @@ def run_reference(args, cfg):
     Tv = cfg.valid_tokens
 
     def step(i):
-        toks = (np.arange(n_step) + i * n_step) % Tv
-        oracle.moe_forward_tokens(np.unique(toks), xb, sb, cfg.top_k, weights, fp8=cfg.fp8, scale_ub=cfg.scale_ub)
-        return len(np.unique(toks))
+        toks = np.unique((np.arange(n_step) + i * n_step) % Tv)
+        if layer is None:
+            oracle.moe_forward_tokens(toks, xb, sb, cfg.top_k, weights, fp8=cfg.fp8, scale_ub=cfg.scale_ub)
+        else:
+            oracle.moe_layer_forward_tokens(toks, xb, layer[0], cfg.top_k, weights, fp8=cfg.fp8, shared=layer[1],
+                                            scale_ub=cfg.scale_ub)
+        return len(toks)
 
     for i in range(args.warmup):
         step(i)
@@ -472,7 +526,8 @@ def run_reference(args, cfg):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 accumulate",
         "data": "synthetic, seeded (same workload generator as the GPU arm)",
-        "config": {"workload": workload_desc(cfg), "sample_tokens_per_step": n_step},
+        "config": {"workload": workload_desc(cfg) + (" + router + shared expert" if layer else ""),
+                   "sample_tokens_per_step": n_step},
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
                          "sample": f"{n_step} valid tokens per step (of {Tv}), tokens cycling through the workload"},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -491,6 +546,11 @@ def main(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU-baseline leg")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work of the oracle baseline sample")
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
+    p.add_argument("--layer", choices=["routed", "full"], default="routed",
+                   help="routed: the routed-expert path from router scores; full: router scores, shared "
+                        "expert and routed experts (the whole MoE layer)")
+    p.add_argument("--no-overlap", action="store_true",
+                   help="full layer: run the shared expert on the main stream instead of a second one")
     p.add_argument("--cta-pairs", choices=["auto", "on", "off"], default="auto",
                    help="256-row GEMM tiles on CTA pairs (default: when the batch has >= 256 rows per expert)")
     args = p.parse_args(argv)

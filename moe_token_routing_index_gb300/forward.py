@@ -1,16 +1,23 @@
-"""The single-GPU routed-expert forward, composed from the C-ABI stages.
+"""The single-GPU MoE layer forward, composed from the C-ABI stages.
 
-Stage order of mslk/moe/layers.py, MetaShufflingMoE._no_comm_forward
-(routed experts, no shared expert):
+Stage order of mslk/moe/layers.py, MetaShufflingMoE._no_comm_forward:
 
-  bf16:  route -> gather*score -> grouped GEMM w13 with the SiLU*mul epilogue
-         -> grouped GEMM w2 -> scatter-add (both GEMMs in one persistent launch,
-         moe_expert_mlp, when the layer streams its weights: T*top_k <= 128*E)
-  FP8:   route -> gather*score -> e4m3 rows -> grouped GEMM w13 (FP8 rowwise)
-         -> silu_mul_quant -> grouped GEMM w2 (FP8 rowwise) -> scatter-add
+  router (optional): scores = sigmoid(tokens @ router_DE)        moe_router_scores
+  routed experts, bf16:  route -> gather*score -> grouped GEMM w13 with the
+         SiLU*mul epilogue -> grouped GEMM w2 -> scatter-add (both GEMMs in one
+         persistent launch, moe_expert_mlp, when the layer streams its weights:
+         T*top_k <= 128*E)
+  routed experts, FP8:   route -> gather*score -> e4m3 rows -> grouped GEMM w13
+         (FP8 rowwise) -> silu_mul_quant -> grouped GEMM w2 (FP8 rowwise) -> scatter-add
+  shared expert (optional): the same MLP over every valid token (one expert,
+         unit scores) written into the output first; the routed combine then
+         adds into it, as _routed_expert does with shared_output.
 
 With top_k = 1 the scatter-add is fused into the w2 GEMM's epilogue (each
 routed row owns its token), as _routed_expert does with _scatter_add_indices.
+The shared expert runs on a second stream while the router, routing and
+gather run (overlap_router_and_shared_expert of _no_comm_forward); the
+combine waits for it.
 
 Weights stay resident on the device; every buffer of the pipeline is
 allocated once per token-buffer size, so a forward launches kernels only
@@ -19,7 +26,7 @@ allocated once per token-buffer size, so a forward launches kernels only
 """
 from __future__ import annotations
 
-from dataclasses import dataclass
+from dataclasses import dataclass, field
 
 import torch
 
@@ -27,6 +34,8 @@ from . import binding as mb
 from .workloads import MoEConfig
 
 __all__ = ["MoELayer"]
+
+MAIN, SIDE = "main", "side"
 
 
 @dataclass
@@ -41,18 +50,26 @@ class _Buffers:
     z: torch.Tensor               # bf16 [T*k, H] or e4m3 [T*k, H]
     zs: torch.Tensor | None       # FP8: row scales [T*k]
     o: torch.Tensor               # GEMM2 output bf16 [T*k, D]
+    extra: dict = field(default_factory=dict)   # router and shared-expert buffers
 
 
 class MoELayer:
-    """Routed experts of one MoE layer on one GPU.
+    """One MoE layer on one GPU: routed experts, and optionally the router and
+    a shared expert.
 
     w13 [E, 2H, D] and w2 [E, D, H]: bf16 (bf16 layer), or e4m3 with fp32
     per-row scales w13_scale [E, 2H], w2_scale [E, D] (FP8-rowwise layer).
+    router: bf16 [E, D], router_DE transposed (None: the caller passes scores).
+    shared_w13 [2Hs, D], shared_w2 [D, Hs]: the shared expert, in the layer's
+    dtype (e4m3 with scales shared_w13_scale [2Hs], shared_w2_scale [D]).
     """
 
     def __init__(self, top_k: int, w13: torch.Tensor, w2: torch.Tensor, w13_scale: torch.Tensor | None = None,
                  w2_scale: torch.Tensor | None = None, scale_ub: float | None = None,
-                 fused_mlp: bool | None = None, cta_pairs: bool | None = None):
+                 fused_mlp: bool | None = None, cta_pairs: bool | None = None, *,
+                 router: torch.Tensor | None = None, shared_w13: torch.Tensor | None = None,
+                 shared_w2: torch.Tensor | None = None, shared_w13_scale: torch.Tensor | None = None,
+                 shared_w2_scale: torch.Tensor | None = None, overlap_shared: bool = True):
         self.E, n2, self.D = w13.shape
         self.H = n2 // 2
         assert w2.shape == (self.E, self.D, self.H), "w2 must be [E, D, H]"
@@ -73,12 +90,40 @@ class MoELayer:
         # keep 128-row tiles: on GB300 their pair tiles measured slower (prefill,
         # 512 rows per expert) or padded more rows (344 rows per expert).
         self.cta_pairs = cta_pairs
+        self.router = None if router is None else router.contiguous()
+        if self.router is not None:
+            assert self.router.shape == (self.E, self.D) and self.router.dtype == torch.bfloat16
+        self.shared = shared_w13 is not None
+        if self.shared:
+            assert shared_w2 is not None and shared_w13.shape[1] == self.D
+            self.Hs = shared_w13.shape[0] // 2
+            assert shared_w2.shape == (self.D, self.Hs)
+            assert (shared_w13.dtype == torch.float8_e4m3fn) == self.fp8
+            # one expert of the grouped kernels: [1, 2Hs, D] and [1, D, Hs]
+            self.sw13, self.sw2 = shared_w13.contiguous()[None], shared_w2.contiguous()[None]
+            self.sw13_scale = None if shared_w13_scale is None else shared_w13_scale.contiguous()
+            self.sw2_scale = None if shared_w2_scale is None else shared_w2_scale.contiguous()
+            if self.fp8:
+                assert self.sw13_scale is not None and self.sw2_scale is not None
+        self.overlap_shared = overlap_shared
+        self._side: torch.cuda.Stream | None = None
         self._bufs: _Buffers | None = None
 
     @classmethod
-    def from_weights(cls, cfg: MoEConfig, w13: torch.Tensor, w2: torch.Tensor, **kw) -> "MoELayer":
-        """bf16 weights as they are; fp32 weights of an FP8 layer are quantised
-        per row on the device (moe_quantize_rows)."""
+    def from_weights(cls, cfg: MoEConfig, w13: torch.Tensor, w2: torch.Tensor, *,
+                     router: torch.Tensor | None = None, shared: tuple | None = None, **kw) -> "MoELayer":
+        """bf16 weights as they are; fp32 weights of an FP8 layer (routed and
+        shared) are quantised per row on the device (moe_quantize_rows)."""
+        if shared is not None:
+            s13, s2 = shared
+            if cfg.fp8:
+                q13, sc13 = mb.moe_quantize_rows(s13.float().contiguous())
+                q2, sc2 = mb.moe_quantize_rows(s2.float().contiguous())
+                kw.update(shared_w13=q13, shared_w2=q2, shared_w13_scale=sc13, shared_w2_scale=sc2)
+            else:
+                kw.update(shared_w13=s13.to(torch.bfloat16), shared_w2=s2.to(torch.bfloat16))
+        if router is not None:
+            kw["router"] = router.to(torch.bfloat16)
         if cfg.fp8:
             w13q, w13s = mb.moe_quantize_rows(w13.float().contiguous())
             w2q, w2s = mb.moe_quantize_rows(w2.float().contiguous())
@@ -92,28 +137,91 @@ class MoELayer:
         k, E, D, H = self.top_k, self.E, self.D, self.H
         a = T * k
         i32 = dict(dtype=torch.int32, device=device)
+        f32 = dict(dtype=torch.float32, device=device)
+        bf = dict(dtype=torch.bfloat16, device=device)
+        e4 = dict(dtype=torch.float8_e4m3fn, device=device)
         route = dict(counts=torch.zeros(E + 1, **i32), expert_offsets=torch.zeros(E + 1, **i32),
                      expert_indices=torch.zeros(a, **i32), token_indices=torch.zeros(a, **i32),
                      inv_rows=torch.zeros(a, **i32))
         ws = torch.empty(max(mb.moe_route_workspace_size(T, E, k), 256), dtype=torch.uint8, device=device)
-        mlp_ws = torch.empty(mb.moe_expert_mlp_workspace_size(E), dtype=torch.uint8, device=device)
+        mlp_ws = torch.empty(mb.moe_expert_mlp_workspace_size(max(E, 1)), dtype=torch.uint8, device=device)
         if self.fp8:
-            e4 = dict(dtype=torch.float8_e4m3fn, device=device)
-            f32 = dict(dtype=torch.float32, device=device)
             b = _Buffers(T, route, ws, mlp_ws, torch.empty(a, D, **e4), torch.empty(a, **f32),
-                         torch.empty(a, 2 * H, dtype=torch.bfloat16, device=device), torch.empty(a, H, **e4),
-                         torch.empty(a, **f32), torch.empty(a, D, dtype=torch.bfloat16, device=device))
+                         torch.empty(a, 2 * H, **bf), torch.empty(a, H, **e4), torch.empty(a, **f32),
+                         torch.empty(a, D, **bf))
         else:
-            bf = dict(dtype=torch.bfloat16, device=device)
             b = _Buffers(T, route, ws, mlp_ws, torch.empty(a, D, **bf), None, None, torch.empty(a, H, **bf), None,
                          torch.empty(a, D, **bf))
+        x = b.extra
+        if self.router is not None:
+            x["scores"] = torch.empty(T, E, **bf)
+            x["router_ws"] = torch.empty(max(mb.moe_router_workspace_size(T, D, E), 256), dtype=torch.uint8,
+                                         device=device)
+        if self.shared:
+            Hs = self.Hs
+            x["all_tokens"] = torch.tensor([T], **i32)       # the shared expert's row count without a valid count
+            x["ident"] = torch.arange(T, **i32)
+            x["sh_mlp_ws"] = torch.empty(mb.moe_expert_mlp_workspace_size(1), dtype=torch.uint8, device=device)
+            if self.fp8:
+                x["zero"] = torch.zeros(T, **i32)
+                x["unit"] = torch.ones(T, 1, **f32)           # unit scores: the gather's product is exact
+                x["sh_xq"], x["sh_xs"] = torch.empty(T, D, **e4), torch.empty(T, **f32)
+                x["sh_y"] = torch.empty(T, 2 * Hs, **bf)
+                x["sh_zq"], x["sh_zs"] = torch.empty(T, Hs, **e4), torch.empty(T, **f32)
+            else:
+                x["sh_z"] = torch.empty(T, Hs, **bf)
         self._bufs = b
         return b
 
     # ------------------------------------------------------------ forward
-    def stages(self, x: torch.Tensor, scores: torch.Tensor, num_valid_tokens: torch.Tensor | None,
+    def stages(self, x: torch.Tensor, scores: torch.Tensor | None, num_valid_tokens: torch.Tensor | None,
                out: torch.Tensor, accumulate: bool):
-        """The forward as a list of (stage name, launch callable), in order."""
+        """The forward as a list of (stage name, launch callable, lane), in a valid
+        serial order.  Lane SIDE holds the shared expert, which only reads x and
+        writes out; the first MAIN stage after it that touches out is the combine."""
+        T = x.shape[0]
+        b = self.buffers(T, x.device)
+        ex = b.extra
+        st = []
+        if scores is None:
+            if self.router is None:
+                raise ValueError("scores are required for a layer without a router")
+            scores = ex["scores"]
+            st.append(("router", lambda: mb.moe_router_scores(x, self.router, num_valid_tokens, out=ex["scores"],
+                                                              workspace=ex["router_ws"]), MAIN))
+        if self.shared:
+            st += [(n, f, SIDE) for n, f in self._shared_stages(x, num_valid_tokens, out, accumulate)]
+            accumulate = True       # the routed rows are added into the shared expert's output
+        st += [(n, f, MAIN) for n, f in self._routed_stages(x, scores, num_valid_tokens, out, accumulate)]
+        return st
+
+    def _shared_stages(self, x, num_valid_tokens, out, accumulate):
+        T = x.shape[0]
+        ex = self.buffers(T, x.device).extra
+        rows = num_valid_tokens if num_valid_tokens is not None else ex["all_tokens"]   # counts of one expert
+        # accumulate: the shared rows are added into out (row t to token t)
+        add = dict(scatter_indices=ex["ident"], accumulate=True) if accumulate else {}
+        if not self.fp8:
+            if T <= 128:
+                return [("shared_mlp", lambda: mb.moe_expert_mlp(x, self.sw13, self.sw2, rows, z=ex["sh_z"], out=out,
+                                                                 workspace=ex["sh_mlp_ws"], **add))]
+            return [
+                ("shared_w13_silu", lambda: mb.moe_grouped_gemm(x, self.sw13, rows, epilogue=mb.MOE_EPILOGUE_SILU_MUL,
+                                                                out=ex["sh_z"])),
+                ("shared_w2", lambda: mb.moe_grouped_gemm(ex["sh_z"], self.sw2, rows, out=out, **add)),
+            ]
+        return [
+            ("shared_quant", lambda: mb.moe_gather_scale_quant(x, ex["ident"], ex["zero"], ex["unit"], self.scale_ub,
+                                                               rows, out=ex["sh_xq"], out_scale=ex["sh_xs"])),
+            ("shared_w13", lambda: mb.moe_grouped_gemm_fp8_rowwise(ex["sh_xq"], self.sw13, rows, ex["sh_xs"],
+                                                                   self.sw13_scale, out=ex["sh_y"])),
+            ("shared_silu_quant", lambda: mb.moe_silu_mul_quant(ex["sh_y"], self.Hs, self.scale_ub, rows,
+                                                                out=ex["sh_zq"], out_scale=ex["sh_zs"])),
+            ("shared_w2", lambda: mb.moe_grouped_gemm_fp8_rowwise(ex["sh_zq"], self.sw2, rows, ex["sh_zs"],
+                                                                  self.sw2_scale, out=out, **add)),
+        ]
+
+    def _routed_stages(self, x, scores, num_valid_tokens, out, accumulate):
         T = x.shape[0]
         b = self.buffers(T, x.device)
         r = b.route
@@ -156,15 +264,65 @@ class MoELayer:
             st.append(("scatter", lambda: mb.moe_scatter_add(out, b.o, ti, inv, k, valid, accumulate=accumulate)))
         return st
 
-    def __call__(self, x: torch.Tensor, scores: torch.Tensor, num_valid_tokens: torch.Tensor | None = None,
-                 out: torch.Tensor | None = None, accumulate: bool = False) -> torch.Tensor:
-        """x[T, D] bf16, scores[T, E] (bf16 or f32) on the device; num_valid_tokens:
-        device int32 [1] (None: all T).  Returns out[T, D] bf16: for valid tokens
-        the routed sum (added into out when accumulate), other rows untouched."""
+    @staticmethod
+    def combine_stage(names) -> str:
+        """The first routed stage that writes the layer output."""
+        for n in ("scatter", "expert_mlp", "gemm_w2"):   # top_k > 1: the scatter; else the w2 GEMM's epilogue
+            if n in names:
+                return n
+        raise ValueError("no combine stage")
+
+    def run(self, stages, overlap: bool | None = None, events=None):
+        """Launch the stages; with overlap the SIDE lane runs on a second stream
+        from the start and the combine stage waits for it.  events: optional
+        {name: (start, end)} CUDA events recorded around each MAIN-lane stage
+        (and SIDE-lane stages on their stream)."""
+        overlap = self.overlap_shared if overlap is None else overlap
+        side = [s for s in stages if s[2] == SIDE]
+        if not side or not overlap:
+            for n, f, _ in stages:
+                self._launch(n, f, events)
+            return
+        main = torch.cuda.current_stream()
+        if self._side is None:
+            self._side = torch.cuda.Stream(device=main.device)
+            self._fork, self._join = torch.cuda.Event(), torch.cuda.Event()
+        fork, join = self._fork, self._join
+        fork.record(main)
+        with torch.cuda.stream(self._side):
+            self._side.wait_event(fork)
+            for n, f, _ in side:
+                self._launch(n, f, events)
+            join.record(self._side)
+        comb = self.combine_stage([s[0] for s in stages if s[2] == MAIN])
+        for n, f, lane in stages:
+            if lane != MAIN:
+                continue
+            if n == comb:
+                main.wait_event(join)
+            self._launch(n, f, events)
+
+    @staticmethod
+    def _launch(name, f, events):
+        if events is None:
+            f()
+            return
+        s, e = events[name]
+        s.record()
+        f()
+        e.record()
+
+    def __call__(self, x: torch.Tensor, scores: torch.Tensor | None = None,
+                 num_valid_tokens: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                 accumulate: bool = False) -> torch.Tensor:
+        """x[T, D] bf16 and scores[T, E] (bf16 or f32; None: the layer's router
+        computes them) on the device; num_valid_tokens: device int32 [1] (None:
+        all T).  Returns out[T, D] bf16: for valid tokens the shared expert's
+        output (if any) plus the routed sum, added into out when accumulate;
+        other rows untouched."""
         if out is None:
             out = torch.zeros(x.shape[0], self.D, dtype=torch.bfloat16, device=x.device)
-        for _, launch in self.stages(x, scores, num_valid_tokens, out, accumulate):
-            launch()
+        self.run(self.stages(x, scores, num_valid_tokens, out, accumulate))
         return out
 
     def use_fused_mlp(self, T: int) -> bool:
@@ -179,12 +337,16 @@ class MoELayer:
             return self.cta_pairs
         return not self.fp8 and T * self.top_k >= 256 * self.E
 
-    def kernel_launches(self, T: int | None = None) -> int:
-        """Kernels one forward launches: routing (1 for small batches, else 3),
-        gather, the GEMMs (1 fused, or 2), silu_mul_quant (FP8), scatter."""
+    def kernel_launches(self, T: int | None = None, with_router: bool = False) -> int:
+        """Kernels one forward launches: the router (if used), routing (1 for
+        small batches, else 3), gather, the GEMMs (1 fused, or 2),
+        silu_mul_quant (FP8), scatter, and the shared expert's."""
         T = self._bufs.T if T is None and self._bufs is not None else (T or 0)
         route = 1 if (T <= 1024 and T * self.E <= 16384 and T * self.top_k <= 8192 and self.E <= 256) else 3
         scatter = 0 if self.top_k == 1 else 1
-        if self.fp8:
-            return route + 4 + scatter
-        return route + 1 + (1 if self.use_fused_mlp(T) else 2) + scatter
+        n = (route + 4 + scatter) if self.fp8 else (route + 1 + (1 if self.use_fused_mlp(T) else 2) + scatter)
+        if with_router:
+            n += 1
+        if self.shared:
+            n += 4 if self.fp8 else (1 if T <= 128 else 2)
+        return n
