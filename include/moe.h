@@ -108,13 +108,14 @@ int moe_router_workspace_size(int T, int D, int E, size_t* bytes);
  *                  not written.  Pass it to moe_route with stride_t = E,
  *                  stride_e = 1.
  * ws, ws_bytes     device workspace of at least moe_router_workspace_size
- *                  bytes, 256-byte aligned, owned by the caller; contents need
- *                  not survive between calls.  Too small: MOE_ERR_WORKSPACE.
+ *                  bytes, 256-byte aligned, owned by the caller (NULL when that
+ *                  size is 0, as it is in this build).  Too small:
+ *                  MOE_ERR_WORKSPACE.
  *
  * Supports 1 <= E <= 256 and D a positive multiple of 16
  * (MOE_ERR_UNSUPPORTED otherwise).  T = 0 is a no-op.  The sum over d may be
- * split across CTAs; the partial sums are always added in the same order, so
- * identical inputs on the same device give identical bytes.
+ * split across the CTAs of a cluster; the partial sums are always added in the
+ * same order, so identical inputs on the same device give identical bytes.
  */
 int moe_router_scores(const void* x, int T, int D, const void* w_router, int E,
                       const int32_t* num_valid_tokens, void* scores, void* ws, size_t ws_bytes,

@@ -159,7 +159,7 @@ int moe_router_scores(const void* x, int T, int D, const void* w_router, int E, 
   int rc = moe_router_workspace_size(T, D, E, &need);
   if (rc != MOE_OK) return rc;
   if (T == 0) return MOE_OK;
-  if (!x || !w_router || !scores || !ws) return MOE_ERR_INVALID;
+  if (!x || !w_router || !scores || (need > 0 && !ws)) return MOE_ERR_INVALID;
   if (ws_bytes < need) return MOE_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_INVALID;
   if (!aligned16(x) || !aligned16(w_router) || (reinterpret_cast<uintptr_t>(scores) & 1u)) return MOE_ERR_UNSUPPORTED;

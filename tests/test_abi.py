@@ -84,7 +84,9 @@ def test_host_side_validation_without_gpu(lib):
     assert L.moe_router_workspace_size(64, 64, 300, ctypes.byref(n)) == lib.MOE_ERR_UNSUPPORTED
     assert L.moe_router_workspace_size(64, 24, 8, ctypes.byref(n)) == lib.MOE_ERR_UNSUPPORTED
     assert L.moe_router_workspace_size(0, 64, 8, ctypes.byref(n)) == lib.MOE_OK and n.value == 0
-    assert L.moe_router_workspace_size(8192, 5120, 16, ctypes.byref(n)) == lib.MOE_OK and n.value > 0
-    assert L.moe_router_scores(fake, 8192, 5120, fake, 16, None, fake, fake, 16, None) == lib.MOE_ERR_WORKSPACE
+    assert L.moe_router_workspace_size(8192, 5120, 16, ctypes.byref(n)) == lib.MOE_OK
+    assert L.moe_router_scores(fake, 8192, 5120, fake, 0, None, fake, None, 0, None) == lib.MOE_ERR_INVALID
+    assert L.moe_router_scores(fake, 8192, 5120, ctypes.c_void_p(0x1008), 16, None, fake, None, 0, None) \
+        == lib.MOE_ERR_UNSUPPORTED                                                   # misaligned router weight
     assert L.moe_router_scores(None, 0, 64, None, 8, None, None, None, 0, None) == lib.MOE_OK
     assert L.moe_router_scores(None, 4, 64, fake, 8, None, fake, fake, 1 << 30, None) == lib.MOE_ERR_INVALID
