@@ -441,10 +441,15 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
 # summarised under profiles/, with the hash of the kernel sources they were taken
 # on: when those sources change the figure no longer applies and is reported as null.
 TRAFFIC: dict = {
-    ("decode", "expert_mlp"): (4_037_536_000 + 6_564_096, "grouped_gemm.cu", "dbbc561c7cec"),
-    ("prefill_fp8", "gemm_w13"): (1_385_705_000 + 249_711_616, "grouped_gemm.cu", "dbbc561c7cec"),
+    ("decode", "expert_mlp"): (4_037_200_000 + 6_585_088, "grouped_gemm.cu", "9d7ef97c99ea"),
+    ("prefill_fp8", "gemm_w13"): (1_385_605_000 + 249_712_640, "grouped_gemm.cu", "9d7ef97c99ea"),
     ("padded_fp8", "gather_quant"): (93_180_672 + 118_366_720, "rowwise.cu", "d196775be574"),
 }
+
+
+# the device-code headers each kernel source includes
+KERNEL_HEADERS = {"grouped_gemm.cu": ("common.cuh", "tcgen05.cuh"), "router.cu": ("common.cuh", "tcgen05.cuh"),
+                  "rowwise.cu": ("common.cuh",), "route.cu": ("common.cuh",)}
 
 
 def kernel_source_hash(name: str) -> str:
@@ -452,7 +457,7 @@ def kernel_source_hash(name: str) -> str:
 
     csrc = ROOT / "moe_token_routing_index_gb300" / "csrc"
     h = hashlib.sha1()
-    for f in (name, "common.cuh"):
+    for f in (name, *KERNEL_HEADERS.get(name, ("common.cuh",))):
         h.update((csrc / f).read_bytes())
     return h.hexdigest()[:12]
 
