@@ -338,11 +338,11 @@ class MoELayer:
         return not self.fp8 and T * self.top_k >= 256 * self.E
 
     def kernel_launches(self, T: int | None = None, with_router: bool = False) -> int:
-        """Kernels one forward launches: the router (if used), routing (1 for
-        small batches, else 3), gather, the GEMMs (1 fused, or 2),
+        """Kernels one forward launches: the router (if used), routing (one
+        kernel: single-block or cooperative), gather, the GEMMs (1 fused, or 2),
         silu_mul_quant (FP8), scatter, and the shared expert's."""
         T = self._bufs.T if T is None and self._bufs is not None else (T or 0)
-        route = 1 if (T <= 1024 and T * self.E <= 16384 and T * self.top_k <= 8192 and self.E <= 256) else 3
+        route = 1
         scatter = 0 if self.top_k == 1 else 1
         n = (route + 4 + scatter) if self.fp8 else (route + 1 + (1 if self.use_fused_mlp(T) else 2) + scatter)
         if with_router:
