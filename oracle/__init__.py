@@ -79,6 +79,7 @@ def _load():
             "oracle_silu_mul_quant": ([P, P, L, I, I, P, P, P], None),
             "oracle_scatter_add": ([P, I, I, P, P, I], None),
             "oracle_router_scores": ([P, P, I, I, I, I, P, P], None),
+            "oracle_topk_finalize": ([P, L, I, P, P, I, I, P, P], None),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -336,6 +337,75 @@ def moe_forward_tokens(tokens, x, scores, top_k: int, weights, *, fp8: bool, out
     oi = None if out_init is None else np.ascontiguousarray(out_init[tokens])
     res = moe_forward(xs, ss, top_k, weights, fp8=fp8, out_init=oi, scale_ub=scale_ub)
     return res["out"], res
+
+
+# ----------------------------------------------------------- top-k finalize
+
+def topk_weights(scores, r):
+    """The routing weights in the order of the route's inverse permutation:
+    w[t, j] = f32(scores[t, expert of row inv[t, j]]) (the top-k values)."""
+    sc = np.asarray(scores)
+    if sc.dtype == np.uint16:
+        sc = bf16_to_f32(sc)
+    inv = np.asarray(r["inv"])
+    e = np.asarray(r["expert_indices"])[inv]
+    t = np.arange(inv.shape[0])[:, None]
+    return np.ascontiguousarray(sc[t, e], np.float32)
+
+
+def topk_finalize(rows, weights, idx, shared=None):
+    """rows[n, D] bf16 bits, weights fp32 [M, k], idx int32 [M, k] (-1: absent),
+    shared bf16 bits [M, D] or None -> out[M, D] bf16 bits."""
+    rows = _c(rows, np.uint16)
+    w = _c(weights, np.float32)
+    ix = _c(idx, np.int32)
+    M, k = ix.shape
+    D = rows.shape[1]
+    sh = None if shared is None else _c(shared, np.uint16)
+    out = np.zeros((M, D), np.uint16)
+    _load().oracle_topk_finalize(_p(rows), rows.shape[0], D, _p(w), _p(ix), M, k, _p(sh), _p(out))
+    return out
+
+
+def moe_forward_output_weighted(x, scores, top_k: int, weights, *, fp8: bool, valid_tokens: int | None = None,
+                                shared_out=None, scale_ub: float | None = None):
+    """The routed experts with the routing weights applied to the expert outputs
+    (top-k finalize) instead of their inputs: route -> gather (unit scores) ->
+    grouped GEMM w13 -> silu_mul(_quant) -> grouped GEMM w2 -> topk_finalize with
+    the top-k values in inverse-permutation order, plus ``shared_out`` when given.
+    Returns the dict of the stages; out[t] for t >= valid_tokens is zero."""
+    T, D = x.shape
+    E = scores.shape[1]
+    v = T if valid_tokens is None else int(valid_tokens)
+    r = route(scores, top_k, v)
+    counts = r["counts"][:E]
+    used = [e for e in range(E) if counts[e] > 0]
+    out = np.zeros((T, D), np.uint16)
+    res = dict(route=r, used_experts=used)
+    if not used:
+        if shared_out is not None:
+            out[:v] = topk_finalize(np.zeros((0, D), np.uint16), np.zeros((v, top_k), np.float32),
+                                    np.full((v, top_k), -1, np.int32), shared_out[:v])
+        res["out"] = out
+        return res
+    cu = counts[used]
+    w13, w2 = weights(used)
+    Hd = w2.shape[2]
+    unit = np.full((T, E), 0x3F80, np.uint16)       # bf16 1.0: the gather copies the row
+    if not fp8:
+        xg = gather_scale(x, r["token_indices"], r["expert_indices"], unit)
+        z = silu_mul(grouped_gemm_bf16(xg, w13, cu), Hd)
+        o = grouped_gemm_bf16(z, w2, cu)
+    else:
+        w13q, w13s = quantize_rows(w13)
+        w2q, w2s = quantize_rows(w2)
+        xq, xs = gather_scale_quant(x, r["token_indices"], r["expert_indices"], unit, scale_ub)
+        zq, zs = silu_mul_quant(grouped_gemm_fp8(xq, w13q, cu, xs, w13s), Hd, scale_ub)
+        o = grouped_gemm_fp8(zq, w2q, cu, zs, w2s)
+    wts = topk_weights(scores, r)
+    out[:v] = topk_finalize(o, wts, r["inv"], None if shared_out is None else shared_out[:v])
+    res.update(o=o, topk_weights=wts, out=out)
+    return res
 
 
 # ------------------------------------------------------------ shared expert

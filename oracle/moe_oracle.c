@@ -349,6 +349,40 @@ void oracle_grouped_gemm_fp8(const uint8_t* x, const uint8_t* w, const int32_t* 
     }
 }
 
+/* ------------------------------------------------------------ top-k finalize */
+
+/*
+ * Top-k finalize of an unfinalized MoE output (the single-GPU part of
+ * AllReduceRMSNormWithReduceScatterEarlyExit.finalize on the "kimi_k3 ...
+ * allreduce_rmsnorm_reduce_scatter_early_exit" page): the routing weights are
+ * applied to the unweighted GEMM2 rows.  For every token t < M and column d:
+ *   acc = 0; for slot j = 0 .. k-1: p = idx[t, j]; if p >= 0:
+ *       acc = acc + w[t, j] * rows[p, d]          (fp32 multiply, fp32 add)
+ *   r = bf16(acc), a negative zero written as +0
+ *   out[t, d] = shared ? bf16(f32(r) + f32(shared[t, d])) : r
+ * rows bf16 [n_rows, D]; w fp32 [M, k]; idx int32 [M, k]; shared bf16 [M, D] or NULL.
+ * An index >= n_rows is skipped (the GPU flags it).
+ */
+void oracle_topk_finalize(const uint16_t* rows, int64_t n_rows, int D, const float* w, const int32_t* idx,
+                          int M, int k, const uint16_t* shared, uint16_t* out) {
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < M; ++t) {
+        for (int d = 0; d < D; ++d) {
+            float acc = 0.0f;
+            for (int j = 0; j < k; ++j) {
+                const int32_t p = idx[(int64_t)t * k + j];
+                if (p < 0 || p >= n_rows) continue;
+                const float prod = w[(int64_t)t * k + j] * bf16_to_f32(rows[(int64_t)p * D + d]);
+                acc = acc + prod;
+            }
+            uint16_t r = f32_to_bf16(acc);
+            if (r == 0x8000u) r = 0; /* negative zero -> +0 */
+            if (shared) r = f32_to_bf16(bf16_to_f32(r) + bf16_to_f32(shared[(int64_t)t * D + d]));
+            out[(int64_t)t * D + d] = r;
+        }
+    }
+}
+
 /* ---------------------------------------------------------- router scores */
 
 /*
