@@ -14,6 +14,8 @@
  *   moe_grouped_gemm_fp8_rowwise   the same on e4m3 operands with row scales
  *   moe_silu_mul(_quant)      z = silu(y0) * y1 (and FP8 quantisation)
  *   moe_scatter_add           add routed rows back into token order
+ *   moe_scatter_add_padded    the same for the padded-token layout (counts per expert)
+ *   moe_topk_finalize         routing weights applied to the expert outputs
  *   moe_quantize_rows         per-row FP8 quantisation of a weight matrix
  *
  * Conventions (every entry point):
@@ -151,14 +153,18 @@ int moe_route_workspace_size(int T, int E, int top_k, size_t* bytes);
  *                          Tv * top_k are not written
  *   inv_rows[T * top_k]    (nullable) inv_rows[t * top_k + j] = the j-th
  *                          smallest routed row of token t, for t < Tv
+ * topk_weights  (nullable) device float [T * top_k]: topk_weights[t * top_k + j]
+ *               = the score (as fp32) of the expert of routed row
+ *               inv_rows[t * top_k + j], for t < Tv: the top-k values, in the
+ *               order of inv_rows (what moe_topk_finalize takes).
  * ws, ws_bytes  device workspace of at least moe_route_workspace_size bytes,
  *               256-byte aligned; its contents on entry do not matter.
  * Requires 1 <= top_k <= E <= 1024 and T >= 0.  The result is deterministic.
  */
 int moe_route(const void* scores, int scores_dtype, int64_t stride_t, int64_t stride_e, int T, int E,
               int top_k, const int32_t* num_valid_tokens, int32_t* counts, int32_t* expert_offsets,
-              int32_t* expert_indices, int32_t* token_indices, int32_t* inv_rows, void* ws,
-              size_t ws_bytes, cudaStream_t stream);
+              int32_t* expert_indices, int32_t* token_indices, int32_t* inv_rows,
+              float* topk_weights, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * moe_route without a caller workspace: for callers that cannot allocate
@@ -175,6 +181,7 @@ int moe_route(const void* scores, int scores_dtype, int64_t stride_t, int64_t st
  * process exits.  Nothing is allocated: no cudaMalloc, cudaFree or allocating
  * library routine is called.
  *
+ * - Outputs: as moe_route without topk_weights (use moe_route for those).
  * - Sizes: returns MOE_ERR_WORKSPACE (and launches nothing) when
  *   moe_route_workspace_size(T, E, top_k) exceeds
  *   MOE_ROUTE_NO_ALLOC_SCRATCH_BYTES (1 MiB).  For example T = 16384,
@@ -205,7 +212,9 @@ int moe_route_no_alloc(const void* scores, int scores_dtype, int64_t stride_t, i
  *   out[i, :] = bf16( f32(x[t, :]) * f32(scores[t, e]) ),
  *   t = token_indices[i], e = expert_indices[i].
  * x [T, D] bf16; token_indices, expert_indices [a] int32; scores as in
- * moe_route (E experts); valid_token_count: device int32 count of ROUTED ROWS
+ * moe_route (E experts), or NULL for unit scores (the rows are copied, as the
+ * output-weighted path of moe_topk_finalize wants; this holds for the
+ * quantising variant too); valid_token_count: device int32 count of ROUTED ROWS
  * (NULL: a), e.g. &counts[E] from moe_route.  Rows i >= valid are not written.
  * out [a, D] bf16.  a == 0 or D == 0 is a no-op.
  * inv_rows (nullable) and top_k: moe_route's inverse permutation.  With it
@@ -350,6 +359,48 @@ int moe_silu_mul_quant(const void* x0, const void* x1, int64_t ld, int a, int H,
 int moe_scatter_add(void* out, const void* in, const int32_t* token_indices,
                     const int32_t* inv_rows, int top_k, int a, int T, int D,
                     const int32_t* valid_token_count, int accumulate, cudaStream_t stream);
+
+/*
+ * scatter_add_padded_tokens (mslk/moe/gather_scatter.py,
+ * _mslk_scatter_add_padded_tokens) on one GPU (EP = 1): in [T_K, D] holds each
+ * expert's rows back to back (expert e at rows [sum_{e' < e} counts[e'],
+ * ... + counts[e])) followed by padding; the valid rows are the first
+ * sum(token_counts[0, E)) and each is added into out[token_indices[row], :].
+ * With one rank this is moe_scatter_add with that row count, and it is
+ * computed the same deterministic way (token_counts is read on the device).
+ * token_counts [E] device int32 (negative entries count as 0 and are flagged
+ * MOE_DEVERR_BAD_COUNT); T_K must be a multiple of T (T_K = T * top_k).
+ * Other arguments as moe_scatter_add.
+ */
+int moe_scatter_add_padded(void* out, const void* in, const int32_t* token_counts, int E,
+                           const int32_t* token_indices, const int32_t* inv_rows, int top_k,
+                           int T_K, int T, int D, int accumulate, cudaStream_t stream);
+
+/* ----------------------------------------------------------- top-k finalize */
+
+/*
+ * Top-k finalize of an unfinalized MoE output: the single-GPU part of
+ * AllReduceRMSNormWithReduceScatterEarlyExit.finalize on the "kimi_k3 ...
+ * allreduce_rmsnorm_reduce_scatter_early_exit" page, where the routing
+ * weights act on the expert outputs rather than their inputs.  For every token
+ * t < M (or < *valid_token_count) and column d:
+ *   acc = 0 (fp32); for slot j = 0 .. top_k-1 in order:
+ *     p = expanded_idx_to_permuted_idx[t, j]; skipped when p < 0;
+ *     acc = acc + w[t, j] * rows[p, d]        (fp32 multiply, then fp32 add)
+ *   r = bf16(acc) with a negative zero written as +0
+ *   out[t, d] = r, or bf16(f32(r) + f32(shared_output[t, d])) with a shared output
+ * rows [n_rows, D] bf16: the unweighted GEMM2 rows in the routed (by-expert)
+ *   order; expert_weights [M, top_k] fp32 (MOE_DTYPE_F32) or bf16
+ *   (MOE_DTYPE_BF16); expanded_idx_to_permuted_idx [M, top_k] int32 (moe_route's
+ *   inv_rows, with its topk_weights, fit directly); shared_output [M, D] bf16 or
+ *   NULL; out [M, D] bf16.  An index >= n_rows is skipped and flagged
+ *   MOE_DEVERR_BAD_INDEX.  Tokens t >= the valid count are not written.
+ * D a multiple of 16 and 16-byte aligned rows/out/shared (MOE_ERR_UNSUPPORTED).
+ */
+int moe_topk_finalize(const void* rows, int64_t n_rows, int D, const void* expert_weights,
+                      int weights_dtype, const int32_t* expanded_idx_to_permuted_idx, int M,
+                      int top_k, const int32_t* valid_token_count, const void* shared_output,
+                      void* out, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -48,13 +48,15 @@ def _load() -> ctypes.CDLL:
         "moe_router_workspace_size": ([I, I, I, ctypes.POINTER(S)], I),
         "moe_router_scores": ([P, I, I, P, I, P, P, P, S, P], I),
         "moe_route_workspace_size": ([I, I, I, ctypes.POINTER(S)], I),
-        "moe_route": ([P, I, L, L, I, I, I, P, P, P, P, P, P, P, S, P], I),
+        "moe_route": ([P, I, L, L, I, I, I, P, P, P, P, P, P, P, P, S, P], I),
         "moe_route_no_alloc": ([P, I, L, L, I, I, I, P, P, P, P, P, P, P], I),
         "moe_gather_scale": ([P, I, I, P, P, I, P, I, L, L, I, P, P, I, P, P], I),
         "moe_gather_scale_quant": ([P, I, I, P, P, I, P, I, L, L, I, P, P, I, P, P, P, P], I),
         "moe_quantize_rows": ([P, L, I, P, P, P, P], I),
         "moe_grouped_gemm": ([P, P, P, I, I, I, I, P, I, P, I, I, P], I),
         "moe_expert_mlp_workspace_size": ([I, ctypes.POINTER(S)], I),
+        "moe_scatter_add_padded": ([P, P, P, I, P, P, I, I, I, I, I, P], I),
+        "moe_topk_finalize": ([P, L, I, P, I, P, I, I, P, P, P, P], I),
         "moe_expert_mlp": ([P, P, P, P, I, I, I, I, P, P, P, I, I, P, S, P], I),
         "moe_grouped_gemm_fp8_rowwise": ([P, P, P, P, P, I, I, I, I, P, I, P, I, I, P], I),
         "moe_silu_mul": ([P, P, L, I, I, P, P, P], I),
@@ -151,9 +153,11 @@ def moe_route_workspace_size(T: int, E: int, top_k: int) -> int:
 
 
 def moe_route(scores: torch.Tensor, top_k: int, num_valid_tokens: torch.Tensor | None = None, *,
-              with_inv: bool = True, out: dict | None = None, workspace: torch.Tensor | None = None, stream=None):
+              with_inv: bool = True, with_weights: bool = False, out: dict | None = None,
+              workspace: torch.Tensor | None = None, stream=None):
     """Route scores[T, E]; returns dict(counts, expert_offsets, expert_indices,
-    token_indices, inv_rows) of int32 device tensors (index arrays of T * top_k)."""
+    token_indices, inv_rows) of int32 device tensors (index arrays of T * top_k),
+    plus topk_weights (fp32 [T * top_k], in inv_rows order) when with_weights."""
     T, E = scores.shape
     dev = scores.device
     o = dict(out or {})
@@ -166,6 +170,10 @@ def moe_route(scores: torch.Tensor, top_k: int, num_valid_tokens: torch.Tensor |
         o.setdefault("inv_rows", torch.empty(T * top_k, **i32))
     else:
         o["inv_rows"] = None
+    if with_weights:
+        o.setdefault("topk_weights", torch.empty(T * top_k, dtype=torch.float32, device=dev))
+    else:
+        o["topk_weights"] = None
     ws_bytes = moe_route_workspace_size(T, E, top_k)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
@@ -174,9 +182,16 @@ def moe_route(scores: torch.Tensor, top_k: int, num_valid_tokens: torch.Tensor |
     st = _lib.moe_route(_ptr(scores), _dtype_code(scores), scores.stride(0), scores.stride(1), T, E, top_k,
                         _ptr(num_valid_tokens), _ptr(o["counts"]), _ptr(o["expert_offsets"]),
                         _ptr(o["expert_indices"]), _ptr(o["token_indices"]), _ptr(o["inv_rows"]),
-                        _ptr(workspace), workspace.numel(), _stream(stream))
+                        _ptr(o["topk_weights"]), _ptr(workspace), workspace.numel(), _stream(stream))
     _check("moe_route", st)
     return o
+
+
+def _scores_args(scores):
+    """(pointer, dtype code, stride_t, stride_e, E) of a score tensor; None = unit scores."""
+    if scores is None:
+        return None, MOE_DTYPE_BF16, 0, 0, 1
+    return _ptr(scores), _dtype_code(scores), scores.stride(0), scores.stride(1), scores.shape[1]
 
 
 # ------------------------------------------------------------------- gather
@@ -188,8 +203,7 @@ def moe_gather_scale(x, token_indices, expert_indices, scores, valid_token_count
     _need(x, torch.bfloat16, "x")
     if out is None:
         out = torch.empty(a, D, dtype=x.dtype, device=x.device)
-    st = _lib.moe_gather_scale(_ptr(x), T, D, _ptr(token_indices), _ptr(expert_indices), a, _ptr(scores),
-                               _dtype_code(scores), scores.stride(0), scores.stride(1), scores.shape[1],
+    st = _lib.moe_gather_scale(_ptr(x), T, D, _ptr(token_indices), _ptr(expert_indices), a, *_scores_args(scores),
                                _ptr(valid_token_count), _ptr(inv_rows), top_k, _ptr(out), _stream(stream))
     _check("moe_gather_scale", st)
     return out
@@ -204,8 +218,8 @@ def moe_gather_scale_quant(x, token_indices, expert_indices, scores, scale_ub=No
         out = torch.empty(a, D, dtype=torch.float8_e4m3fn, device=x.device)
     if out_scale is None:
         out_scale = torch.empty(a, dtype=torch.float32, device=x.device)
-    st = _lib.moe_gather_scale_quant(_ptr(x), T, D, _ptr(token_indices), _ptr(expert_indices), a, _ptr(scores),
-                                     _dtype_code(scores), scores.stride(0), scores.stride(1), scores.shape[1],
+    st = _lib.moe_gather_scale_quant(_ptr(x), T, D, _ptr(token_indices), _ptr(expert_indices), a,
+                                     *_scores_args(scores),
                                      _ptr(valid_token_count), _ptr(inv_rows), top_k, _ptr(scale_ub), _ptr(out),
                                      _ptr(out_scale), _stream(stream))
     _check("moe_gather_scale_quant", st)
@@ -345,4 +359,39 @@ def moe_scatter_add(out, rows, token_indices, inv_rows=None, top_k: int = 1, val
     st = _lib.moe_scatter_add(_ptr(out), _ptr(rows), _ptr(token_indices), _ptr(inv_rows), top_k, a, T, D,
                               _ptr(valid_token_count), int(accumulate), _stream(stream))
     _check("moe_scatter_add", st)
+    return out
+
+
+def moe_scatter_add_padded(out, rows, token_counts, token_indices, inv_rows=None, top_k: int = 1, *,
+                           accumulate: bool = True, stream=None):
+    """scatter_add_padded_tokens on one GPU: the first sum(token_counts) rows of
+    rows[T_K, D] (by-expert order) are added into out[T, D] by token."""
+    T, D = out.shape
+    T_K = rows.shape[0]
+    E = token_counts.shape[0]
+    _need(out, torch.bfloat16, "out")
+    _need(rows, torch.bfloat16, "rows")
+    _need(token_counts, torch.int32, "token_counts")
+    st = _lib.moe_scatter_add_padded(_ptr(out), _ptr(rows), _ptr(token_counts), E, _ptr(token_indices),
+                                     _ptr(inv_rows), top_k, T_K, T, D, int(accumulate), _stream(stream))
+    _check("moe_scatter_add_padded", st)
+    return out
+
+
+def moe_topk_finalize(rows, expert_weights, expanded_idx_to_permuted_idx, shared_output=None,
+                      valid_token_count=None, *, out=None, stream=None):
+    """out[M, D] = bf16(sum_j w[t, j] * rows[idx[t, j]]) (-0 -> +0), plus the shared
+    output (one more rounding); rows[n, D] bf16, weights fp32 or bf16 [M, k], idx int32 [M, k]."""
+    n_rows, D = rows.shape
+    M, k = expanded_idx_to_permuted_idx.shape
+    _need(rows, torch.bfloat16, "rows")
+    _need(expanded_idx_to_permuted_idx, torch.int32, "expanded_idx_to_permuted_idx")
+    if shared_output is not None:
+        _need(shared_output, torch.bfloat16, "shared_output")
+    if out is None:
+        out = torch.empty(M, D, dtype=torch.bfloat16, device=rows.device)
+    st = _lib.moe_topk_finalize(_ptr(rows), n_rows, D, _ptr(expert_weights), _dtype_code(expert_weights),
+                                _ptr(expanded_idx_to_permuted_idx), M, k, _ptr(valid_token_count),
+                                _ptr(shared_output), _ptr(out), _stream(stream))
+    _check("moe_topk_finalize", st)
     return out

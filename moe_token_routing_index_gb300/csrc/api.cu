@@ -126,7 +126,8 @@ int moe_route_workspace_size(int T, int E, int top_k, size_t* bytes) {
 
 int moe_route(const void* scores, int scores_dtype, int64_t stride_t, int64_t stride_e, int T, int E, int top_k,
               const int32_t* num_valid_tokens, int32_t* counts, int32_t* expert_offsets, int32_t* expert_indices,
-              int32_t* token_indices, int32_t* inv_rows, void* ws, size_t ws_bytes, cudaStream_t stream) {
+              int32_t* token_indices, int32_t* inv_rows, float* topk_weights, void* ws, size_t ws_bytes,
+              cudaStream_t stream) {
   size_t need;
   int rc = moe_route_workspace_size(T, E, top_k, &need);
   if (rc != MOE_OK) return rc;
@@ -139,8 +140,9 @@ int moe_route(const void* scores, int scores_dtype, int64_t stride_t, int64_t st
   }
   if (ws_bytes < need) return MOE_ERR_WORKSPACE;
   if (ws && (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOE_ERR_INVALID;
-  moe::RouteArgs a{scores, scores_dtype, stride_t, stride_e, T, E, top_k, num_valid_tokens, counts, expert_offsets,
-                   expert_indices, token_indices, inv_rows, ws, nullptr};
+  moe::RouteArgs a{scores,         scores_dtype,  stride_t,     stride_e, T,  E,      top_k,
+                   num_valid_tokens, counts,      expert_offsets, expert_indices, token_indices, inv_rows,
+                   topk_weights,   ws,            nullptr};
   rc = device_error_word(&a.err);
   if (rc != MOE_OK) return rc;
   return finish(moe::launch_route(a, stream));
@@ -174,8 +176,10 @@ static int check_gather(const void* x, int T, int D, const int32_t* ti, const in
   if (T < 0 || D < 0 || a < 0) return MOE_ERR_INVALID;
   if (a == 0 || D == 0) return MOE_OK;
   if (!x || !ti || !ei || !out) return MOE_ERR_INVALID;
-  int rc = check_scores(scores, dtype, E);
-  if (rc != MOE_OK) return rc;
+  if (scores) {  // NULL scores: every score is 1 (the rows are copied)
+    int rc = check_scores(scores, dtype, E);
+    if (rc != MOE_OK) return rc;
+  }
   if (D % 16 != 0 || !aligned16(x) || !aligned16(out)) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
@@ -257,10 +261,45 @@ int moe_scatter_add(void* out, const void* in, const int32_t* token_indices, con
   if (top_k > 1 && !inv_rows) return MOE_ERR_INVALID;
   if (!inv_rows && !token_indices) return MOE_ERR_INVALID;
   if (D % 16 != 0 || !aligned16(out) || !aligned16(in)) return MOE_ERR_UNSUPPORTED;
-  moe::ScatterArgs g{out, in, token_indices, inv_rows, top_k, a, T, D, valid_token_count, accumulate != 0, nullptr};
+  moe::ScatterArgs g{out, in, token_indices, inv_rows, top_k, a, T, D, valid_token_count, accumulate != 0,
+                     nullptr, 0, nullptr};
   int rc = device_error_word(&g.err);
   if (rc != MOE_OK) return rc;
   return finish(moe::launch_scatter_add(g, stream));
+}
+
+int moe_scatter_add_padded(void* out, const void* in, const int32_t* token_counts, int E,
+                           const int32_t* token_indices, const int32_t* inv_rows, int top_k, int T_K, int T, int D,
+                           int accumulate, cudaStream_t stream) {
+  if (E < 1 || T_K < 0 || T < 0 || D < 0 || top_k < 1) return MOE_ERR_INVALID;
+  if (T_K == 0 || D == 0 || T == 0) return MOE_OK;
+  if (!out || !in || !token_counts) return MOE_ERR_INVALID;
+  if (E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (T_K % T != 0) return MOE_ERR_INVALID;  // the padded layout holds T_K = T * top_k rows
+  if (top_k > 1 && !inv_rows) return MOE_ERR_INVALID;
+  if (!inv_rows && !token_indices) return MOE_ERR_INVALID;
+  if (D % 16 != 0 || !aligned16(out) || !aligned16(in)) return MOE_ERR_UNSUPPORTED;
+  moe::ScatterArgs g{out, in, token_indices, inv_rows, top_k, T_K, T, D, nullptr, accumulate != 0,
+                     token_counts, E, nullptr};
+  int rc = device_error_word(&g.err);
+  if (rc != MOE_OK) return rc;
+  return finish(moe::launch_scatter_add(g, stream));
+}
+
+int moe_topk_finalize(const void* rows, int64_t n_rows, int D, const void* expert_weights, int weights_dtype,
+                      const int32_t* expanded_idx_to_permuted_idx, int M, int top_k,
+                      const int32_t* valid_token_count, const void* shared_output, void* out, cudaStream_t stream) {
+  if (n_rows < 0 || D < 0 || M < 0 || top_k < 1) return MOE_ERR_INVALID;
+  if (M == 0 || D == 0) return MOE_OK;
+  if (!out || !expert_weights || !expanded_idx_to_permuted_idx || (n_rows > 0 && !rows)) return MOE_ERR_INVALID;
+  if (weights_dtype != MOE_DTYPE_F32 && weights_dtype != MOE_DTYPE_BF16) return MOE_ERR_INVALID;
+  if (D % 16 != 0 || !aligned16(out) || (rows && !aligned16(rows)) || (shared_output && !aligned16(shared_output)))
+    return MOE_ERR_UNSUPPORTED;
+  moe::FinalizeArgs g{rows, n_rows, D, expert_weights, weights_dtype, expanded_idx_to_permuted_idx, M, top_k,
+                      valid_token_count, shared_output, out, nullptr};
+  int rc = device_error_word(&g.err);
+  if (rc != MOE_OK) return rc;
+  return finish(moe::launch_topk_finalize(g, stream));
 }
 
 static int grouped_gemm_common(const void* x, const void* w, const int32_t* counts, const float* x_scale,

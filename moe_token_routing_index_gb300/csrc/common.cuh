@@ -30,7 +30,9 @@ __device__ __forceinline__ int read_count(const int32_t* p, int hi, unsigned int
   return v;
 }
 
+// A routing score; NULL scores read as 1.0 (the gathers then copy rows unscaled).
 __device__ __forceinline__ float load_score(const void* scores, int dtype, int64_t off) {
+  if (!scores) return 1.0f;
   if (dtype == MOE_DTYPE_F32) return __ldg(reinterpret_cast<const float*>(scores) + off);
   return __bfloat162float(__ldg(reinterpret_cast<const __nv_bfloat16*>(scores) + off));
 }

@@ -19,6 +19,7 @@ struct RouteArgs {
   int32_t* expert_indices;
   int32_t* token_indices;
   int32_t* inv;
+  float* weights;  // nullable: top-k scores in the order of inv
   void* ws;
   unsigned int* err;
 };
@@ -87,10 +88,28 @@ struct ScatterArgs {
   int top_k, a, T, D;
   const int32_t* valid;
   bool accumulate;
+  const int32_t* sum_counts;  // nullable: the valid row count is sum(sum_counts[0, E)) instead of *valid
+  int E;
   unsigned int* err;
 };
 
 cudaError_t launch_scatter_add(const ScatterArgs& a, cudaStream_t s);
+
+struct FinalizeArgs {
+  const void* rows;          // bf16 [n_rows, D]
+  int64_t n_rows;
+  int D;
+  const void* weights;       // [M, k] f32 or bf16
+  int weights_dtype;
+  const int32_t* idx;        // [M, k], -1: absent
+  int M, k;
+  const int32_t* valid;      // nullable: M
+  const void* shared;        // nullable: bf16 [M, D]
+  void* out;                 // bf16 [M, D]
+  unsigned int* err;
+};
+
+cudaError_t launch_topk_finalize(const FinalizeArgs& a, cudaStream_t s);
 
 struct GemmArgs {
   const void* x;        // [a_max, K] bf16 or e4m3

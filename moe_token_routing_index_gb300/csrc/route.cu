@@ -119,7 +119,8 @@ __device__ void route_scan_expert(int e, int32_t* __restrict__ hist_t, int nblk,
 __device__ void route_emit_chunk(int c, int E, int k, int Tv, const int32_t* __restrict__ chosen,
                                  const int32_t* __restrict__ hist_t, int nblk, const int* s_off, unsigned int* s_bits,
                                  int32_t* __restrict__ expert_indices, int32_t* __restrict__ token_indices,
-                                 int32_t* __restrict__ inv) {
+                                 int32_t* __restrict__ inv, float* __restrict__ wts, const void* __restrict__ scores,
+                                 int dtype, int64_t st, int64_t se) {
   const int tid = threadIdx.x;
   const int t0 = c * kTokBlock;
   const int nt = min(kTokBlock, Tv - t0);
@@ -139,10 +140,11 @@ __device__ void route_emit_chunk(int c, int E, int k, int Tv, const int32_t* __r
     const int row = s_off[e] + __ldcg(hist_t + (int64_t)e * nblk + c) + rank;
     expert_indices[row] = e;
     token_indices[row] = t;
-    if (inv) {
+    if (inv || wts) {
       int pos = 0;  // rows of t ascend with the expert index
       for (int jj = 0; jj < k; ++jj) pos += __ldcg(ch + jj) < e;
-      inv[(int64_t)t * k + pos] = row;
+      if (inv) inv[(int64_t)t * k + pos] = row;
+      if (wts) wts[(int64_t)t * k + pos] = load_score(scores, dtype, (int64_t)t * st + (int64_t)e * se);
     }
   }
   __syncthreads();
@@ -186,7 +188,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_coop_kernel(
     const int32_t* __restrict__ num_valid, int32_t* __restrict__ chosen, int32_t* __restrict__ hist_t, int nblk,
     unsigned int* barrier, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
     int32_t* __restrict__ expert_indices, int32_t* __restrict__ token_indices, int32_t* __restrict__ inv,
-    unsigned int* err) {
+    float* __restrict__ wts, unsigned int* err) {
   __shared__ int s_a[1024];          // select: histogram; emit: expert offsets
   __shared__ unsigned int s_bits[1024];
   __shared__ int s_part[kRouteThreads];
@@ -229,7 +231,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_coop_kernel(
     }
   }
   for (int c = blockIdx.x; c < nchunks; c += gridDim.x)
-    route_emit_chunk(c, E, k, Tv, chosen, hist_t, nblk, s_a, s_bits, expert_indices, token_indices, inv);
+    route_emit_chunk(c, E, k, Tv, chosen, hist_t, nblk, s_a, s_bits, expert_indices, token_indices, inv, wts, scores,
+                     dtype, st, se);
 }
 
 // ---------------------------------------------------------------------------
@@ -252,7 +255,7 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
     const void* __restrict__ scores, int dtype, int64_t st, int64_t se, int T, int E, int k,
     const int32_t* __restrict__ num_valid, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
     int32_t* __restrict__ expert_indices, int32_t* __restrict__ token_indices, int32_t* __restrict__ inv,
-    unsigned int* err) {
+    float* __restrict__ wts, unsigned int* err) {
   extern __shared__ __align__(16) uint8_t smem[];
   uint32_t* s_key = reinterpret_cast<uint32_t*>(smem);                 // [T][E]
   int* s_hist = reinterpret_cast<int*>(s_key + (size_t)T * E);        // [warps][E]: counts, then bases
@@ -345,10 +348,11 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
       my_hist[e] += 1;
       expert_indices[row] = e;
       token_indices[row] = t;
-      if (inv) {
+      if (inv || wts) {
         int pos = 0;
         for (int jj = 0; jj < k; ++jj) pos += s_chosen[t * k + jj] < e;
-        inv[(int64_t)t * k + pos] = row;
+        if (inv) inv[(int64_t)t * k + pos] = row;
+        if (wts) wts[(int64_t)t * k + pos] = load_score(scores, dtype, (int64_t)t * st + (int64_t)e * se);
       }
     }
     __syncwarp();
@@ -362,7 +366,8 @@ cudaError_t launch_small(const RouteArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<1, kSmallThreads, smem, s>>>(a.scores, a.dtype, a.stride_t, a.stride_e, a.T, a.E, a.top_k, a.num_valid,
-                                      a.counts, a.offsets, a.expert_indices, a.token_indices, a.inv, a.err);
+                                      a.counts, a.offsets, a.expert_indices, a.token_indices, a.inv, a.weights,
+                                      a.err);
   return cudaGetLastError();
 }
 
@@ -385,7 +390,7 @@ cudaError_t launch_coop(const RouteArgs& a, int32_t* chosen, int32_t* hist_t, in
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, kern, a.scores, a.dtype, a.stride_t, a.stride_e, a.T, a.E, a.top_k, a.num_valid,
                          chosen, hist_t, nblk, barrier, a.counts, a.offsets, a.expert_indices, a.token_indices,
-                         a.inv, a.err);
+                         a.inv, a.weights, a.err);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

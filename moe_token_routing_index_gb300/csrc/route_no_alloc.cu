@@ -70,5 +70,6 @@ extern "C" int moe_route_no_alloc(const void* scores, int scores_dtype, int64_t 
   // The routing kernels write every scratch word before they read it, so the
   // previous call's leftovers need no clearing.
   return moe_route(scores, scores_dtype, stride_t, stride_e, T, E, top_k, num_valid_tokens, counts,
-                   expert_offsets, expert_indices, token_indices, inv_rows, scratch, kScratchBytes, stream);
+                   expert_offsets, expert_indices, token_indices, inv_rows, nullptr, scratch, kScratchBytes,
+                   stream);
 }

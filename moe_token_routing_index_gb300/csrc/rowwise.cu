@@ -112,7 +112,8 @@ __global__ void __launch_bounds__(kThreads) gather_scale_kernel(
       t = __ldg(ti + rn);
       e = __ldg(ei + rn);
     }
-    if ((unsigned)ct >= (unsigned)T || (unsigned)ce >= (unsigned)E) {
+    // the expert index only addresses the scores (NULL scores: every score is 1)
+    if ((unsigned)ct >= (unsigned)T || (scores && (unsigned)ce >= (unsigned)E)) {
       if (lane == 0) flag_error(err, MOE_DEVERR_BAD_INDEX);
       continue;
     }
@@ -163,7 +164,7 @@ __global__ void __launch_bounds__(kThreads) gather_scale_quant_kernel(
   bool ok = false;
   int nt = 0, ne = 0;  // indices of the next row
   auto fetch_data = [&](int t, int e) {
-    ok = (unsigned)t < (unsigned)T && (unsigned)e < (unsigned)E;
+    ok = (unsigned)t < (unsigned)T && (!scores || (unsigned)e < (unsigned)E);
     if (ok) {
       s = load_score(scores, dtype, (int64_t)t * st + (int64_t)e * se);
       const uint4* src = x + (int64_t)t * D8;
@@ -347,7 +348,7 @@ __global__ void __launch_bounds__(kStagedWarps * 32, 1) gather_staged_kernel(
       const int r = inv ? __ldg(inv + (int64_t)item * k + j) : item;
       const int t = inv ? item : __ldg(ti + item);
       const int e = (unsigned)r < (unsigned)a ? __ldg(ei + r) : -1;
-      if ((unsigned)r < (unsigned)a && (unsigned)e < (unsigned)E && (unsigned)t < (unsigned)T) {
+      if ((unsigned)r < (unsigned)a && (!scores || (unsigned)e < (unsigned)E) && (unsigned)t < (unsigned)T) {
         m_row = r;
         m_s = load_score(scores, dtype, (int64_t)t * st + (int64_t)e * se);
       }
@@ -587,6 +588,35 @@ __global__ void __launch_bounds__(kThreads) silu_mul_quant_kernel(const __nv_bfl
 
 // ------------------------------------------------------------- scatter-add
 
+// The number of valid routed rows: *valid_p (clamped to a), or, when sum_counts is
+// given, the sum of the E per-expert counts (the padded-token layout, whose valid
+// rows are every expert's rows).  Called by every thread of the block.
+__device__ int valid_rows(const int32_t* valid_p, const int32_t* sum_counts, int E, int a, unsigned int* err) {
+  if (!sum_counts) return read_count(valid_p, a, err);
+  __shared__ int s_rows;
+  if (threadIdx.x < 32) {
+    int v = 0;
+    bool bad = false;
+    for (int e = threadIdx.x; e < E; e += 32) {
+      const int c = __ldg(sum_counts + e);
+      bad |= c < 0;
+      v += c > 0 ? c : 0;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    bad = __any_sync(0xffffffffu, bad);
+    if (threadIdx.x == 0) {
+      if (bad || v > a) {
+        if (blockIdx.x == 0) flag_error(err, MOE_DEVERR_BAD_COUNT);
+        if (v > a) v = a;
+      }
+      s_rows = v;
+    }
+  }
+  __syncthreads();
+  return s_rows;
+}
+
 // top_k == 1 without the inverse permutation: routed row r owns token ti[r].
 // Work items as in the gather: (row, chunk).
 template <bool ACC>
@@ -594,8 +624,9 @@ __global__ void __launch_bounds__(kThreads) scatter_add_rows_kernel(uint4* __res
                                                                     const uint4* __restrict__ in,
                                                                     const int32_t* __restrict__ ti, int a, int T,
                                                                     int D8, const int32_t* __restrict__ valid_p,
+                                                                    const int32_t* __restrict__ sum_counts, int E,
                                                                     unsigned int* err) {
-  const int valid = read_count(valid_p, a, err);
+  const int valid = valid_rows(valid_p, sum_counts, E, a, err);
   const int lane = threadIdx.x & 31;
   const int chunks = (D8 + kChunk - 1) / kChunk;
   const int64_t items = (int64_t)valid * chunks;
@@ -642,8 +673,9 @@ __global__ void __launch_bounds__(kThreads) scatter_add_tokens_kernel(uint4* __r
                                                                       const int32_t* __restrict__ inv, int k, int a,
                                                                       int T, int D8,
                                                                       const int32_t* __restrict__ valid_p,
+                                                                      const int32_t* __restrict__ sum_counts, int E,
                                                                       unsigned int* err) {
-  const int valid = read_count(valid_p, a, err);
+  const int valid = valid_rows(valid_p, sum_counts, E, a, err);
   if (valid % k != 0 && blockIdx.x == 0 && threadIdx.x == 0) flag_error(err, MOE_DEVERR_BAD_COUNT);
   int Tv = valid / k;
   if (Tv > T) Tv = T;
@@ -697,6 +729,78 @@ __global__ void __launch_bounds__(kThreads) scatter_add_tokens_kernel(uint4* __r
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u)
       if (c0 + 32 * u < D8) o[c0 + 32 * u] = f32_to_bf16x8(acc[u]);
+  }
+}
+
+// Top-k finalize: a warp owns a (token, chunk) item, multiplies each present
+// route's row by its weight and adds it in slot order into an fp32 accumulator
+// started at zero (fp32 multiply, then fp32 add); the bf16 result has its
+// negative zero replaced by +0, and the shared output is added with one more
+// rounding.  Tokens t >= the valid count are not written.
+template <bool SHARED, bool F32W>
+__global__ void __launch_bounds__(kThreads) topk_finalize_kernel(uint4* __restrict__ out,
+                                                                 const uint4* __restrict__ rows, int64_t n_rows,
+                                                                 int D8, const void* __restrict__ weights,
+                                                                 const int32_t* __restrict__ idx, int M, int k,
+                                                                 const int32_t* __restrict__ valid_p,
+                                                                 const uint4* __restrict__ shared, unsigned int* err) {
+  const int Mv = read_count(valid_p, M, err);
+  const int lane = threadIdx.x & 31;
+  const int chunks = (D8 + kChunk - 1) / kChunk;
+  const int64_t items = (int64_t)Mv * chunks;
+  for (int64_t it = global_warp(); it < items; it += num_warps()) {
+    const int t = (int)(it / chunks);
+    const int c0 = (int)(it - (int64_t)t * chunks) * kChunk + lane;
+    float acc[kUnroll][8];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
+    for (int j = 0; j < k; ++j) {
+      const int64_t sj = (int64_t)t * k + j;
+      const int p = __ldg(idx + sj);
+      if (p < 0) continue;  // a route that is absent
+      if (p >= n_rows) {
+        if (lane == 0) flag_error(err, MOE_DEVERR_BAD_INDEX);
+        continue;
+      }
+      const float w = F32W ? __ldg(reinterpret_cast<const float*>(weights) + sj)
+                           : __bfloat162float(__ldg(reinterpret_cast<const __nv_bfloat16*>(weights) + sj));
+      const uint4* src = rows + (int64_t)p * D8;
+      uint4 v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        if (c0 + 32 * u < D8) v[u] = __ldg(src + c0 + 32 * u);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        if (c0 + 32 * u < D8) {
+          float fi[8];
+          bf16x8_to_f32(v[u], fi);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[u][i] = __fadd_rn(acc[u][i], __fmul_rn(w, fi[i]));
+        }
+    }
+    uint4* o = out + (int64_t)t * D8;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (c0 + 32 * u < D8) {
+        uint4 r = f32_to_bf16x8(acc[u]);
+        uint32_t* h = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // negative zero -> +0, per bf16 half
+          if ((h[q] & 0xFFFFu) == 0x8000u) h[q] &= 0xFFFF0000u;
+          if ((h[q] >> 16) == 0x8000u) h[q] &= 0x0000FFFFu;
+        }
+        if (SHARED) {
+          float fr[8], fs[8];
+          bf16x8_to_f32(r, fr);
+          bf16x8_to_f32(__ldg(shared + (int64_t)t * D8 + c0 + 32 * u), fs);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) fr[i] = __fadd_rn(fr[i], fs[i]);
+          r = f32_to_bf16x8(fr);
+        }
+        o[c0 + 32 * u] = r;
+      }
   }
 }
 
@@ -790,13 +894,24 @@ cudaError_t launch_scatter_add(const ScatterArgs& g, cudaStream_t s) {
     auto k = g.accumulate ? scatter_add_tokens_kernel<true> : scatter_add_tokens_kernel<false>;
     const int grid = persistent_grid(k, (int64_t)g.T * ((D8 + kChunk - 1) / kChunk), kWarps);
     k<<<grid, kThreads, 0, s>>>(static_cast<uint4*>(g.out), static_cast<const uint4*>(g.in), g.inv, g.top_k, g.a,
-                                g.T, D8, g.valid, g.err);
+                                g.T, D8, g.valid, g.sum_counts, g.E, g.err);
   } else {
     auto k = g.accumulate ? scatter_add_rows_kernel<true> : scatter_add_rows_kernel<false>;
     const int grid = persistent_grid(k, (int64_t)g.a * ((D8 + kChunk - 1) / kChunk), kWarps);
     k<<<grid, kThreads, 0, s>>>(static_cast<uint4*>(g.out), static_cast<const uint4*>(g.in), g.token_indices, g.a,
-                                g.T, D8, g.valid, g.err);
+                                g.T, D8, g.valid, g.sum_counts, g.E, g.err);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk_finalize(const FinalizeArgs& g, cudaStream_t s) {
+  const int D8 = g.D / 8;
+  const bool f32 = g.weights_dtype == MOE_DTYPE_F32;
+  auto k = g.shared ? (f32 ? topk_finalize_kernel<true, true> : topk_finalize_kernel<true, false>)
+                    : (f32 ? topk_finalize_kernel<false, true> : topk_finalize_kernel<false, false>);
+  const int grid = persistent_grid(k, (int64_t)g.M * ((D8 + kChunk - 1) / kChunk), kWarps);
+  k<<<grid, kThreads, 0, s>>>(static_cast<uint4*>(g.out), static_cast<const uint4*>(g.rows), g.n_rows, D8, g.weights,
+                              g.idx, g.M, g.k, g.valid, static_cast<const uint4*>(g.shared), g.err);
   return cudaGetLastError();
 }
 

@@ -69,7 +69,8 @@ class MoELayer:
                  fused_mlp: bool | None = None, cta_pairs: bool | None = None, *,
                  router: torch.Tensor | None = None, shared_w13: torch.Tensor | None = None,
                  shared_w2: torch.Tensor | None = None, shared_w13_scale: torch.Tensor | None = None,
-                 shared_w2_scale: torch.Tensor | None = None, overlap_shared: bool = True):
+                 shared_w2_scale: torch.Tensor | None = None, overlap_shared: bool = True,
+                 weighting: str = "input"):
         self.E, n2, self.D = w13.shape
         self.H = n2 // 2
         assert w2.shape == (self.E, self.D, self.H), "w2 must be [E, D, H]"
@@ -106,6 +107,11 @@ class MoELayer:
             if self.fp8:
                 assert self.sw13_scale is not None and self.sw2_scale is not None
         self.overlap_shared = overlap_shared
+        # "input": the score scales each routed row before the experts (gather_scale_dense_tokens);
+        # "output": the experts see the unscaled rows and the top-k finalize weights their outputs.
+        if weighting not in ("input", "output"):
+            raise ValueError("weighting must be 'input' or 'output'")
+        self.weighting = weighting
         self._side: torch.cuda.Stream | None = None
         self._bufs: _Buffers | None = None
 
@@ -143,6 +149,8 @@ class MoELayer:
         route = dict(counts=torch.zeros(E + 1, **i32), expert_offsets=torch.zeros(E + 1, **i32),
                      expert_indices=torch.zeros(a, **i32), token_indices=torch.zeros(a, **i32),
                      inv_rows=torch.zeros(a, **i32))
+        if self.weighting == "output":
+            route["topk_weights"] = torch.zeros(a, **f32)
         ws = torch.empty(max(mb.moe_route_workspace_size(T, E, k), 256), dtype=torch.uint8, device=device)
         mlp_ws = torch.empty(mb.moe_expert_mlp_workspace_size(max(E, 1)), dtype=torch.uint8, device=device)
         if self.fp8:
@@ -161,6 +169,8 @@ class MoELayer:
             Hs = self.Hs
             x["all_tokens"] = torch.tensor([T], **i32)       # the shared expert's row count without a valid count
             x["ident"] = torch.arange(T, **i32)
+            if self.weighting == "output":
+                x["sh_out"] = torch.empty(T, D, **bf)           # the finalize adds it to the weighted sum
             x["sh_mlp_ws"] = torch.empty(mb.moe_expert_mlp_workspace_size(1), dtype=torch.uint8, device=device)
             if self.fp8:
                 x["zero"] = torch.zeros(T, **i32)
@@ -189,6 +199,15 @@ class MoELayer:
             scores = ex["scores"]
             st.append(("router", lambda: mb.moe_router_scores(x, self.router, num_valid_tokens, out=ex["scores"],
                                                               workspace=ex["router_ws"]), MAIN))
+        if self.weighting == "output":
+            if accumulate:
+                raise ValueError("the top-k finalize writes the output; accumulate is not supported with it")
+            sh_out = None
+            if self.shared:
+                sh_out = ex["sh_out"]
+                st += [(n, f, SIDE) for n, f in self._shared_stages(x, num_valid_tokens, sh_out, False)]
+            st += [(n, f, MAIN) for n, f in self._routed_stages(x, scores, num_valid_tokens, out, False, sh_out)]
+            return st
         if self.shared:
             st += [(n, f, SIDE) for n, f in self._shared_stages(x, num_valid_tokens, out, accumulate)]
             accumulate = True       # the routed rows are added into the shared expert's output
@@ -221,7 +240,7 @@ class MoELayer:
                                                                   self.sw2_scale, out=out, **add)),
         ]
 
-    def _routed_stages(self, x, scores, num_valid_tokens, out, accumulate):
+    def _routed_stages(self, x, scores, num_valid_tokens, out, accumulate, shared_out=None):
         T = x.shape[0]
         b = self.buffers(T, x.device)
         r = b.route
@@ -230,13 +249,16 @@ class MoELayer:
         ti, ei = r["token_indices"], r["expert_indices"]
         inv = r["inv_rows"] if self.top_k > 1 else None
         k = self.top_k
-        fuse_combine = k == 1
+        out_w = self.weighting == "output"
+        fuse_combine = k == 1 and not out_w
         pairs = mb.MOE_GEMM_CTA_PAIRS if self.use_cta_pairs(T) else 0
         # the w2 GEMM writes either the routed rows o, or (top_k = 1) the tokens' rows of out
         w2_out = dict(out=out, scatter_indices=ti, accumulate=accumulate) if fuse_combine else dict(out=b.o)
-        st = [("route", lambda: mb.moe_route(scores, k, num_valid_tokens, out=r, workspace=b.ws))]
+        st = [("route", lambda: mb.moe_route(scores, k, num_valid_tokens, with_weights=out_w, out=r,
+                                             workspace=b.ws))]
+        gscores = None if out_w else scores    # output weighting: the gathers copy the rows
         if not self.fp8:
-            st.append(("gather", lambda: mb.moe_gather_scale(x, ti, ei, scores, valid, inv_rows=inv, top_k=k,
+            st.append(("gather", lambda: mb.moe_gather_scale(x, ti, ei, gscores, valid, inv_rows=inv, top_k=k,
                                                              out=b.xr)))
             if self.use_fused_mlp(T):
                 st.append(("expert_mlp", lambda: mb.moe_expert_mlp(b.xr, self.w13, self.w2, counts, z=b.z,
@@ -250,7 +272,7 @@ class MoELayer:
                 ]
         else:
             st += [
-                ("gather_quant", lambda: mb.moe_gather_scale_quant(x, ti, ei, scores, self.scale_ub, valid,
+                ("gather_quant", lambda: mb.moe_gather_scale_quant(x, ti, ei, gscores, self.scale_ub, valid,
                                                                    inv_rows=inv, top_k=k, out=b.xr,
                                                                    out_scale=b.xs)),
                 ("gemm_w13", lambda: mb.moe_grouped_gemm_fp8_rowwise(b.xr, self.w13, counts, b.xs, self.w13_scale,
@@ -260,14 +282,19 @@ class MoELayer:
                 ("gemm_w2", lambda: mb.moe_grouped_gemm_fp8_rowwise(b.z, self.w2, counts, b.zs, self.w2_scale,
                                                                     epilogue=pairs, **w2_out)),
             ]
-        if not fuse_combine:
+        if out_w:
+            idx = r["inv_rows"].view(T, k)
+            wts = r["topk_weights"].view(T, k)
+            st.append(("finalize", lambda: mb.moe_topk_finalize(b.o, wts, idx, shared_out, num_valid_tokens,
+                                                                out=out)))
+        elif not fuse_combine:
             st.append(("scatter", lambda: mb.moe_scatter_add(out, b.o, ti, inv, k, valid, accumulate=accumulate)))
         return st
 
     @staticmethod
     def combine_stage(names) -> str:
         """The first routed stage that writes the layer output."""
-        for n in ("scatter", "expert_mlp", "gemm_w2"):   # top_k > 1: the scatter; else the w2 GEMM's epilogue
+        for n in ("finalize", "scatter", "expert_mlp", "gemm_w2"):   # else the w2 GEMM's epilogue (top_k = 1)
             if n in names:
                 return n
         raise ValueError("no combine stage")
@@ -343,7 +370,7 @@ class MoELayer:
         silu_mul_quant (FP8), scatter, and the shared expert's."""
         T = self._bufs.T if T is None and self._bufs is not None else (T or 0)
         route = 1
-        scatter = 0 if self.top_k == 1 else 1
+        scatter = 0 if (self.top_k == 1 and self.weighting == "input") else 1   # scatter or finalize
         n = (route + 4 + scatter) if self.fp8 else (route + 1 + (1 if self.use_fused_mlp(T) else 2) + scatter)
         if with_router:
             n += 1

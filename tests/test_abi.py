@@ -45,10 +45,10 @@ def test_host_side_validation_without_gpu(lib):
     assert L.moe_route_workspace_size(64, 8, 2, ctypes.byref(n)) == lib.MOE_OK and n.value > 0
     fake = ctypes.c_void_p(0x1000)
     # route: workspace too small
-    assert L.moe_route(fake, 0, 8, 1, 64, 8, 2, None, fake, fake, fake, fake, None, fake, 16, None) \
+    assert L.moe_route(fake, 0, 8, 1, 64, 8, 2, None, fake, fake, fake, fake, None, None, fake, 16, None) \
         == lib.MOE_ERR_WORKSPACE
     # route: null counts
-    assert L.moe_route(fake, 0, 8, 1, 64, 8, 2, None, None, fake, fake, fake, None, fake, 1 << 20, None) \
+    assert L.moe_route(fake, 0, 8, 1, 64, 8, 2, None, None, fake, fake, fake, None, None, fake, 1 << 20, None) \
         == lib.MOE_ERR_INVALID
     # gather: D not a multiple of 16; empty is a no-op
     assert L.moe_gather_scale(fake, 4, 24, fake, fake, 4, fake, 0, 8, 1, 8, None, None, 1, fake, None) \
@@ -90,3 +90,12 @@ def test_host_side_validation_without_gpu(lib):
         == lib.MOE_ERR_UNSUPPORTED                                                   # misaligned router weight
     assert L.moe_router_scores(None, 0, 64, None, 8, None, None, None, 0, None) == lib.MOE_OK
     assert L.moe_router_scores(None, 4, 64, fake, 8, None, fake, fake, 1 << 30, None) == lib.MOE_ERR_INVALID
+    # top-k finalize: bad weight dtype, odd D, empty is a no-op
+    assert L.moe_topk_finalize(fake, 8, 32, fake, 7, fake, 4, 2, None, None, fake, None) == lib.MOE_ERR_INVALID
+    assert L.moe_topk_finalize(fake, 8, 24, fake, 1, fake, 4, 2, None, None, fake, None) == lib.MOE_ERR_UNSUPPORTED
+    assert L.moe_topk_finalize(None, 0, 32, None, 1, None, 0, 2, None, None, None, None) == lib.MOE_OK
+    assert L.moe_topk_finalize(fake, 8, 32, fake, 1, fake, 4, 0, None, None, fake, None) == lib.MOE_ERR_INVALID
+    # padded scatter: T_K not a multiple of T, missing counts, top_k > 1 without the inverse permutation
+    assert L.moe_scatter_add_padded(fake, fake, fake, 8, fake, None, 1, 30, 8, 32, 1, None) == lib.MOE_ERR_INVALID
+    assert L.moe_scatter_add_padded(fake, fake, None, 8, fake, None, 1, 32, 8, 32, 1, None) == lib.MOE_ERR_INVALID
+    assert L.moe_scatter_add_padded(fake, fake, fake, 8, fake, None, 2, 32, 16, 32, 1, None) == lib.MOE_ERR_INVALID
