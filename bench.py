@@ -234,7 +234,7 @@ def run_ours(args, cfg):
         router = workloads.make_router(cfg, device=dev)
         shared = workloads.make_shared_weights(cfg, device=dev)
     layer = MoELayer.from_weights(cfg, w13, w2, cta_pairs=pairs, router=router, shared=shared,
-                                  overlap_shared=not args.no_overlap)
+                                  overlap_shared=not args.no_overlap, weighting=args.weighting)
     if args.no_cpu_baseline or world > 1 or rank != 0:
         # only the oracle baseline needs the source weights (fp32 for FP8 layers)
         del w13, w2
@@ -297,45 +297,72 @@ def run_ours(args, cfg):
 
 
 def run_e2e(args, cfg, layer, x, s, nv, out, world):
-    """The same forward through the public API with pinned host buffers: each
-    step copies its inputs host -> device and its result device -> host."""
+    """The same forward through the public API with pinned host buffers: every
+    step copies its inputs host -> device and its result device -> host.  Steps
+    are pipelined over two buffer slots, as a serving loop would run them: the
+    inputs of step i+1 and the result of step i-1 move on two copy streams
+    while step i computes.  The timed region spans all K steps, copies included."""
     import torch
     import torch.distributed as dist
 
     K = args.steps
-    xh = x.cpu().pin_memory()
-    sh = None if s is None else s.cpu().pin_memory()     # the whole layer computes its own scores
-    nvh = None if nv is None else nv.cpu().pin_memory()
-    outh = torch.empty(cfg.T, cfg.D, dtype=torch.bfloat16).pin_memory()
-    xd, sd = torch.empty_like(x), None if s is None else torch.empty_like(s)
-    nvd = None if nv is None else torch.empty_like(nv)
-    outd = torch.zeros_like(out)
+    slots = 2
+    comp = torch.cuda.current_stream()
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+    xh = [x.cpu().pin_memory() for _ in range(slots)]
+    sh = [None if s is None else s.cpu().pin_memory() for _ in range(slots)]   # the whole layer routes itself
+    nvh = [None if nv is None else nv.cpu().pin_memory() for _ in range(slots)]
+    outh = [torch.empty(cfg.T, cfg.D, dtype=torch.bfloat16).pin_memory() for _ in range(slots)]
+    xd = [torch.empty_like(x) for _ in range(slots)]
+    sd = [None if s is None else torch.empty_like(s) for _ in range(slots)]
+    nvd = [None if nv is None else torch.empty_like(nv) for _ in range(slots)]
+    outd = [torch.zeros_like(out) for _ in range(slots)]
+    ev_in = [torch.cuda.Event() for _ in range(slots)]
+    ev_comp = [torch.cuda.Event() for _ in range(slots)]
+    ev_out = [torch.cuda.Event() for _ in range(slots)]
+    for i in range(slots):           # every slot starts free
+        ev_comp[i].record(comp)
+        ev_out[i].record(comp)
 
-    def e2e_step():
-        xd.copy_(xh, non_blocking=True)
-        if sd is not None:
-            sd.copy_(sh, non_blocking=True)
-        if nvd is not None:
-            nvd.copy_(nvh, non_blocking=True)
-        layer(xd, sd, nvd, out=outd)
-        outh.copy_(outd, non_blocking=True)
+    def e2e_step(i):
+        j = i % slots
+        with torch.cuda.stream(h2d_s):
+            h2d_s.wait_event(ev_comp[j])           # the compute that read this slot is done
+            xd[j].copy_(xh[j], non_blocking=True)
+            if sd[j] is not None:
+                sd[j].copy_(sh[j], non_blocking=True)
+            if nvd[j] is not None:
+                nvd[j].copy_(nvh[j], non_blocking=True)
+            ev_in[j].record(h2d_s)
+        comp.wait_event(ev_in[j])
+        comp.wait_event(ev_out[j])                 # this slot's previous result has left the device
+        layer(xd[j], sd[j], nvd[j], out=outd[j])
+        ev_comp[j].record(comp)
+        with torch.cuda.stream(d2h_s):
+            d2h_s.wait_event(ev_comp[j])
+            outh[j].copy_(outd[j], non_blocking=True)
+            ev_out[j].record(d2h_s)
 
-    for _ in range(max(2, min(args.warmup, 10))):
-        e2e_step()
+    for i in range(max(2, min(args.warmup, 10))):
+        e2e_step(i)
     torch.cuda.synchronize()
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
-    e_start.record()
-    for _ in range(K):
-        e2e_step()
-    e_end.record()
+    e_start.record(comp)
+    h2d_s.wait_event(e_start)
+    d2h_s.wait_event(e_start)
+    for i in range(K):
+        e2e_step(i)
+    for j in range(slots):
+        comp.wait_event(ev_out[j])
+    e_end.record(comp)
     torch.cuda.synchronize()
     e2e_ms = e_start.elapsed_time(e_end) / K
     e2e_ms = max_over_ranks(e2e_ms, x.device)
-    h2d = xh.numel() * xh.element_size() + (0 if sh is None else sh.numel() * sh.element_size()) + \
-        (0 if nvh is None else 4)
-    d2h = outh.numel() * outh.element_size()
+    h2d = xh[0].numel() * xh[0].element_size() + (0 if sh[0] is None else sh[0].numel() * sh[0].element_size()) + \
+        (0 if nvh[0] is None else 4)
+    d2h = outh[0].numel() * outh[0].element_size()
     return e2e_ms, h2d, d2h
 
 
@@ -362,6 +389,8 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
     }
     if cfg.fp8:
         work["silu_quant"] = ("hbm", a * 2 * H * 2 + a * H + a * 4)
+    # top-k finalize: the weighted rows, weights and indices in, the tokens out (+ the shared output read)
+    work["finalize"] = ("hbm", a * D * 2 + a * 8 + cfg.valid_tokens * D * 2 * (2 if layer.shared else 1))
     full = args.layer == "full"
     if full:
         Tv = cfg.valid_tokens
@@ -376,8 +405,9 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
         work["shared_w2"] = ("gemm", D * Hs * wb + Tv * Hs * wb + Tv * D * 2, 2.0 * Tv * D * Hs)
         # the routed combine adds into the shared expert's output: one more read of it
         comb = layer.combine_stage(names)
-        kind, *w = work[comb]
-        work[comb] = (kind, w[0] + Tv * D * 2, *w[1:])
+        if comb != "finalize":
+            kind, *w = work[comb]
+            work[comb] = (kind, w[0] + Tv * D * 2, *w[1:])
     peak_t = peaks["bf16_tflops_sustained"] * (FP8_OVER_BF16 if cfg.fp8 else 1.0)
     gemm_stages = [n for n in stage_ms if work[n][0] == "gemm"]
     stages = {}
@@ -418,6 +448,7 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
                 "synthetic, seeded: x~N(0,1), scores=bf16(sigmoid(N(0,1) logits)), expert weights N(0,0.02) random init",
         "config": {"workload": workload_desc(cfg) + (" + router + shared expert" if full else ""),
                    "layer": "router + shared expert + routed experts" if full else "routed experts",
+                   "weighting": args.weighting,
                    "T": cfg.T, "valid_tokens": cfg.valid_tokens, "D": D, "H": H,
                    "E": E, "top_k": k, "routed_rows": a, "active_experts": active,
                    "l2": "inputs larger than L2: each step streams the active experts' weights "
@@ -430,7 +461,9 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
         "e2e": None if e2e_ms is None else {
             "value": round(job_tokens_per_s(cfg.valid_tokens, world, e2e_ms), 1), "unit": UNIT,
             "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+            "method": "pinned host buffers, 2 slots: step i+1's H2D and step i-1's D2H on copy streams overlap "
+                      "step i's compute"},
         "gpu_launches": layer.kernel_launches(cfg.T, with_router=full) * args.steps,
         "clocks": clocks,
     }
@@ -554,6 +587,9 @@ def main(argv=None):
     p.add_argument("--layer", choices=["routed", "full"], default="routed",
                    help="routed: the routed-expert path from router scores; full: router scores, shared "
                         "expert and routed experts (the whole MoE layer)")
+    p.add_argument("--weighting", choices=["input", "output"], default="input",
+                   help="input: scores scale the expert inputs (gather*score); output: the top-k finalize weights "
+                        "the expert outputs")
     p.add_argument("--no-overlap", action="store_true",
                    help="full layer: run the shared expert on the main stream instead of a second one")
     p.add_argument("--cta-pairs", choices=["auto", "on", "off"], default="auto",
