@@ -331,7 +331,7 @@ class MoELayer:
 
     @staticmethod
     def _launch(name, f, events):
-        if events is None:
+        if events is None or name not in events:
             f()
             return
         s, e = events[name]
