@@ -165,3 +165,40 @@ def test_output_weighted_layer(name, with_shared):
     assert (err <= tol * rms(exp)).mean() >= 0.999
     if Tv < cfg.T:
         assert is_sentinel(out[Tv:])
+
+
+@pytest.mark.parametrize("name", ["tiny", "padded_fp8"])
+def test_output_weighted_layer_with_router(name):
+    """Router scores, the shared expert and output-side weighting together: the
+    routing decision is taken on the GPU's own scores on both sides."""
+    from moe_token_routing_index_gb300.forward import MoELayer
+
+    mb = _mb()
+    cfg = workloads.CONFIGS[name]
+    x = workloads.make_tokens(cfg)
+    w13, w2 = workloads.make_weights(cfg, device="cuda")
+    router = workloads.make_router(cfg).cuda()
+    sh = workloads.make_shared_weights(cfg, device="cuda")
+    layer = MoELayer.from_weights(cfg, w13, w2, router=router, shared=sh, weighting="output")
+    Tv = cfg.valid_tokens
+    nv = None if cfg.Tv is None else torch.tensor([Tv], dtype=torch.int32, device="cuda")
+    out = sentinel_like((cfg.T, cfg.D), torch.bfloat16)
+    layer(x.cuda(), None, nv, out=out)
+    torch.cuda.synchronize()
+    assert mb.device_error() == 0
+    scores = bits(layer.buffers(cfg.T, "cuda").extra["scores"])
+    rng = np.random.default_rng(4)
+    sample = np.arange(Tv) if Tv <= 64 else np.unique(np.concatenate([[0, Tv - 1], rng.integers(0, Tv, 10)]))
+    xs, ss = np.ascontiguousarray(bits(x)[sample]), np.ascontiguousarray(scores[sample])
+    conv = (lambda t: t.float().cpu().numpy()) if cfg.fp8 else bits
+    base = oracle.shared_expert(xs, conv(sh[0]), conv(sh[1]), fp8=cfg.fp8, scale_ub=cfg.scale_ub)
+    ref = oracle.moe_forward_output_weighted(xs, ss, cfg.top_k, _host_weights(cfg, w13, w2), fp8=cfg.fp8,
+                                             shared_out=base, scale_ub=cfg.scale_ub)["out"]
+    got = f64(bits(out[torch.from_numpy(sample).cuda()]))
+    exp = f64(ref)
+    tol = 6e-2 if cfg.fp8 else 2e-2
+    err = np.abs(got - exp)
+    assert np.all(err <= tol * rms(exp) + _bf16_step(exp)), err.max() / rms(exp)
+    assert (err <= tol * rms(exp)).mean() >= 0.999
+    if Tv < cfg.T:
+        assert is_sentinel(out[Tv:])
