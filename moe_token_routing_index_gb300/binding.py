@@ -104,11 +104,17 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
-def _need(t: torch.Tensor, dtype, name: str):
+def _need(t: torch.Tensor, dtype, name: str, contiguous: bool = True):
+    """dtype, device and layout checks of a matrix argument: the C ABI reads it as a
+    dense row-major array (contiguous=False: only the last dimension must be dense)."""
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if not contiguous and t.dim() > 0 and t.stride(-1) != 1:
+        raise ValueError(f"{name} must be dense along its last dimension")
 
 
 def device_error(stream=None) -> int:
@@ -137,6 +143,7 @@ def moe_router_scores(x: torch.Tensor, w_router: torch.Tensor, num_valid_tokens:
         _need(num_valid_tokens, torch.int32, "num_valid_tokens")
     if out is None:
         out = torch.empty(T, E, dtype=torch.bfloat16, device=x.device)
+    _need(out, out.dtype, "out")
     ws_bytes = moe_router_workspace_size(T, D, E)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=x.device)
@@ -203,6 +210,7 @@ def moe_gather_scale(x, token_indices, expert_indices, scores, valid_token_count
     _need(x, torch.bfloat16, "x")
     if out is None:
         out = torch.empty(a, D, dtype=x.dtype, device=x.device)
+    _need(out, out.dtype, "out")
     st = _lib.moe_gather_scale(_ptr(x), T, D, _ptr(token_indices), _ptr(expert_indices), a, *_scores_args(scores),
                                _ptr(valid_token_count), _ptr(inv_rows), top_k, _ptr(out), _stream(stream))
     _check("moe_gather_scale", st)
@@ -216,8 +224,10 @@ def moe_gather_scale_quant(x, token_indices, expert_indices, scores, scale_ub=No
     _need(x, torch.bfloat16, "x")
     if out is None:
         out = torch.empty(a, D, dtype=torch.float8_e4m3fn, device=x.device)
+    _need(out, out.dtype, "out")
     if out_scale is None:
         out_scale = torch.empty(a, dtype=torch.float32, device=x.device)
+    _need(out_scale, out_scale.dtype, "out_scale")
     st = _lib.moe_gather_scale_quant(_ptr(x), T, D, _ptr(token_indices), _ptr(expert_indices), a,
                                      *_scores_args(scores),
                                      _ptr(valid_token_count), _ptr(inv_rows), top_k, _ptr(scale_ub), _ptr(out),
@@ -233,8 +243,10 @@ def moe_quantize_rows(w: torch.Tensor, scale_ub=None, *, out=None, out_scale=Non
     rows = w.numel() // cols if cols else 0
     if out is None:
         out = torch.empty(w.shape, dtype=torch.float8_e4m3fn, device=w.device)
+    _need(out, out.dtype, "out")
     if out_scale is None:
         out_scale = torch.empty(w.shape[:-1], dtype=torch.float32, device=w.device)
+    _need(out_scale, out_scale.dtype, "out_scale")
     st = _lib.moe_quantize_rows(_ptr(w), rows, cols, _ptr(scale_ub), _ptr(out), _ptr(out_scale), _stream(stream))
     _check("moe_quantize_rows", st)
     return out, out_scale
@@ -263,6 +275,7 @@ def moe_grouped_gemm(x, w, counts, *, epilogue: int = MOE_EPILOGUE_NONE, out=Non
     si, t_out, acc = _scatter_args(scatter_indices, out, accumulate)
     if out is None:
         out = torch.empty(a_max, n_out, dtype=torch.bfloat16, device=x.device)
+    _need(out, out.dtype, "out")
     st = _lib.moe_grouped_gemm(_ptr(x), _ptr(w), _ptr(counts), E, a_max, N, K, _ptr(out), epilogue, _ptr(si),
                                t_out, acc, _stream(stream))
     _check("moe_grouped_gemm", st)
@@ -280,6 +293,7 @@ def moe_grouped_gemm_fp8_rowwise(x, w, counts, x_scale, w_scale, *, epilogue: in
     si, t_out, acc = _scatter_args(scatter_indices, out, accumulate)
     if out is None:
         out = torch.empty(a_max, n_out, dtype=torch.bfloat16, device=x.device)
+    _need(out, out.dtype, "out")
     st = _lib.moe_grouped_gemm_fp8_rowwise(_ptr(x), _ptr(w), _ptr(counts), _ptr(x_scale), _ptr(w_scale), E, a_max,
                                            N, K, _ptr(out), epilogue, _ptr(si), t_out, acc, _stream(stream))
     _check("moe_grouped_gemm_fp8_rowwise", st)
@@ -304,9 +318,11 @@ def moe_expert_mlp(x, w13, w2, counts, *, z=None, out=None, scatter_indices=None
         _need(t, torch.bfloat16, n)
     if z is None:
         z = torch.empty(a_max, H, dtype=torch.bfloat16, device=x.device)
+    _need(z, z.dtype, "z")
     si, t_out, acc = _scatter_args(scatter_indices, out, accumulate)
     if out is None:
         out = torch.empty(a_max, D, dtype=torch.bfloat16, device=x.device)
+    _need(out, out.dtype, "out")
     if workspace is None:
         workspace = torch.empty(moe_expert_mlp_workspace_size(E), dtype=torch.uint8, device=x.device)
     st = _lib.moe_expert_mlp(_ptr(x), _ptr(w13), _ptr(w2), _ptr(counts), E, a_max, D, H, _ptr(z), _ptr(out),
@@ -321,9 +337,10 @@ def moe_silu_mul(y, H: int | None = None, valid_rows=None, *, out=None, stream=N
     """y[a, 2H] bf16 -> z[a, H] = silu(y[:, :H]) * y[:, H:]."""
     a, n2 = y.shape
     H = n2 // 2 if H is None else H
-    _need(y, torch.bfloat16, "y")
+    _need(y, torch.bfloat16, "y", contiguous=False)
     if out is None:
         out = torch.empty(a, H, dtype=torch.bfloat16, device=y.device)
+    _need(out, out.dtype, "out")
     x1 = ctypes.c_void_p(y.data_ptr() + H * y.element_size())
     st = _lib.moe_silu_mul(_ptr(y), x1, y.stride(0), a, H, _ptr(valid_rows), _ptr(out), _stream(stream))
     _check("moe_silu_mul", st)
@@ -334,11 +351,13 @@ def moe_silu_mul_quant(y, H: int | None = None, scale_ub=None, valid_rows=None, 
                        stream=None):
     a, n2 = y.shape
     H = n2 // 2 if H is None else H
-    _need(y, torch.bfloat16, "y")
+    _need(y, torch.bfloat16, "y", contiguous=False)
     if out is None:
         out = torch.empty(a, H, dtype=torch.float8_e4m3fn, device=y.device)
+    _need(out, out.dtype, "out")
     if out_scale is None:
         out_scale = torch.empty(a, dtype=torch.float32, device=y.device)
+    _need(out_scale, out_scale.dtype, "out_scale")
     x1 = ctypes.c_void_p(y.data_ptr() + H * y.element_size())
     st = _lib.moe_silu_mul_quant(_ptr(y), x1, y.stride(0), a, H, _ptr(valid_rows), _ptr(scale_ub), _ptr(out),
                                  _ptr(out_scale), _stream(stream))
@@ -390,6 +409,7 @@ def moe_topk_finalize(rows, expert_weights, expanded_idx_to_permuted_idx, shared
         _need(shared_output, torch.bfloat16, "shared_output")
     if out is None:
         out = torch.empty(M, D, dtype=torch.bfloat16, device=rows.device)
+    _need(out, out.dtype, "out")
     st = _lib.moe_topk_finalize(_ptr(rows), n_rows, D, _ptr(expert_weights), _dtype_code(expert_weights),
                                 _ptr(expanded_idx_to_permuted_idx), M, k, _ptr(valid_token_count),
                                 _ptr(shared_output), _ptr(out), _stream(stream))

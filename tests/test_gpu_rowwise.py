@@ -200,3 +200,18 @@ def test_token_major_gather_equals_row_major(name, quant):
         np.testing.assert_array_equal(bits(o1[:a]), ref)
         assert is_sentinel(o1[a:])
     assert mb.device_error() == 0
+
+
+def test_binding_rejects_strided_matrices():
+    mb = _mb()
+    x = torch.randn(64, 32, device="cuda").to(torch.bfloat16).t()        # a transposed view: not row-major
+    ti = torch.zeros(4, dtype=torch.int32, device="cuda")
+    s = torch.rand(32, 2, device="cuda")
+    with pytest.raises(ValueError):
+        mb.moe_gather_scale(x, ti, ti, s)
+    y = torch.randn(8, 64, device="cuda").to(torch.bfloat16)
+    with pytest.raises(ValueError):
+        mb.moe_silu_mul(y, 16, out=torch.empty(16, 8, dtype=torch.bfloat16, device="cuda").t())
+    # rows of y may be strided (the ABI takes the row stride): a column slice is accepted
+    z = mb.moe_silu_mul(torch.randn(8, 96, device="cuda").to(torch.bfloat16)[:, :64], 32)
+    assert z.shape == (8, 32) and mb.device_error() == 0
