@@ -12,6 +12,7 @@
  *   moe_gather_scale_quant    ... and quantise each row to FP8 (e4m3)
  *   moe_grouped_gemm          per-expert GEMM with w13 or w2 (bf16)
  *   moe_grouped_gemm_fp8_rowwise   the same on e4m3 operands with row scales
+ *   moe_dense_gemm            split-K dense GEMM (the shared expert of small batches)
  *   moe_silu_mul(_quant)      z = silu(y0) * y1 (and FP8 quantisation)
  *   moe_scatter_add           add routed rows back into token order
  *   moe_scatter_add_padded    the same for the padded-token layout (counts per expert)
@@ -317,6 +318,26 @@ int moe_expert_mlp_workspace_size(int E, size_t* bytes);
 int moe_expert_mlp(const void* x, const void* w13, const void* w2, const int32_t* counts, int E, int a_max,
                    int D, int H, void* z, void* y, const int32_t* scatter_indices, int T_out, int accumulate,
                    void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------ dense GEMM (shared expert) */
+
+/*
+ * The shared expert's dense GEMMs of mslk/moe/layers.py
+ * (MetaShufflingMoE._shared_expert_part1 / _part2: x @ w13.T, then z @ w2.T)
+ * for batches with few row tiles: the K dimension is split across the CTAs of
+ * a thread-block cluster and the fp32 partials are added in a fixed order over
+ * distributed shared memory, so more SMs stream the weights.
+ *   v[r, n] = sum_k x[r, k] * w[n, k]                   (fp32)
+ *   MOE_EPILOGUE_NONE:     y [M, N] bf16, y[r, n] = bf16(v[r, n])
+ *   MOE_EPILOGUE_SILU_MUL: N = 2H, y [M, H] bf16,
+ *                          y[r, j] = bf16(silu_mul(bf16(v[r, j]), bf16(v[r, H + j])))
+ *                          (the grouped GEMM's SiLU*mul epilogue)
+ * x [M, K], w [N, K] bf16, row-major, 16-byte aligned; valid_rows: device int32
+ * row count (NULL: M), rows at or past it are not written.  K, N multiples of
+ * 16 (MOE_ERR_UNSUPPORTED).  Deterministic on a given device.
+ */
+int moe_dense_gemm(const void* x, int M, int K, const void* w, int N, const int32_t* valid_rows,
+                   void* y, int epilogue, cudaStream_t stream);
 
 /* ---------------------------------------------------------------- silu_mul */
 

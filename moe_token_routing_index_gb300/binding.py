@@ -47,6 +47,7 @@ def _load() -> ctypes.CDLL:
         "moe_device_error": ([U, P], I),
         "moe_router_workspace_size": ([I, I, I, ctypes.POINTER(S)], I),
         "moe_router_scores": ([P, I, I, P, I, P, P, P, S, P], I),
+        "moe_dense_gemm": ([P, I, I, P, I, P, P, I, P], I),
         "moe_route_workspace_size": ([I, I, I, ctypes.POINTER(S)], I),
         "moe_route": ([P, I, L, L, I, I, I, P, P, P, P, P, P, P, P, S, P], I),
         "moe_route_no_alloc": ([P, I, L, L, I, I, I, P, P, P, P, P, P, P], I),
@@ -414,4 +415,23 @@ def moe_topk_finalize(rows, expert_weights, expanded_idx_to_permuted_idx, shared
                                 _ptr(expanded_idx_to_permuted_idx), M, k, _ptr(valid_token_count),
                                 _ptr(shared_output), _ptr(out), _stream(stream))
     _check("moe_topk_finalize", st)
+    return out
+
+
+def moe_dense_gemm(x, w, valid_rows=None, *, epilogue: int = MOE_EPILOGUE_NONE, out=None, stream=None):
+    """y = x[M, K] @ w[N, K]^T (bf16, split-K over a cluster); with the SiLU*mul
+    epilogue y[M, N/2] = silu_mul of the two halves."""
+    M, K = x.shape
+    N, K2 = w.shape
+    assert K == K2
+    _need(x, torch.bfloat16, "x")
+    _need(w, torch.bfloat16, "w")
+    if valid_rows is not None:
+        _need(valid_rows, torch.int32, "valid_rows")
+    n_out = N // 2 if epilogue == MOE_EPILOGUE_SILU_MUL else N
+    if out is None:
+        out = torch.empty(M, n_out, dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, "out")
+    st = _lib.moe_dense_gemm(_ptr(x), M, K, _ptr(w), N, _ptr(valid_rows), _ptr(out), epilogue, _stream(stream))
+    _check("moe_dense_gemm", st)
     return out

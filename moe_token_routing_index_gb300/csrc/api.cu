@@ -171,6 +171,20 @@ int moe_router_scores(const void* x, int T, int D, const void* w_router, int E, 
   return finish(moe::launch_router_scores(a, stream));
 }
 
+int moe_dense_gemm(const void* x, int M, int K, const void* w, int N, const int32_t* valid_rows, void* y,
+                   int epilogue, cudaStream_t stream) {
+  if (M < 0 || K < 0 || N < 0) return MOE_ERR_INVALID;
+  if (epilogue != MOE_EPILOGUE_NONE && epilogue != MOE_EPILOGUE_SILU_MUL) return MOE_ERR_INVALID;
+  if (M == 0 || N == 0) return MOE_OK;
+  if (!x || !w || !y) return MOE_ERR_INVALID;
+  if (K == 0 || K % 16 != 0 || N % 16 != 0) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(w) || (reinterpret_cast<uintptr_t>(y) & 1u)) return MOE_ERR_UNSUPPORTED;
+  moe::DenseArgs a{x, M, K, w, N, epilogue, valid_rows, y, nullptr};
+  int rc = device_error_word(&a.err);
+  if (rc != MOE_OK) return rc;
+  return finish(moe::launch_dense_gemm(a, stream));
+}
+
 static int check_gather(const void* x, int T, int D, const int32_t* ti, const int32_t* ei, int a,
                         const void* scores, int dtype, int E, const void* out) {
   if (T < 0 || D < 0 || a < 0) return MOE_ERR_INVALID;

@@ -41,6 +41,19 @@ struct RouterArgs {
 size_t router_workspace_bytes(int T, int D, int E);
 cudaError_t launch_router_scores(const RouterArgs& a, cudaStream_t s);
 
+struct DenseArgs {
+  const void* x;             // bf16 [M, K]
+  int M, K;
+  const void* w;             // bf16 [N, K]
+  int N;
+  int epilogue;              // MOE_EPILOGUE_NONE or MOE_EPILOGUE_SILU_MUL
+  const int32_t* rows_valid; // nullable: M
+  void* y;                   // bf16 [M, N] or [M, N / 2]
+  unsigned int* err;
+};
+
+cudaError_t launch_dense_gemm(const DenseArgs& a, cudaStream_t s);
+
 struct GatherArgs {
   const void* x;
   int T, D;

@@ -11,7 +11,9 @@ Stage order of mslk/moe/layers.py, MetaShufflingMoE._no_comm_forward:
          (FP8 rowwise) -> silu_mul_quant -> grouped GEMM w2 (FP8 rowwise) -> scatter-add
   shared expert (optional): the same MLP over every valid token (one expert,
          unit scores) written into the output first; the routed combine then
-         adds into it, as _routed_expert does with shared_output.
+         adds into it, as _routed_expert does with shared_output.  Small bf16
+         batches use the split-K dense GEMMs (moe_dense_gemm), the others the
+         grouped kernels with one expert.
 
 With top_k = 1 the scatter-add is fused into the w2 GEMM's epilogue (each
 routed row owns its token), as _routed_expert does with _scatter_add_indices.
@@ -221,6 +223,13 @@ class MoELayer:
         # accumulate: the shared rows are added into out (row t to token t)
         add = dict(scatter_indices=ex["ident"], accumulate=True) if accumulate else {}
         if not self.fp8:
+            if T <= 256 and not accumulate:
+                # few row tiles: split the weights' K dimension over clusters so that every SM streams
+                return [
+                    ("shared_w13_silu", lambda: mb.moe_dense_gemm(x, self.sw13[0], rows,
+                                                                  epilogue=mb.MOE_EPILOGUE_SILU_MUL, out=ex["sh_z"])),
+                    ("shared_w2", lambda: mb.moe_dense_gemm(ex["sh_z"], self.sw2[0], rows, out=out)),
+                ]
             if T <= 128:
                 return [("shared_mlp", lambda: mb.moe_expert_mlp(x, self.sw13, self.sw2, rows, z=ex["sh_z"], out=out,
                                                                  workspace=ex["sh_mlp_ws"], **add))]
@@ -375,5 +384,5 @@ class MoELayer:
         if with_router:
             n += 1
         if self.shared:
-            n += 4 if self.fp8 else (1 if T <= 128 else 2)
+            n += 4 if self.fp8 else 2
         return n

@@ -311,3 +311,31 @@ def test_grouped_gemm_cta_pairs(E, counts, N, K, a_max, fp8):
         assert mb.device_error() == 0
         assert torch.equal(z[:a], mb.moe_silu_mul(y[:a].contiguous(), N // 2))
         assert is_sentinel(z[a:])
+
+
+@pytest.mark.parametrize("M,K,N,valid", [(128, 5120, 16384, 128), (128, 8192, 5120, 128), (200, 1024, 512, 170),
+                                         (1, 256, 64, 1), (300, 4096, 2048, 300), (64, 16, 48, 64)])
+def test_dense_splitk_gemm(M, K, N, valid):
+    """moe_dense_gemm (K split over a cluster, partials added in rank order): the plain
+    output within the oracle bound on sampled columns; the SiLU*mul epilogue equal to
+    moe_silu_mul of the plain output bit for bit (same tiles, same split, same sums)."""
+    mb = _mb()
+    g = torch.Generator().manual_seed(M + K + N)
+    x = torch.randn(M, K, generator=g).to(torch.bfloat16)
+    w = (torch.randn(N, K, generator=g) * 0.05).to(torch.bfloat16)
+    vr = torch.tensor([valid], dtype=torch.int32, device="cuda")
+    y = sentinel_like((M, N), torch.bfloat16)
+    mb.moe_dense_gemm(x.cuda(), w.cuda(), vr, out=y)
+    assert mb.device_error() == 0
+    cols = np.unique(np.random.default_rng(N).integers(0, N, min(N, 384)))
+    ref = oracle.grouped_gemm_bf16(bits(x[:valid]), bits(w)[cols][None], np.array([valid], np.int32))
+    _check_close(bits(y[:valid])[:, cols], ref, _abs_bound_bf16(bits(x[:valid]), bits(w)[cols][None], [valid]))
+    assert is_sentinel(y[valid:])
+    if N % 32 == 0:
+        H = N // 2
+        z = sentinel_like((M, H), torch.bfloat16)
+        mb.moe_dense_gemm(x.cuda(), w.cuda(), vr, epilogue=mb.MOE_EPILOGUE_SILU_MUL, out=z)
+        z_ref = mb.moe_silu_mul(y[:valid].contiguous(), H)
+        assert mb.device_error() == 0
+        assert torch.equal(z[:valid], z_ref)
+        assert is_sentinel(z[valid:])
