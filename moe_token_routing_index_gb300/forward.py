@@ -361,6 +361,23 @@ class MoELayer:
         self.run(self.stages(x, scores, num_valid_tokens, out, accumulate))
         return out
 
+    def capture(self, x: torch.Tensor, scores: torch.Tensor | None = None,
+                num_valid_tokens: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                accumulate: bool = False):
+        """Record one forward on these device tensors into a CUDA graph (stages,
+        the second stream of the shared expert and its events included).  Returns
+        (graph, out): graph.replay() reruns the forward on the tensors' current
+        contents with no host-side launch work."""
+        if out is None:
+            out = torch.zeros(x.shape[0], self.D, dtype=torch.bfloat16, device=x.device)
+        stages = self.stages(x, scores, num_valid_tokens, out, accumulate)
+        self.run(stages)              # resolves the per-device lookups and kernel attributes outside the capture
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            self.run(stages)
+        return graph, out
+
     def use_fused_mlp(self, T: int) -> bool:
         if self.fp8:
             return False

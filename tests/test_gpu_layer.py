@@ -126,3 +126,34 @@ def test_layer_overlap_equals_serial(name):
     layer.overlap_shared = True
     o3 = _forward(cfg, layer, x)
     assert torch.equal(o1, o3)
+
+
+@pytest.mark.parametrize("name,full", [("tiny", True), ("decode", False), ("decode", True), ("padded_fp8", True),
+                                       ("fine_grained", False), ("prefill_fp8", False)])
+def test_cuda_graph_replay_equals_eager(name, full):
+    """A captured forward (CUDA graph, with the shared expert's second stream) replays to
+    the eager forward's bytes, and follows new input contents."""
+    from moe_token_routing_index_gb300 import binding as mb
+    from moe_token_routing_index_gb300.forward import MoELayer
+
+    cfg = workloads.CONFIGS[name]
+    x = workloads.make_tokens(cfg).cuda()
+    s = None if full else workloads.make_scores(cfg).cuda()
+    w13, w2 = workloads.make_weights(cfg, device="cuda")
+    kw = dict(router=workloads.make_router(cfg).cuda(), shared=workloads.make_shared_weights(cfg, device="cuda")) \
+        if full else {}
+    layer = MoELayer.from_weights(cfg, w13, w2, **kw)
+    nv = None if cfg.Tv is None else torch.tensor([cfg.Tv], dtype=torch.int32, device="cuda")
+    eager = layer(x, s, nv).clone()
+    graph, out = layer.capture(x, s, nv)
+    out.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert mb.device_error() == 0
+    assert torch.equal(out, eager)
+    x2 = workloads.make_tokens(cfg, seed=1).cuda()
+    eager2 = layer(x2, s, nv).clone()
+    x.copy_(x2)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager2)
