@@ -80,20 +80,34 @@ __device__ void route_select_chunk(int c, const void* __restrict__ scores, int d
 }
 
 // Block-wide exclusive scan of one value per thread; returns the thread's
-// exclusive prefix, and the total in *total.
+// exclusive prefix, and the total in *total.  Two levels of warp shuffles: each
+// warp scans its 32 values, warp 0 scans the 32 warp totals (s_part[0..32]).
 __device__ __forceinline__ int block_exclusive_scan(int v, int* s_part, int* total) {
-  s_part[threadIdx.x] = v;
-  __syncthreads();
-  for (int o = 1; o < kRouteThreads; o <<= 1) {  // Hillis-Steele inclusive scan
-    const int u = threadIdx.x >= o ? s_part[threadIdx.x - o] : 0;
-    __syncthreads();
-    s_part[threadIdx.x] += u;
-    __syncthreads();
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
   }
-  const int incl = s_part[threadIdx.x];
-  *total = s_part[kRouteThreads - 1];
+  if (lane == 31) s_part[w] = incl;
   __syncthreads();
-  return incl - v;
+  if (w == 0) {
+    const int x = lane < kWarps ? s_part[lane] : 0;
+    int xi = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, xi, o);
+      if (lane >= o) xi += t;
+    }
+    s_part[lane] = xi - x;           // the warps' exclusive bases
+    if (lane == 31) s_part[32] = xi;  // the block total
+  }
+  __syncthreads();
+  const int excl = incl - v + s_part[w];
+  *total = s_part[32];
+  __syncthreads();  // s_part may be reused once every thread has read it
+  return excl;
 }
 
 // Phase 2 for expert e: exclusive scan of hist_t[e, 0..nblk) in place; counts[e] = total.
