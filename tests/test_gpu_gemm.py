@@ -66,6 +66,8 @@ SHAPES = [
     (2, [77, 200], 512, 320, None),     # several N tiles and K blocks
     (4, [1, 0, 0, 129], 48, 80, 300),   # partial N tile, K tail, rows past the counts
     (5, [300, 17, 0, 64, 250], 1040, 272, 700),
+    # the largest expert count: 1024 experts, most of them empty or with a few rows
+    (1024, [int(c) for c in np.random.default_rng(1024).choice([0, 0, 0, 1, 3, 130], 1024)], 64, 64, None),
 ]
 
 
@@ -266,6 +268,7 @@ PAIR_SHAPES = [
     (3, [5, 0, 130], 256, 64, None),
     (4, [1, 0, 0, 383], 48, 80, 500),
     (5, [300, 17, 0, 640, 250], 1040, 272, 1300),
+    (1024, [int(c) for c in np.random.default_rng(1025).choice([0, 0, 0, 2, 257], 1024)], 64, 64, None),
 ]
 
 
