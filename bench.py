@@ -132,6 +132,26 @@ def _layer_weights_host(cfg, router, shared):
     return _host_bits(router), sh
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), best effort."""
+    import subprocess
+
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
 def oracle_tokens_per_s(cfg, x, s, w13, w2, seconds: float, max_tokens: int | None = None, layer=None):
     """Time the oracle's forward (as it stands) on a bounded sample of tokens.
 
@@ -261,8 +281,8 @@ def run_ours(args, cfg):
                for n in names if only in (None, n)} for _ in range(n_steps)]
         return ev
 
-    def stage_means(ev):
-        return {n: statistics.fmean(e[n][0].elapsed_time(e[n][1]) for e in ev) for n in ev[0]}
+    def stage_means(ev):  # the median over the steps of each stage's event time
+        return {n: statistics.median(e[n][0].elapsed_time(e[n][1]) for e in ev) for n in ev[0]}
 
     # the dominant stage, from a short pass with events around every stage
     pre = stage_pass(min(args.warmup, 5))
@@ -330,6 +350,7 @@ def run_ours(args, cfg):
             tps, n, cores, dt = oracle_tokens_per_s(cfg, x, s, w13, w2, args.cpu_seconds,
                                                     layer=_layer_weights_host(cfg, router, shared))
             result["cpu_baseline"] = {"value": round(tps, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+                                      "cpu": cpu_model(),
                                       "sample": f"first {n} valid tokens of the workload (repeated to {dt:.1f} s of wall time)"}
         print(json.dumps(result), flush=True)
     if world > 1:
@@ -609,6 +630,7 @@ def run_reference(args, cfg):
         "config": {"workload": workload_desc(cfg) + (" + router + shared expert" if layer else ""),
                    "sample_tokens_per_step": n_step},
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                         "cpu": cpu_model(),
                          "sample": f"{n_step} valid tokens per step (of {Tv}), tokens cycling through the workload"},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
