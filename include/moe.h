@@ -124,6 +124,21 @@ int moe_router_scores(const void* x, int T, int D, const void* w_router, int E,
                       const int32_t* num_valid_tokens, void* scores, void* ws, size_t ws_bytes,
                       cudaStream_t stream);
 
+/* ------------------------------------------------------------- diagnostics */
+
+/*
+ * Exercises one of the library's bounded device-side waits against a
+ * condition that never comes true, so that a caller (or a test) can see the
+ * failure path work without a GPU fault: which = 0 waits on an mbarrier phase
+ * that no one completes (the wait of every TMA/tensor-core pipeline here);
+ * which = 1 runs a cooperative grid whose last block skips the grid barrier
+ * (the barrier of the cooperative routing kernel).  The wait gives up after
+ * limit_ns (1 us .. 2 s) of the device's global timer, records
+ * MOE_DEVERR_TIMEOUT (read it with moe_device_error) and returns; the context
+ * stays usable.  Returns MOE_ERR_INVALID for other arguments.
+ */
+int moe_selftest_bounded_wait(int which, int64_t limit_ns, cudaStream_t stream);
+
 /* ------------------------------------------------------------------ routing */
 
 /*

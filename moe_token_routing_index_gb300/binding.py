@@ -48,6 +48,7 @@ def _load() -> ctypes.CDLL:
         "moe_router_workspace_size": ([I, I, I, ctypes.POINTER(S)], I),
         "moe_router_scores": ([P, I, I, P, I, P, P, P, S, P], I),
         "moe_dense_gemm": ([P, I, I, P, I, P, P, I, P], I),
+        "moe_selftest_bounded_wait": ([I, L, P], I),
         "moe_route_workspace_size": ([I, I, I, ctypes.POINTER(S)], I),
         "moe_route": ([P, I, L, L, I, I, I, P, P, P, P, P, P, P, P, S, P], I),
         "moe_route_no_alloc": ([P, I, L, L, I, I, I, P, P, P, P, P, P, P], I),
@@ -435,3 +436,10 @@ def moe_dense_gemm(x, w, valid_rows=None, *, epilogue: int = MOE_EPILOGUE_NONE, 
     st = _lib.moe_dense_gemm(_ptr(x), M, K, _ptr(w), N, _ptr(valid_rows), _ptr(out), epilogue, _stream(stream))
     _check("moe_dense_gemm", st)
     return out
+
+
+def moe_selftest_bounded_wait(which: int, limit_ns: int = 20_000_000, stream=None) -> int:
+    """Run a bounded device wait that never succeeds (0: mbarrier, 1: grid barrier);
+    returns the device error bits afterwards (MOE_DEVERR_TIMEOUT expected)."""
+    _check("moe_selftest_bounded_wait", _lib.moe_selftest_bounded_wait(which, limit_ns, _stream(stream)))
+    return device_error(stream)

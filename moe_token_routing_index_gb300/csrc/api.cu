@@ -185,6 +185,15 @@ int moe_dense_gemm(const void* x, int M, int K, const void* w, int N, const int3
   return finish(moe::launch_dense_gemm(a, stream));
 }
 
+int moe_selftest_bounded_wait(int which, int64_t limit_ns, cudaStream_t stream) {
+  if (which != 0 && which != 1) return MOE_ERR_INVALID;
+  if (limit_ns < 1000 || limit_ns > 2000000000ll) return MOE_ERR_INVALID;
+  unsigned int* err = nullptr;
+  int rc = device_error_word(&err);
+  if (rc != MOE_OK) return rc;
+  return finish(moe::launch_selftest_wait(which, (uint64_t)limit_ns, err, stream));
+}
+
 static int check_gather(const void* x, int T, int D, const int32_t* ti, const int32_t* ei, int a,
                         const void* scores, int dtype, int E, const void* out) {
   if (T < 0 || D < 0 || a < 0) return MOE_ERR_INVALID;

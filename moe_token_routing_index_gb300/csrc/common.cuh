@@ -30,6 +30,40 @@ __device__ __forceinline__ int read_count(const int32_t* p, int hi, unsigned int
   return v;
 }
 
+// Grid-wide barrier of a cooperative launch: every block arrives once per
+// barrier on a counter that starts at 0, so barrier n completes at n * grid
+// arrivals.  The wait is bounded (limit_ns of %globaltimer, 1 s by default);
+// false means it gave up.  Called by every thread of the block.
+__device__ __forceinline__ bool grid_barrier(unsigned int* counter, unsigned int target,
+                                             uint64_t limit_ns = 1000000000ull) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(counter, 1u);
+    uint64_t t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    int ok = 1;
+    for (uint32_t i = 0;; ++i) {
+      unsigned int v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+      if (v >= target) break;
+      if ((i & 63) == 63) {
+        uint64_t t1;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+        if (t1 - t0 > limit_ns) {
+          ok = 0;
+          break;
+        }
+      }
+    }
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
 // A routing score; NULL scores read as 1.0 (the gathers then copy rows unscaled).
 __device__ __forceinline__ float load_score(const void* scores, int dtype, int64_t off) {
   if (!scores) return 1.0f;

@@ -54,6 +54,8 @@ struct DenseArgs {
 
 cudaError_t launch_dense_gemm(const DenseArgs& a, cudaStream_t s);
 
+cudaError_t launch_selftest_wait(int which, uint64_t limit_ns, unsigned int* err, cudaStream_t s);
+
 struct GatherArgs {
   const void* x;
   int T, D;

@@ -164,38 +164,6 @@ __device__ void route_emit_chunk(int c, int E, int k, int Tv, const int32_t* __r
   __syncthreads();
 }
 
-// Grid-wide barrier of a cooperative launch: every block arrives once per
-// barrier on a counter that starts at 0, so barrier n completes at n * grid
-// arrivals.  The wait is bounded (1 s); false means it gave up.
-__device__ bool grid_barrier(unsigned int* counter, unsigned int target) {
-  __shared__ int s_ok;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(counter, 1u);
-    uint64_t t0;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-    int ok = 1;
-    for (uint32_t i = 0;; ++i) {
-      unsigned int v;
-      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
-      if (v >= target) break;
-      if ((i & 63) == 63) {
-        uint64_t t1;
-        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
-        if (t1 - t0 > 1000000000ull) {
-          ok = 0;
-          break;
-        }
-      }
-    }
-    __threadfence();
-    s_ok = ok;
-  }
-  __syncthreads();
-  return s_ok != 0;
-}
-
 template <int EPL>
 __global__ void __launch_bounds__(kRouteThreads) route_coop_kernel(
     const void* __restrict__ scores, int dtype, int64_t st, int64_t se, int T, int E, int k,

@@ -99,3 +99,7 @@ def test_host_side_validation_without_gpu(lib):
     assert L.moe_scatter_add_padded(fake, fake, fake, 8, fake, None, 1, 30, 8, 32, 1, None) == lib.MOE_ERR_INVALID
     assert L.moe_scatter_add_padded(fake, fake, None, 8, fake, None, 1, 32, 8, 32, 1, None) == lib.MOE_ERR_INVALID
     assert L.moe_scatter_add_padded(fake, fake, fake, 8, fake, None, 2, 32, 16, 32, 1, None) == lib.MOE_ERR_INVALID
+    # bounded-wait self-test: unknown mode, limits outside [1 us, 2 s]
+    assert L.moe_selftest_bounded_wait(2, 1000000, None) == lib.MOE_ERR_INVALID
+    assert L.moe_selftest_bounded_wait(0, 10, None) == lib.MOE_ERR_INVALID
+    assert L.moe_selftest_bounded_wait(1, 3000000000, None) == lib.MOE_ERR_INVALID
