@@ -539,7 +539,7 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
 TRAFFIC: dict = {
     ("decode", "expert_mlp"): (4_037_355_000 + 6_043_648, "grouped_gemm.cu", "f796cfcae1f4"),
     ("prefill_fp8", "gemm_w13"): (1_385_569_000 + 249_881_344, "grouped_gemm.cu", "f796cfcae1f4"),
-    ("padded_fp8", "gather_quant"): (93_180_672 + 118_366_720, "rowwise.cu", "d196775be574"),
+    ("padded_fp8", "gather_quant"): (93_188_096 + 118_469_888, "rowwise.cu", "b3c96b709583"),
 }
 
 
