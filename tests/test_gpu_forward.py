@@ -130,3 +130,46 @@ def test_forward_cta_pair_tiles_change_no_bit(name):
     torch.cuda.synchronize()
     assert mb.device_error() == 0
     assert torch.equal(outs[0], outs[1])
+
+
+@pytest.mark.parametrize("name,with_shared", [("tiny", False), ("tiny", True), ("decode", False),
+                                              ("fine_grained", False), ("padded_fp8", True)])
+def test_forward_accumulates_into_existing_output(name, with_shared):
+    """accumulate=True adds the layer into out (a residual, say): the shared rows are added
+    into out first (fp32 sum, one rounding), then the routed rows, as the oracle's combine
+    adds them into its starting output."""
+    from moe_token_routing_index_gb300 import binding as mb
+    from moe_token_routing_index_gb300.forward import MoELayer
+
+    cfg = workloads.CONFIGS[name]
+    x = workloads.make_tokens(cfg)
+    s = workloads.make_scores(cfg)
+    w13, w2 = workloads.make_weights(cfg, device="cuda")
+    sh = workloads.make_shared_weights(cfg, device="cuda") if with_shared else None
+    layer = MoELayer.from_weights(cfg, w13, w2, shared=sh)
+    g = torch.Generator().manual_seed(11)
+    init = torch.randn(cfg.T, cfg.D, generator=g).to(torch.bfloat16)
+    out = init.cuda()
+    nv = None if cfg.Tv is None else torch.tensor([cfg.Tv], dtype=torch.int32, device="cuda")
+    layer(x.cuda(), s.cuda(), nv, out=out, accumulate=True)
+    torch.cuda.synchronize()
+    assert mb.device_error() == 0
+    Tv = cfg.valid_tokens
+    rng = np.random.default_rng(6)
+    sample = np.arange(Tv) if Tv <= 64 else np.unique(np.concatenate([[0, Tv - 1], rng.integers(0, Tv, 10)]))
+    base = bits(init)[sample]
+    if sh is not None:
+        conv = (lambda t: t.float().cpu().numpy()) if cfg.fp8 else bits
+        shared = oracle.shared_expert(np.ascontiguousarray(bits(x)[sample]), conv(sh[0]), conv(sh[1]), fp8=cfg.fp8,
+                                      scale_ub=cfg.scale_ub)
+        base = bits((torch.from_numpy(f64(base)).float() + torch.from_numpy(f64(shared)).float()).to(torch.bfloat16))
+    ref, _ = oracle.moe_forward_tokens(sample, bits(x), bits(s), cfg.top_k, _weights_fn(cfg, w13, w2), fp8=cfg.fp8,
+                                       out_init=None, scale_ub=cfg.scale_ub)
+    res = oracle.moe_forward(np.ascontiguousarray(bits(x)[sample]), np.ascontiguousarray(bits(s)[sample]), cfg.top_k,
+                             _weights_fn(cfg, w13, w2), fp8=cfg.fp8, out_init=np.ascontiguousarray(base),
+                             scale_ub=cfg.scale_ub)
+    got = f64(bits(out[torch.from_numpy(sample).cuda()]))
+    _assert_close(got, f64(res["out"]), _tol(cfg))
+    assert rms(f64(res["out"]) - f64(ref)) > 0              # the starting output did take part
+    if Tv < cfg.T:
+        assert torch.equal(out[Tv:].cpu(), init[Tv:]), "padding tokens keep their values"
