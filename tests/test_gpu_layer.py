@@ -157,3 +157,33 @@ def test_cuda_graph_replay_equals_eager(name, full):
     graph.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, eager2)
+
+
+def test_two_layers_on_two_streams_match_sequential_runs():
+    """Independent layers (own buffers and workspaces) may run concurrently on separate
+    streams: cooperative routes, persistent GEMMs and cluster launches of both share
+    the device, and each output equals its sequential run bit for bit."""
+    from moe_token_routing_index_gb300 import binding as mb
+    from moe_token_routing_index_gb300.forward import MoELayer
+
+    layers, inputs = [], []
+    for name, full in (("padded_fp8", True), ("fine_grained", False)):
+        cfg = workloads.CONFIGS[name]
+        w13, w2 = workloads.make_weights(cfg, device="cuda")
+        kw = dict(router=workloads.make_router(cfg).cuda(), shared=workloads.make_shared_weights(cfg, device="cuda")) \
+            if full else {}
+        layers.append(MoELayer.from_weights(cfg, w13, w2, **kw))
+        nv = None if cfg.Tv is None else torch.tensor([cfg.Tv], dtype=torch.int32, device="cuda")
+        inputs.append((workloads.make_tokens(cfg).cuda(), None if full else workloads.make_scores(cfg).cuda(), nv))
+    ref = [layer(*inp).clone() for layer, inp in zip(layers, inputs)]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [torch.zeros_like(r) for r in ref]
+    for _ in range(3):
+        for layer, inp, st, o in zip(layers, inputs, streams, outs):
+            with torch.cuda.stream(st):
+                layer(*inp, out=o)
+    torch.cuda.synchronize()
+    assert mb.device_error() == 0
+    for o, r in zip(outs, ref):
+        assert torch.equal(o, r)
