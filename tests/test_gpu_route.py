@@ -92,3 +92,12 @@ def test_route_out_of_range_valid_count_is_clamped_and_flagged():
     got = mb.moe_route(s, 2, torch.tensor([1000], dtype=torch.int32, device="cuda"))
     assert mb.device_error() & mb.MOE_DEVERR_BAD_COUNT
     assert int(got["counts"][8]) == 80
+
+
+@pytest.mark.parametrize("T,E,k,Tv", [(131072, 64, 2, 131072), (200000, 8, 1, 199999), (65536, 256, 6, 40001)])
+def test_route_large_batches(T, E, k, Tv):
+    """Far more 32-token chunks than resident blocks (each block loops over many),
+    the largest expert counts per chunk, and a valid count inside a chunk."""
+    g = torch.Generator().manual_seed(T + E)
+    s = torch.randn(T, E, generator=g).to(torch.bfloat16)
+    _compare(s, k, Tv)
