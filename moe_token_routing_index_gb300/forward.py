@@ -30,6 +30,7 @@ from __future__ import annotations
 
 from dataclasses import dataclass, field
 
+import numpy as np
 import torch
 
 from . import binding as mb
@@ -88,11 +89,16 @@ class MoELayer:
         # None: one launch for both bf16 GEMMs when the batch averages at most one
         # 128-row tile per expert (weight-streaming, HBM-bound), else two launches.
         self.fused_mlp = fused_mlp
-        # None: 256-row tiles on CTA pairs for the bf16 GEMMs when the batch averages
-        # at least one such tile per expert; 128-row tiles otherwise.  The FP8 GEMMs
-        # keep 128-row tiles: on GB300 their pair tiles measured slower (prefill,
-        # 512 rows per expert) or padded more rows (344 rows per expert).
+        # None: 256-row tiles on CTA pairs for the bf16 GEMMs when they pad the expert
+        # rows little more than 128-row tiles do (judged from the previous forward's
+        # counts; before the first, when the batch averages at least 256 rows per
+        # expert).  The output is the same bit for bit either way.  The FP8 GEMMs keep
+        # 128-row tiles: on GB300 their pair tiles measured slower (prefill, 512 rows
+        # per expert) or padded more rows (344 rows per expert).
         self.cta_pairs = cta_pairs
+        self._counts_host: torch.Tensor | None = None   # pinned copy of the last forward's counts
+        self._counts_event: torch.cuda.Event | None = None
+        self._capturing = False
         self.router = None if router is None else router.contiguous()
         if self.router is not None:
             assert self.router.shape == (self.E, self.D) and self.router.dtype == torch.bfloat16
@@ -359,6 +365,8 @@ class MoELayer:
         if out is None:
             out = torch.zeros(x.shape[0], self.D, dtype=torch.bfloat16, device=x.device)
         self.run(self.stages(x, scores, num_valid_tokens, out, accumulate))
+        if not self.use_fused_mlp(x.shape[0]):
+            self._note_counts(self.buffers(x.shape[0], x.device).route["counts"])
         return out
 
     def capture(self, x: torch.Tensor, scores: torch.Tensor | None = None,
@@ -374,8 +382,12 @@ class MoELayer:
         self.run(stages)              # resolves the per-device lookups and kernel attributes outside the capture
         torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            self.run(stages)
+        self._capturing = True
+        try:
+            with torch.cuda.graph(graph):
+                self.run(stages)
+        finally:
+            self._capturing = False
         return graph, out
 
     def use_fused_mlp(self, T: int) -> bool:
@@ -385,10 +397,47 @@ class MoELayer:
             return self.fused_mlp
         return T * self.top_k <= 128 * self.E
 
+    # Rows per useful row that 256-row pair tiles may pad beyond 128-row tiles and
+    # still win: on the bf16 fine_grained GEMMs pairs took 9% less time per row.
+    PAIR_PADDING_MARGIN = 1.09
+
+    @staticmethod
+    def prefer_pairs(counts) -> bool:
+        """256-row tiles for these per-expert row counts: when they pad at most
+        PAIR_PADDING_MARGIN times the rows that 128-row tiles pad to."""
+        c = np.asarray(counts, np.int64)
+        c = c[c > 0]
+        if c.size == 0:
+            return False
+        pair_rows = int(np.sum((c + 255) // 256 * 256))
+        single_rows = int(np.sum((c + 127) // 128 * 128))
+        return pair_rows <= MoELayer.PAIR_PADDING_MARGIN * single_rows
+
     def use_cta_pairs(self, T: int) -> bool:
         if self.cta_pairs is not None:
             return self.cta_pairs
-        return not self.fp8 and T * self.top_k >= 256 * self.E
+        if self.fp8:
+            return False
+        last = self._last_counts()
+        if last is not None:
+            return self.prefer_pairs(last)
+        return T * self.top_k >= 256 * self.E
+
+    def _last_counts(self):
+        """The previous forward's per-expert counts, if their copy to the host has landed."""
+        if self._counts_event is None or not self._counts_event.query():
+            return None
+        return self._counts_host[: self.E].numpy()
+
+    def _note_counts(self, counts: torch.Tensor):
+        """Start a copy of this forward's counts to pinned host memory (for the tile choice)."""
+        if self._capturing or self.fp8 or self.cta_pairs is not None:
+            return
+        if self._counts_host is None:
+            self._counts_host = torch.empty(self.E + 1, dtype=torch.int32).pin_memory()
+            self._counts_event = torch.cuda.Event()
+        self._counts_host.copy_(counts, non_blocking=True)
+        self._counts_event.record()
 
     def kernel_launches(self, T: int | None = None, with_router: bool = False) -> int:
         """Kernels one forward launches: the router (if used), routing (one
