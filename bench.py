@@ -152,7 +152,24 @@ def cpu_model() -> str:
     return "unknown"
 
 
-def oracle_tokens_per_s(cfg, x, s, w13, w2, seconds: float, max_tokens: int | None = None, layer=None):
+def oracle_forward_tokens(cfg, toks, xb, sb, weights, layer, weighting: str):
+    """The oracle forward of the sampled tokens: the routed experts on the given scores, or
+    (layer = router bits and shared arrays) the whole layer; input- or output-side weighting."""
+    import numpy as np
+
+    import oracle
+
+    if layer is not None:
+        return oracle.moe_layer_forward_tokens(toks, xb, layer[0], cfg.top_k, weights, fp8=cfg.fp8, shared=layer[1],
+                                               scale_ub=cfg.scale_ub, weighting=weighting)[0]
+    if weighting == "output":
+        return oracle.moe_forward_output_weighted(np.ascontiguousarray(xb[toks]), np.ascontiguousarray(sb[toks]),
+                                                  cfg.top_k, weights, fp8=cfg.fp8, scale_ub=cfg.scale_ub)["out"]
+    return oracle.moe_forward_tokens(toks, xb, sb, cfg.top_k, weights, fp8=cfg.fp8, scale_ub=cfg.scale_ub)[0]
+
+
+def oracle_tokens_per_s(cfg, x, s, w13, w2, seconds: float, max_tokens: int | None = None, layer=None,
+                        weighting: str = "input"):
     """Time the oracle's forward (as it stands) on a bounded sample of tokens.
 
     Returns (tokens/s, tokens in the sample, threads, wall seconds).  The
@@ -169,11 +186,7 @@ def oracle_tokens_per_s(cfg, x, s, w13, w2, seconds: float, max_tokens: int | No
     cache = {}
 
     def forward(toks):
-        if layer is None:
-            oracle.moe_forward_tokens(toks, xb, sb, cfg.top_k, weights, fp8=cfg.fp8, scale_ub=cfg.scale_ub)
-        else:
-            oracle.moe_layer_forward_tokens(toks, xb, layer[0], cfg.top_k, weights, fp8=cfg.fp8, shared=layer[1],
-                                            scale_ub=cfg.scale_ub)
+        oracle_forward_tokens(cfg, toks, xb, sb, weights, layer, weighting)
 
     def weights(ids):
         missing = [e for e in ids if e not in cache]
@@ -352,7 +365,8 @@ def run_ours(args, cfg):
                                 "note": "the same step captured once and replayed K times"}
         if not args.no_cpu_baseline and world == 1:
             tps, n, cores, dt = oracle_tokens_per_s(cfg, x, s, w13, w2, args.cpu_seconds,
-                                                    layer=_layer_weights_host(cfg, router, shared))
+                                                    layer=_layer_weights_host(cfg, router, shared),
+                                                    weighting=args.weighting)
             result["cpu_baseline"] = {"value": round(tps, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
                                       "cpu": cpu_model(),
                                       "sample": f"first {n} valid tokens of the workload (repeated to {dt:.1f} s of wall time)"}
@@ -592,7 +606,7 @@ def run_reference(args, cfg):
     budget = 150.0                                  # seconds for the whole --steps/--warmup run
     # calibrate the per-token cost, then size each step's sample to the budget
     tps, n, cores, dt = oracle_tokens_per_s(cfg, x, s, w13, w2, min(3.0, budget / (args.steps + args.warmup)),
-                                            layer=layer)
+                                            layer=layer, weighting=args.weighting)
     per_tok = dt / n
     n_step = int(max(1, min(cfg.valid_tokens, budget / (args.steps + args.warmup) / per_tok)))
     xb, sb = _host_bits(x), _host_bits(s)
@@ -613,11 +627,7 @@ def run_reference(args, cfg):
 
     def step(i):
         toks = np.unique((np.arange(n_step) + i * n_step) % Tv)
-        if layer is None:
-            oracle.moe_forward_tokens(toks, xb, sb, cfg.top_k, weights, fp8=cfg.fp8, scale_ub=cfg.scale_ub)
-        else:
-            oracle.moe_layer_forward_tokens(toks, xb, layer[0], cfg.top_k, weights, fp8=cfg.fp8, shared=layer[1],
-                                            scale_ub=cfg.scale_ub)
+        oracle_forward_tokens(cfg, toks, xb, sb, weights, layer, args.weighting)
         return len(toks)
 
     for i in range(args.warmup):

@@ -441,28 +441,34 @@ def shared_expert(x, w13, w2, *, fp8: bool, scale_ub: float | None = None, valid
 
 
 def moe_layer_forward(x, w_router, top_k: int, weights, *, fp8: bool, shared=None,
-                      valid_tokens: int | None = None, scale_ub: float | None = None):
+                      valid_tokens: int | None = None, scale_ub: float | None = None, weighting: str = "input"):
     """The whole MoE layer of MetaShufflingMoE._no_comm_forward on one GPU:
     router scores, the shared expert (``shared`` = (w13, w2), or None for a
-    layer without one), and the routed experts added into its output.
+    layer without one), and the routed experts added into its output
+    (``weighting`` "input": scores scale the expert inputs; "output": the top-k
+    finalize weights the expert outputs and adds the shared output).
     Returns the routed forward's dict plus ``scores`` and ``shared_out``.
     """
     scores = router_scores(x, w_router, valid_tokens)
     base = None
     if shared is not None:
         base = shared_expert(x, shared[0], shared[1], fp8=fp8, scale_ub=scale_ub, valid_tokens=valid_tokens)
-    res = moe_forward(x, scores, top_k, weights, fp8=fp8, valid_tokens=valid_tokens, out_init=base,
-                      scale_ub=scale_ub)
+    if weighting == "output":
+        res = moe_forward_output_weighted(x, scores, top_k, weights, fp8=fp8, valid_tokens=valid_tokens,
+                                          shared_out=base, scale_ub=scale_ub)
+    else:
+        res = moe_forward(x, scores, top_k, weights, fp8=fp8, valid_tokens=valid_tokens, out_init=base,
+                          scale_ub=scale_ub)
     res["scores"] = scores
     res["shared_out"] = base
     return res
 
 
 def moe_layer_forward_tokens(tokens, x, w_router, top_k: int, weights, *, fp8: bool, shared=None,
-                             scale_ub: float | None = None):
+                             scale_ub: float | None = None, weighting: str = "input"):
     """moe_layer_forward's output rows for a sample of valid tokens: every stage,
     the router and the shared expert included, works token by token."""
     tokens = np.asarray(tokens, np.int64)
     res = moe_layer_forward(np.ascontiguousarray(x[tokens]), w_router, top_k, weights, fp8=fp8, shared=shared,
-                            scale_ub=scale_ub)
+                            scale_ub=scale_ub, weighting=weighting)
     return res["out"], res

@@ -119,3 +119,21 @@ def test_output_weighted_forward_against_dense_formula():
     r2 = oracle.moe_forward_output_weighted(x, s2, k, lambda ids: (w13[ids], w2[ids]), fp8=False, valid_tokens=Tv)
     r1 = oracle.moe_forward_output_weighted(x, s, k, lambda ids: (w13[ids], w2[ids]), fp8=False, valid_tokens=Tv)
     np.testing.assert_array_equal(f64(r2["out"][:Tv]), 2 * f64(r1["out"][:Tv]))
+
+
+def test_layer_forward_with_output_weighting_composes_the_stages():
+    rng = np.random.default_rng(44)
+    T, D, H, E, k = 16, 64, 32, 4, 2
+    x = _bf16(rng.standard_normal((T, D)))
+    wr = _bf16(rng.standard_normal((E, D)) * 0.125)
+    w13 = _bf16(rng.standard_normal((E, 2 * H, D)) * 0.05)
+    w2 = _bf16(rng.standard_normal((E, D, H)) * 0.05)
+    sh = (_bf16(rng.standard_normal((2 * H, D)) * 0.05), _bf16(rng.standard_normal((D, H)) * 0.05))
+    wf = lambda ids: (w13[ids], w2[ids])
+    got = oracle.moe_layer_forward(x, wr, k, wf, fp8=False, shared=sh, weighting="output")["out"]
+    base = oracle.shared_expert(x, *sh, fp8=False)
+    want = oracle.moe_forward_output_weighted(x, oracle.router_scores(x, wr), k, wf, fp8=False, shared_out=base)
+    np.testing.assert_array_equal(got, want["out"])
+    part, _ = oracle.moe_layer_forward_tokens(np.array([1, 5, 9]), x, wr, k, wf, fp8=False, shared=sh,
+                                              weighting="output")
+    np.testing.assert_array_equal(part, got[[1, 5, 9]])
