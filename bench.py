@@ -642,7 +642,7 @@ def run_reference(args, cfg):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 accumulate",
         "data": "synthetic, seeded (same workload generator as the GPU arm)",
         "config": {"workload": workload_desc(cfg) + (" + router + shared expert" if layer else ""),
-                   "sample_tokens_per_step": n_step},
+                   "weighting": args.weighting, "sample_tokens_per_step": n_step},
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
                          "cpu": cpu_model(),
                          "sample": f"{n_step} valid tokens per step (of {Tv}), tokens cycling through the workload"},
