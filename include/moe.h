@@ -287,6 +287,12 @@ int moe_quantize_rows(const float* w, int64_t rows, int cols, const float* scale
  * tensor cores (tcgen05, accumulators in tensor memory, TMA-fed).
  * Requires N, K multiples of 16 (H a multiple of 16 for SILU_MUL), E <= 1024.
  *
+ * epilogue may carry MOE_GEMM_CTA_PAIRS (OR-ed in): 256-row x 256-column tiles
+ * computed by a cluster of two CTAs with tcgen05.mma.cta_group::2 instead of
+ * 128-row tiles on one CTA.  Each output element is accumulated in the same
+ * order either way, so the bytes are identical; pairs move a third less operand
+ * data per K block but pad each expert to a multiple of 256 rows.
+ *
  * scatter_indices (nullable; MOE_EPILOGUE_NONE only): the combine fused into
  * the epilogue, grouped_gemm(..., _output_tensor=out,
  * _scatter_add_indices=token_indices) of _routed_expert, for top_k = 1 where
