@@ -555,24 +555,35 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
 # summarised under profiles/, with the hash of the kernel sources they were taken
 # on: when those sources change the figure no longer applies and is reported as null.
 TRAFFIC: dict = {
-    ("decode", "expert_mlp"): (4_037_355_000 + 6_043_648, "grouped_gemm.cu", "f796cfcae1f4"),
-    ("prefill_fp8", "gemm_w13"): (1_385_569_000 + 249_881_344, "grouped_gemm.cu", "f796cfcae1f4"),
-    ("padded_fp8", "gather_quant"): (93_188_096 + 118_469_888, "rowwise.cu", "b3c96b709583"),
+    ("decode", "expert_mlp"): (4_037_737_472 + 5_864_704, "grouped_gemm.cu", "b630aad71443"),
+    ("prefill_fp8", "gemm_w13"): (1_386_704_128 + 249_189_632, "grouped_gemm.cu", "b630aad71443"),
+    ("padded_fp8", "gather_quant"): (93_194_752 + 118_310_400, "rowwise.cu", "4a5af973a02e"),
 }
 
 
-# the device-code headers each kernel source includes
-KERNEL_HEADERS = {"grouped_gemm.cu": ("common.cuh", "tcgen05.cuh"), "router.cu": ("common.cuh", "tcgen05.cuh"),
-                  "rowwise.cu": ("common.cuh",), "route.cu": ("common.cuh",)}
-
-
 def kernel_source_hash(name: str) -> str:
+    """sha1 (12 hex digits) of a kernel source and every local header it reaches through
+    `#include "..."`, in first-reach order: counters captured on one build are reported only
+    while none of those files has changed."""
     import hashlib
+    import re
 
     csrc = ROOT / "moe_token_routing_index_gb300" / "csrc"
+    seen, order = set(), []
+
+    def visit(path: Path) -> None:
+        path = path.resolve()
+        if path in seen:
+            return
+        seen.add(path)
+        order.append(path)
+        for inc in re.findall(r'^\s*#\s*include\s+"([^"]+)"', path.read_text(), re.M):
+            visit(path.parent / inc)
+
+    visit(csrc / name)
     h = hashlib.sha1()
-    for f in (name, *KERNEL_HEADERS.get(name, ("common.cuh",))):
-        h.update((csrc / f).read_bytes())
+    for f in order:
+        h.update(f.read_bytes())
     return h.hexdigest()[:12]
 
 
