@@ -90,6 +90,22 @@ __device__ __forceinline__ uint4 f32_to_bf16x8(const float* f) {
   return v;
 }
 
+// Two fp32 products, each rounded to nearest even with subnormals kept: one
+// packed f32x2 multiply, the same bits as two scalar __fmul_rn.
+__device__ __forceinline__ float2 fmul2_rn(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 pa, pb, pr;\n\tmov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+      "mul.rn.f32x2 pr, pa, pb;\n\tmov.b64 {%0, %1}, pr;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
+// The two bf16 of a packed word as fp32 (low half first): exact widening.
+__device__ __forceinline__ float2 bf16x2_bits_to_f32(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
 // Two floats -> two e4m3 codes (round to nearest even, saturating to +-448),
 // low byte = a, high byte = b.
 __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float a, float b) {
@@ -106,12 +122,17 @@ __device__ __forceinline__ float silu_mul_f32(float a, float b) {
 
 // The FP8-rowwise scale rule: m = max|v| clamped to [EPS, ub] (or >= EPS);
 // returns s = 448 / m and writes the stored dequantisation scale 1 / s.
-__device__ __forceinline__ float fp8_row_scale(float m, const float* ub, float* inv_out) {
+// fp8_row_scale_val takes the bound already loaded (has_ub false: no bound).
+__device__ __forceinline__ float fp8_row_scale_val(float m, bool has_ub, float ubv, float* inv_out) {
   m = fmaxf(m, kFp8Eps);
-  if (ub) m = fminf(m, __ldg(ub));
+  if (has_ub) m = fminf(m, ubv);
   float s = __fdiv_rn(kFp8Max, m);
   *inv_out = __frcp_rn(s);
   return s;
+}
+
+__device__ __forceinline__ float fp8_row_scale(float m, const float* ub, float* inv_out) {
+  return fp8_row_scale_val(m, ub != nullptr, ub ? __ldg(ub) : 0.0f, inv_out);
 }
 
 __device__ __forceinline__ float fp8_scaled_clamped(float v, float s) {

@@ -275,7 +275,7 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                : "memory");
 }
 
-constexpr int kStagedWarps = 8;
+constexpr int kStagedMaxWarps = 16;  // the launch picks 8..16 warps per block
 
 // Largest |bf16| of 8 packed values, as bf16 magnitude bits (the magnitude
 // bits of a bf16 order like its absolute value), folded into `m`.
@@ -298,17 +298,17 @@ __device__ __forceinline__ uint32_t absmax_bits8(const uint4& v, uint32_t m) {
 // monotone), taken as an integer max over the packed bf16 magnitudes; the
 // clamp to +-448 is the saturation of the e4m3 conversion itself.
 template <bool QUANT>
-__global__ void __launch_bounds__(kStagedWarps * 32, 1) gather_staged_kernel(
+__global__ void __launch_bounds__(kStagedMaxWarps * 32, 1) gather_staged_kernel(
     const uint4* __restrict__ x, int T, int D8, const int32_t* __restrict__ ti, const int32_t* __restrict__ ei,
     const int32_t* __restrict__ inv, int k, int a, const void* __restrict__ scores, int dtype, int64_t st,
     int64_t se, int E, const int32_t* __restrict__ valid_p, const float* __restrict__ ub, void* __restrict__ out,
     float* __restrict__ out_scale, int NB, unsigned int* err) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwb = blockDim.x >> 5;
   const uint32_t row_bytes = (uint32_t)D8 * 16u;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);                      // [warps][NB]
-  int* s_tok = reinterpret_cast<int*>(smem + kStagedWarps * NB * 8);       // [warps][NB]: staged token or -1
-  uint8_t* slots = smem + ((kStagedWarps * NB * 16 + 127) / 128) * 128;    // [warps][NB][row_bytes]
+  int* s_tok = reinterpret_cast<int*>(smem + nwb * NB * 8);                // [warps][NB]: staged token or -1
+  uint8_t* slots = smem + ((nwb * NB * 16 + 127) / 128) * 128;             // [warps][NB][row_bytes]
   const int valid = read_count(valid_p, a, err);
   const int nrows = inv ? k : 1;  // routed rows per item
   int items = valid;
@@ -316,7 +316,8 @@ __global__ void __launch_bounds__(kStagedWarps * 32, 1) gather_staged_kernel(
     if (valid % k != 0 && blockIdx.x == 0 && threadIdx.x == 0) flag_error(err, MOE_DEVERR_BAD_COUNT);
     items = min(valid / k, T);
   }
-  const int gw = blockIdx.x * kStagedWarps + warp, nw = gridDim.x * kStagedWarps;
+  // warps numbered SM-fastest, so a partial last round of items spreads over all blocks
+  const int gw = warp * gridDim.x + blockIdx.x, nw = gridDim.x * nwb;
   auto bar_addr = [&](int b) { return (uint32_t)__cvta_generic_to_shared(&bars[warp * NB + b]); };
   auto slot = [&](int b) { return slots + (size_t)(warp * NB + b) * row_bytes; };
   if (lane == 0)
@@ -330,10 +331,6 @@ __global__ void __launch_bounds__(kStagedWarps * 32, 1) gather_staged_kernel(
     s_tok[warp * NB + b] = ok ? t : -1;
     if (ok) bulk_load((uint32_t)__cvta_generic_to_shared(slot(b)), x + (int64_t)t * D8, row_bytes, bar_addr(b));
   };
-  if (lane == 0)
-    for (int b = 0; b < NB; ++b)
-      if (gw + b * nw < items) issue(gw + b * nw, b);
-  __syncwarp();
   // metadata of routed-row number q of this warp (item q / nrows, its row q % nrows): lane L holds q = base + L
   int meta_base = -32;
   int m_row = -1;
@@ -354,6 +351,15 @@ __global__ void __launch_bounds__(kStagedWarps * 32, 1) gather_staged_kernel(
       }
     }
   };
+  // the first item's row copy, then its metadata (ahead of the other slots' copies in the memory queues)
+  if (lane == 0 && gw < items) issue(gw, 0);
+  __syncwarp();
+  load_meta(0);
+  if (lane == 0)
+    for (int b = 1; b < NB; ++b)
+      if (gw + b * nw < items) issue(gw + b * nw, b);
+  __syncwarp();
+  const float ubv = (QUANT && ub) ? __ldg(ub) : 0.0f;
   uint32_t phase = 0;  // bit b: parity of the next completion of slot b
   int i = 0;
   bool timed_out = false;
@@ -369,50 +375,64 @@ __global__ void __launch_bounds__(kStagedWarps * 32, 1) gather_staged_kernel(
       }
       phase ^= 1u << b;
       const uint4* row = reinterpret_cast<const uint4*>(slot(b));
-      uint32_t mx = 0;
-      if (QUANT) {  // the row's largest |x|, shared by all of its routed rows
+      // the item's rows in one metadata window (nrows <= 32); lane j < nrows takes row j
+      if (i * nrows + nrows > meta_base + 32) load_meta(i * nrows);
+      const int src = i * nrows - meta_base + min(lane, nrows - 1);
+      const int r_l = __shfl_sync(0xffffffffu, m_row, src);
+      const float s_l = __shfl_sync(0xffffffffu, m_s, src);
+      float sc_l = 0.0f;
+      if constexpr (QUANT) {  // the row's largest |x|, shared by all of its routed rows
+        uint32_t mx = 0;
         for (int c = lane; c < D8; c += 32) mx = absmax_bits8(row[c], mx);
         mx = __reduce_max_sync(0xffffffffu, mx);
+        // the rows' scales side by side, one per lane: max_j |x_j * s| = RN(max|x| * |s|)
+        float inv_s;
+        sc_l = fp8_row_scale_val(__fmul_rn(__uint_as_float(mx << 16), fabsf(s_l)), ub != nullptr, ubv, &inv_s);
+        if (lane < nrows && r_l >= 0) out_scale[r_l] = inv_s;
       }
       for (int j = 0; j < nrows; ++j) {
-        const int q = i * nrows + j;
-        if (q >= meta_base + 32) load_meta(q);
-        const int r = __shfl_sync(0xffffffffu, m_row, q - meta_base);
-        const float s = __shfl_sync(0xffffffffu, m_s, q - meta_base);
+        const int r = __shfl_sync(0xffffffffu, r_l, j);
+        const float s = __shfl_sync(0xffffffffu, s_l, j);
         if (r < 0) {
           if (lane == 0) flag_error(err, MOE_DEVERR_BAD_INDEX);
           continue;
         }
         if constexpr (QUANT) {
-          const float m = __fmul_rn(__uint_as_float(mx << 16), fabsf(s));  // = max_j |x_j * s|
-          float inv_s;
-          const float sc = fp8_row_scale(m, ub, &inv_s);
-          if (lane == 0) out_scale[r] = inv_s;
+          const float sc = __shfl_sync(0xffffffffu, sc_l, j);
           uint2* dst = static_cast<uint2*>(out) + (int64_t)r * D8;
-#pragma unroll 2
+          const float2 s2 = make_float2(s, s), sc2 = make_float2(sc, sc);
+#pragma unroll 8
           for (int c = lane; c < D8; c += 32) {
-            float f[8];
-            bf16x8_to_f32(row[c], f);
+            const uint4 v = row[c];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t q[4];
 #pragma unroll
-            for (int q8 = 0; q8 < 8; ++q8) f[q8] = __fmul_rn(__fmul_rn(f[q8], s), sc);
-            dst[c] = e4m3x8(f);  // saturating conversion = the clamp to +-448
+            for (int h = 0; h < 4; ++h) {  // RN(RN(x * s) * sc), two lanes per multiply
+              const float2 p = fmul2_rn(fmul2_rn(bf16x2_bits_to_f32(w[h]), s2), sc2);
+              q[h] = f32x2_to_e4m3x2(p.x, p.y);  // saturating conversion = the clamp to +-448
+            }
+            dst[c] = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
           }
         } else {
           uint4* dst = static_cast<uint4*>(out) + (int64_t)r * D8;
-#pragma unroll 2
+          const float2 s2 = make_float2(s, s);
+#pragma unroll 8
           for (int c = lane; c < D8; c += 32) {
-            float f[8];
-            bf16x8_to_f32(row[c], f);
+            const uint4 v = row[c];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[4];
 #pragma unroll
-            for (int q8 = 0; q8 < 8; ++q8) f[q8] = __fmul_rn(f[q8], s);
-            dst[c] = f32_to_bf16x8(f);
+            for (int h = 0; h < 4; ++h) {
+              const float2 p = fmul2_rn(bf16x2_bits_to_f32(w[h]), s2);
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(p.x, p.y);
+              o[h] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
           }
         }
       }
     } else {
       if (lane == 0) flag_error(err, MOE_DEVERR_BAD_INDEX);
-      for (int j = 0; j < nrows; ++j)  // keep the metadata window in step
-        if (i * nrows + j >= meta_base + 32) load_meta(i * nrows + j);
     }
     // the slot's reads (generic proxy) finish before the next bulk copy (async proxy) writes it
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -437,26 +457,36 @@ __global__ void __launch_bounds__(kStagedWarps * 32, 1) gather_staged_kernel(
   }
 }
 
-// Slots per warp of the staged gather (0: the row does not fit twice in 200 KB).
-inline int staged_slots(int D8) {
-  const size_t row_bytes = (size_t)D8 * 16;
-  return (int)std::min<size_t>(4, (200u * 1024u) / (kStagedWarps * row_bytes));
+// Shape of the staged gather for rows of D8 16-byte vectors: warps per block
+// (8..16) and row slots per warp (2..4), within 226 of the 227 KB of shared
+// memory a block may hold (the rest: barriers and token slots), and
+// with at least two slots per warp (one row consumed while the next lands).
+// More warps first: the consume loop needs issue slots more than it needs
+// deeper per-warp prefetch.  {0, 0}: two slots of 8 warps do not fit.
+struct StagedShape {
+  int warps, slots;
+};
+inline StagedShape staged_shape(int D8) {
+  const size_t row_bytes = (size_t)D8 * 16, budget = 226u * 1024u;
+  const int warps = (int)std::min<size_t>(kStagedMaxWarps, budget / (2 * row_bytes));
+  if (warps < 8) return {0, 0};
+  return {warps, (int)std::min<size_t>(4, budget / (warps * row_bytes))};
 }
 
 template <bool QUANT>
-cudaError_t launch_staged(const GatherArgs& g, int nb, cudaStream_t s) {
-  const int D8 = g.D / 8;
+cudaError_t launch_staged(const GatherArgs& g, StagedShape sh, cudaStream_t s) {
+  const int D8 = g.D / 8, nb = sh.slots;
   const size_t row_bytes = (size_t)D8 * 16;
-  const size_t smem = (size_t)((kStagedWarps * nb * 16 + 127) / 128) * 128 + (size_t)kStagedWarps * nb * row_bytes;
+  const size_t smem = (size_t)((sh.warps * nb * 16 + 127) / 128) * 128 + (size_t)sh.warps * nb * row_bytes;
   auto kern = gather_staged_kernel<QUANT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t items = g.inv ? std::min<int64_t>(g.a / g.top_k, g.T) : g.a;
-  const int64_t need = (items + kStagedWarps - 1) / kStagedWarps;
+  const int64_t need = (items + sh.warps - 1) / sh.warps;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(need, device_sm_count()));
-  kern<<<grid, kStagedWarps * 32, smem, s>>>(static_cast<const uint4*>(g.x), g.T, D8, g.token_indices,
-                                             g.expert_indices, g.inv, g.top_k, g.a, g.scores, g.dtype, g.stride_t,
-                                             g.stride_e, g.E, g.valid, g.scale_ub, g.out, g.out_scale, nb, g.err);
+  kern<<<grid, sh.warps * 32, smem, s>>>(static_cast<const uint4*>(g.x), g.T, D8, g.token_indices,
+                                         g.expert_indices, g.inv, g.top_k, g.a, g.scores, g.dtype, g.stride_t,
+                                         g.stride_e, g.E, g.valid, g.scale_ub, g.out, g.out_scale, nb, g.err);
   return cudaGetLastError();
 }
 
@@ -807,9 +837,9 @@ __global__ void __launch_bounds__(kThreads) topk_finalize_kernel(uint4* __restri
 }  // namespace
 
 cudaError_t launch_gather_scale(const GatherArgs& g, cudaStream_t s) {
-  if (g.inv && g.top_k > 1) {  // token-major: each x row is read once for its top_k rows
-    const int nb = staged_slots(g.D / 8);
-    if (nb >= 2) return launch_staged<false>(g, nb, s);
+  if (g.inv && g.top_k > 1 && g.top_k <= 32) {  // token-major: each x row is read once for its top_k rows
+    const StagedShape sh = staged_shape(g.D / 8);
+    if (sh.warps) return launch_staged<false>(g, sh, s);
   }
   const int grid =
       persistent_grid(gather_scale_kernel, (int64_t)g.a * ((g.D / 8 + kGatherChunk - 1) / kGatherChunk), kWarps);
@@ -837,8 +867,8 @@ cudaError_t launch_gather_scale_quant(const GatherArgs& g, cudaStream_t s) {
   const int D8 = g.D / 8;
   // TMA-staged rows (token-major with the inverse permutation) when two row
   // slots per warp fit in shared memory, else rows held in registers.
-  const int nb = staged_slots(D8);
-  if (nb >= 2) return launch_staged<true>(g, nb, s);
+  const StagedShape sh = staged_shape(D8);
+  if (sh.warps && (!g.inv || g.top_k <= 32)) return launch_staged<true>(g, sh, s);
   const int G = pick_group(D8);
   const bool full = D8 > 32 * G * 4;  // 8 vectors per thread, else 4
   switch (G * 2 + (full ? 1 : 0)) {

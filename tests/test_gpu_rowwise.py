@@ -202,6 +202,45 @@ def test_token_major_gather_equals_row_major(name, quant):
     assert mb.device_error() == 0
 
 
+@pytest.mark.parametrize("T,D,E,k", [(37, 16, 8, 3), (50, 272, 12, 5), (29, 2064, 9, 7), (40, 7168, 40, 32),
+                                     (21, 1024, 64, 40), (13, 8192, 6, 2), (20000, 64, 8, 3), (12000, 2048, 16, 5)])
+@pytest.mark.parametrize("quant", [False, True])
+def test_token_major_gather_ragged(T, D, E, k, quant):
+    """Token-major gathers on ragged shapes: top_k that does not divide the 32-row
+    metadata window, top_k = 32 and above it (row-major fallback), rows of 8 and 16
+    staging warps and rows too wide to stage, many tokens per warp (the slot ring
+    wraps), f32 and bf16 scores, and values whose products are subnormal or
+    saturate the e4m3 range: bit-exact against the oracle."""
+    mb = _mb()
+    g = torch.Generator().manual_seed(T * 7 + D + k)
+    x = torch.randn(T, D, generator=g)
+    x[0, : min(D, 8)] = torch.tensor([1e-39, -3e-40, 2e-38, 0.0, -0.0, 5e-41, 1e-38, -1e-39])[: min(D, 8)]
+    x[min(1, T - 1)] *= 1e30
+    x = x.to(torch.bfloat16)
+    s = torch.rand(T, E, generator=g)
+    s[min(2, T - 1)] *= 1e-30
+    s = s.to(torch.bfloat16)
+    r = oracle.route(bits(s), k)
+    a = T * k
+    ti, ei, inv = _idx(r["token_indices"]), _idx(r["expert_indices"]), _idx(r["inv"].ravel())
+    sd = s.cuda() if T % 2 == 0 else s.float().cuda()
+    s_ref = bits(s) if T % 2 == 0 else s.float().numpy()
+    valid = torch.tensor([a], dtype=torch.int32, device="cuda")
+    if quant:
+        q = sentinel_like((a, D), torch.float8_e4m3fn)
+        sc = sentinel_like((a,), torch.float32)
+        mb.moe_gather_scale_quant(x.cuda(), ti, ei, sd, None, valid, inv_rows=inv, top_k=k, out=q, out_scale=sc)
+        q_ref, sc_ref = oracle.gather_scale_quant(bits(x), r["token_indices"], r["expert_indices"], s_ref)
+        np.testing.assert_array_equal(bits(q), q_ref)
+        np.testing.assert_array_equal(sc.cpu().numpy(), sc_ref)
+    else:
+        o = sentinel_like((a, D), torch.bfloat16)
+        mb.moe_gather_scale(x.cuda(), ti, ei, sd, valid, inv_rows=inv, top_k=k, out=o)
+        np.testing.assert_array_equal(bits(o), oracle.gather_scale(bits(x), r["token_indices"], r["expert_indices"],
+                                                                   s_ref))
+    assert mb.device_error() == 0
+
+
 def test_binding_rejects_strided_matrices():
     mb = _mb()
     x = torch.randn(64, 32, device="cuda").to(torch.bfloat16).t()        # a transposed view: not row-major
