@@ -43,12 +43,19 @@ constexpr int kABytes = kBM * kBKBytes;          // 16 KB
 constexpr int kBBytes = kBN * kBKBytes;          // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;   // 48 KB
 constexpr int kMaxExperts = 1024;
+// Per epilogue warp: a staging block of 32 rows x 128 bytes (one 64-column bf16
+// chunk of the warp's rows, 16-byte pieces XOR-swizzled by row) and the tile's
+// column scales (FP8).
+constexpr int kEpiStageBytes = 32 * 128;
+constexpr int kEpiWarpBytes = kEpiStageBytes + kBN * 4;  // 5 KB
+constexpr int kEpiBytes = 4 * kEpiWarpBytes;             // 20 KB
 
 struct SmemLayout {
   // offsets from the 1024-aligned base
   static constexpr int a = 0;
   static constexpr int b = a + kStages * kABytes;
-  static constexpr int bars = b + kStages * kBBytes;        // full[S], empty[S], tfull[2], tempty[2], drain
+  static constexpr int epi = b + kStages * kBBytes;         // [4 epilogue warps][kEpiWarpBytes]
+  static constexpr int bars = epi + kEpiBytes;              // full[S], empty[S], tfull[2], tempty[2], drain
   static constexpr int nbars = 2 * kStages + 2 * kAccBufs + 1;
   static constexpr int misc = bars + nbars * 8;             // tmem base, abort flag, total tiles, pad
   static constexpr int sched = misc + 16;                   // tile_start[E+1], row_off[E+1], mtiles[E]
@@ -127,90 +134,130 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// Epilogue of one accumulator tile for the calling thread: TMEM lane = the
-// thread's row of the tile (row_in_tile), columns of the phase's N tile.
-// FP8 scales, the SiLU*mul of the two halves or the fused combine, bf16 stores.
+// Epilogue of one accumulator tile for one warp: its 32 rows of the tile
+// (TMEM lanes of the warp's quarter; the calling thread's row is warp_row0 +
+// lane), all columns of the phase's N tile.  FP8 scales, the SiLU*mul of the two
+// halves or the fused combine, then bf16 stores.  Each 64-column chunk goes
+// through the warp's staging block, so that the warp stores 4 rows x 128
+// contiguous bytes per instruction instead of 32 rows x 16 bytes.
 template <bool FP8>
-__device__ __forceinline__ void epilogue_tile(const Phase& p, const Tile& t, int row_in_tile, uint32_t tbase,
-                                              unsigned int* err) {
+__device__ __forceinline__ void epilogue_tile(const Phase& p, const Tile& t, int warp_row0, int lane, uint32_t tbase,
+                                              uint8_t* scratch, unsigned int* err) {
+  uint8_t* stage = scratch;
+  float* wsc_s = reinterpret_cast<float*>(scratch + kEpiStageBytes);
+  const int row_in_tile = warp_row0 + lane;
   const bool row_ok = row_in_tile < t.rows;
   const int row = t.row0 + row_in_tile;
   const int n_out = p.n_out;
+  const int col0 = t.n_idx * p.n_tile_cols;
+  const bool silu = p.epi == MOE_EPILOGUE_SILU_MUL;
   float xs = 1.0f;
   if (FP8 && row_ok) xs = __ldg(p.x_scale + row);
-  __nv_bfloat16* yrow = p.y + (int64_t)row * n_out;  // (the scatter epilogue redirects it)
-  const int col0 = t.n_idx * p.n_tile_cols;
-  const float* wsc = FP8 ? p.w_scale + (int64_t)t.expert * p.N : nullptr;
-  if (p.epi == MOE_EPILOGUE_SILU_MUL) {
+  if (FP8) {
+    // the tile's column scales, clamped to valid columns (SiLU*mul: w_in block, then gate block)
+    const float* wsc = p.w_scale + (int64_t)t.expert * p.N;
     const int H = p.N / 2;
-#pragma unroll 1
-    for (int c = 0; c < kBN / 2; c += 32) {
-      float v0[32], v1[32];
-      tmem_ld32(tbase + c, v0);
-      tmem_ld32(tbase + kBN / 2 + c, v1);
-      if (row_ok && col0 + c < n_out) {
-        float z[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float a0 = v0[i], a1 = v1[i];
+    for (int k = 0; k < kBN / 32; ++k) {
+      const int i = lane + 32 * k;
+      const int col = silu ? (i < kBN / 2 ? min(col0 + i, H - 1) : H + min(col0 + i - kBN / 2, H - 1))
+                           : min(col0 + i, n_out - 1);
+      wsc_s[i] = __ldg(wsc + col);
+    }
+    __syncwarp();
+  }
+  // destination row of each tile row: its own, or with the fused combine (top_k = 1)
+  // its token's row; -1: nothing to store
+  int dst = row_ok ? row : -1;
+  if (p.scatter && row_ok) {
+    const int tok = __ldg(p.scatter + row);
+    if ((unsigned)tok < (unsigned)p.T_out) {
+      dst = tok;
+    } else {
+      dst = -1;
+      flag_error(err, MOE_DEVERR_BAD_INDEX);
+    }
+  }
+  // this lane stores rows (lane >> 3) + 4 j of the warp's 32, 16-byte piece lane & 7 of each chunk
+  int dst_j[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) dst_j[j] = __shfl_sync(0xffffffffu, dst, (lane >> 3) + 4 * j);
+  const bool add = p.scatter && p.accumulate;
+  const int piece = lane & 7;
+  const int out_cols = silu ? kBN / 2 : kBN;
+#pragma unroll 1
+  for (int c = 0; c < out_cols; c += 64) {
+    // the thread's row: 64 output columns as bf16 into staging row `lane`
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int cc = c + 32 * h;
+      float z[32];
+      if (silu) {
+        float v1[32];
+        tmem_ld32(tbase + cc, z);
+        tmem_ld32(tbase + kBN / 2 + cc, v1);
+#pragma unroll
+        for (int i4 = 0; i4 < 8; ++i4) {
+          float4 w0 = make_float4(1.f, 1.f, 1.f, 1.f), w1 = w0;
           if (FP8) {
-            const int col = col0 + c + i < H ? col0 + c + i : H - 1;
-            a0 = __fmul_rn(__fmul_rn(a0, xs), __ldg(wsc + col));
-            a1 = __fmul_rn(__fmul_rn(a1, xs), __ldg(wsc + H + col));
+            w0 = reinterpret_cast<const float4*>(wsc_s + cc)[i4];
+            w1 = reinterpret_cast<const float4*>(wsc_s + kBN / 2 + cc)[i4];
           }
-          // the unfused pipeline rounds the GEMM output to bf16 before silu_mul
-          a0 = __bfloat162float(__float2bfloat16_rn(a0));
-          a1 = __bfloat162float(__float2bfloat16_rn(a1));
-          z[i] = silu_mul_f32(a0, a1);
-        }
+          const float ws0[4] = {w0.x, w0.y, w0.z, w0.w}, ws1[4] = {w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (col0 + c + 8 * q < n_out)
-            *reinterpret_cast<uint4*>(yrow + col0 + c + 8 * q) = f32_to_bf16x8(z + 8 * q);
-      }
-    }
-  } else {
-    // The combine fused in (top_k = 1): this row's destination is its token's row.
-    bool dst_ok = row_ok;
-    if (p.scatter && row_ok) {
-      const int tok = __ldg(p.scatter + row);
-      if ((unsigned)tok < (unsigned)p.T_out) {
-        yrow = p.y + (int64_t)tok * n_out;
+          for (int u = 0; u < 4; ++u) {
+            const int i = 4 * i4 + u;
+            float a0 = z[i], a1 = v1[i];
+            if (FP8) {
+              a0 = __fmul_rn(__fmul_rn(a0, xs), ws0[u]);
+              a1 = __fmul_rn(__fmul_rn(a1, xs), ws1[u]);
+            }
+            // the unfused pipeline rounds the GEMM output to bf16 before silu_mul
+            a0 = __bfloat162float(__float2bfloat16_rn(a0));
+            a1 = __bfloat162float(__float2bfloat16_rn(a1));
+            z[i] = silu_mul_f32(a0, a1);
+          }
+        }
       } else {
-        dst_ok = false;
-        flag_error(err, MOE_DEVERR_BAD_INDEX);
-      }
-    }
-    const bool add = p.scatter && p.accumulate;
-#pragma unroll 1
-    for (int c = 0; c < kBN; c += 32) {
-      float v[32];
-      tmem_ld32(tbase + c, v);
-      if (dst_ok && col0 + c < n_out) {
+        tmem_ld32(tbase + cc, z);
         if (FP8) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int col = col0 + c + i < n_out ? col0 + c + i : n_out - 1;
-            v[i] = __fmul_rn(__fmul_rn(v[i], xs), __ldg(wsc + col));
+          for (int i4 = 0; i4 < 8; ++i4) {
+            const float4 w = reinterpret_cast<const float4*>(wsc_s + cc)[i4];
+            z[4 * i4 + 0] = __fmul_rn(__fmul_rn(z[4 * i4 + 0], xs), w.x);
+            z[4 * i4 + 1] = __fmul_rn(__fmul_rn(z[4 * i4 + 1], xs), w.y);
+            z[4 * i4 + 2] = __fmul_rn(__fmul_rn(z[4 * i4 + 2], xs), w.z);
+            z[4 * i4 + 3] = __fmul_rn(__fmul_rn(z[4 * i4 + 3], xs), w.w);
           }
         }
+      }
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (col0 + c + 8 * q < n_out) {
-            uint4* dst = reinterpret_cast<uint4*>(yrow + col0 + c + 8 * q);
-            uint4 o = f32_to_bf16x8(v + 8 * q);
-            if (add) {  // as moe_scatter_add on the bf16 GEMM output: fp32 add, one rounding
-              float fo[8], fi[8];
-              bf16x8_to_f32(*dst, fo);
-              bf16x8_to_f32(o, fi);
-#pragma unroll
-              for (int i = 0; i < 8; ++i) fo[i] = __fadd_rn(fo[i], fi[i]);
-              o = f32_to_bf16x8(fo);
-            }
-            *dst = o;
-          }
+      for (int q = 0; q < 4; ++q) {
+        const int k = 4 * h + q;  // 16-byte piece of the 128-byte row chunk
+        *reinterpret_cast<uint4*>(stage + lane * 128 + ((k ^ (lane & 7)) << 4)) = f32_to_bf16x8(z + 8 * q);
       }
     }
+    __syncwarp();
+    // the warp's rows: 4 rows x 128 bytes per store instruction
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int r = (lane >> 3) + 4 * j;
+      const int col = col0 + c + 8 * piece;
+      if (dst_j[j] >= 0 && col < n_out) {
+        uint4 o = *reinterpret_cast<const uint4*>(stage + r * 128 + ((piece ^ (r & 7)) << 4));
+        uint4* d = reinterpret_cast<uint4*>(p.y + (int64_t)dst_j[j] * n_out + col);
+        if (add) {  // as moe_scatter_add on the bf16 GEMM output: fp32 add, one rounding
+          float fo[8], fi[8];
+          bf16x8_to_f32(*d, fo);
+          bf16x8_to_f32(o, fi);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) fo[i] = __fadd_rn(fo[i], fi[i]);
+          o = f32_to_bf16x8(fo);
+        }
+        *d = o;
+      }
+    }
+    __syncwarp();  // the staging block is rewritten by the next chunk
   }
 }
 
@@ -447,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   } else {
     // ---------------------------------------------------------- epilogue
     const int sub = warp & 3;                // TMEM lane quarter this warp may access
-    const int row_in_tile = sub * 32 + lane;
+    uint8_t* scratch = smem + SmemLayout::epi + (warp - 2) * kEpiWarpBytes;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
@@ -461,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       }
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * kBN);
-      epilogue_tile<FP8>(p, t, row_in_tile, tbase, err);
+      epilogue_tile<FP8>(p, t, sub * 32, lane, tbase, scratch, err);
       tc_fence_before();
       if (NPHASE == 2 && ph == 0) {
         // publish this warp's share of the tile's z rows to the phase-1 producers
@@ -515,7 +562,8 @@ constexpr int kPairStageBytes = kPairABytes + kPairBBytes;  // 32 KB
 struct PairSmem {
   static constexpr int a = 0;
   static constexpr int b = a + kPairStages * kPairABytes;
-  static constexpr int bars = b + kPairStages * kPairBBytes;  // full[S], empty[S], tfull[2], tempty[2], drain
+  static constexpr int epi = b + kPairStages * kPairBBytes;   // [4 epilogue warps][kEpiWarpBytes]
+  static constexpr int bars = epi + kEpiBytes;                // full[S], empty[S], tfull[2], tempty[2], drain
   static constexpr int nbars = 2 * kPairStages + 2 * kAccBufs + 1;
   static constexpr int misc = bars + nbars * 8;
   static constexpr int sched = misc + 16;
@@ -795,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
   } else {
     // ---------------------------------------------------------- epilogue (both CTAs)
     const int sub = warp & 3;
-    const int row_in_tile = (int)rank * kBM + sub * 32 + lane;
+    uint8_t* scratch = smem + PairSmem::epi + (warp - 2) * kEpiWarpBytes;
     const uint32_t tempty_leader0 = map_to_rank(bar_tempty(0), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -808,7 +856,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
       }
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * kBN);
-      epilogue_tile<FP8>(p, t, row_in_tile, tbase, err);
+      epilogue_tile<FP8>(p, t, (int)rank * kBM + sub * 32, lane, tbase, scratch, err);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty_leader0 + (uint32_t)(acc * 8));
