@@ -44,17 +44,18 @@ constexpr int kBBytes = kBN * kBKBytes;          // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;   // 48 KB
 constexpr int kMaxExperts = 1024;
 // Per epilogue warp: a staging block of 32 rows x 128 bytes (one 64-column bf16
-// chunk of the warp's rows, 16-byte pieces XOR-swizzled by row) and the tile's
-// column scales (FP8).
+// chunk of the warp's rows, 16-byte pieces XOR-swizzled by row: the 128-byte
+// swizzle of a TMA tile, so a block is 1024-byte aligned) and the tile's column
+// scales (FP8).  Layout: the 4 staging blocks, then the 4 scale arrays.
 constexpr int kEpiStageBytes = 32 * 128;
-constexpr int kEpiWarpBytes = kEpiStageBytes + kBN * 4;  // 5 KB
-constexpr int kEpiBytes = 4 * kEpiWarpBytes;             // 20 KB
+constexpr int kEpiScaleBytes = kBN * 4;
+constexpr int kEpiBytes = 4 * (kEpiStageBytes + kEpiScaleBytes);  // 20 KB
 
 struct SmemLayout {
   // offsets from the 1024-aligned base
   static constexpr int a = 0;
   static constexpr int b = a + kStages * kABytes;
-  static constexpr int epi = b + kStages * kBBytes;         // [4 epilogue warps][kEpiWarpBytes]
+  static constexpr int epi = b + kStages * kBBytes;         // epilogue staging blocks and scales
   static constexpr int bars = epi + kEpiBytes;              // full[S], empty[S], tfull[2], tempty[2], drain
   static constexpr int nbars = 2 * kStages + 2 * kAccBufs + 1;
   static constexpr int misc = bars + nbars * 8;             // tmem base, abort flag, total tiles, pad
@@ -118,6 +119,7 @@ struct Phase {
   const int32_t* scatter;  // NONE epilogue only: row r goes to y[scatter[r]] (top_k = 1 combine)
   int T_out;               // rows of y when scattering
   int accumulate;          // scatter: add into y (fp32 add of the bf16 row, one rounding) or overwrite
+  int tma_store;           // y has a store tensor map (rows of a_max, 32 x 64 boxes): full row chunks use TMA
 };
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -139,12 +141,13 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 // lane), all columns of the phase's N tile.  FP8 scales, the SiLU*mul of the two
 // halves or the fused combine, then bf16 stores.  Each 64-column chunk goes
 // through the warp's staging block, so that the warp stores 4 rows x 128
-// contiguous bytes per instruction instead of 32 rows x 16 bytes.
+// contiguous bytes per instruction instead of 32 rows x 16 bytes.  With a store
+// tensor map and all 32 rows inside the tile, lane 0 writes the chunk with one
+// TMA store instead (asynchronous; the block is reused once the store has read it).
 template <bool FP8>
 __device__ __forceinline__ void epilogue_tile(const Phase& p, const Tile& t, int warp_row0, int lane, uint32_t tbase,
-                                              uint8_t* scratch, unsigned int* err) {
-  uint8_t* stage = scratch;
-  float* wsc_s = reinterpret_cast<float*>(scratch + kEpiStageBytes);
+                                              uint8_t* stage, float* wsc_s, const CUtensorMap* map_y,
+                                              unsigned int* err) {
   const int row_in_tile = warp_row0 + lane;
   const bool row_ok = row_in_tile < t.rows;
   const int row = t.row0 + row_in_tile;
@@ -183,10 +186,15 @@ __device__ __forceinline__ void epilogue_tile(const Phase& p, const Tile& t, int
 #pragma unroll
   for (int j = 0; j < 8; ++j) dst_j[j] = __shfl_sync(0xffffffffu, dst, (lane >> 3) + 4 * j);
   const bool add = p.scatter && p.accumulate;
+  const bool tma = p.tma_store && warp_row0 + 32 <= t.rows;
   const int piece = lane & 7;
   const int out_cols = silu ? kBN / 2 : kBN;
 #pragma unroll 1
   for (int c = 0; c < out_cols; c += 64) {
+    if (p.tma_store) {  // the previous TMA store from the staging block has read it
+      if (lane == 0) bulk_wait_group_read0();
+      __syncwarp();
+    }
     // the thread's row: 64 output columns as bf16 into staging row `lane`
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -237,6 +245,15 @@ __device__ __forceinline__ void epilogue_tile(const Phase& p, const Tile& t, int
         *reinterpret_cast<uint4*>(stage + lane * 128 + ((k ^ (lane & 7)) << 4)) = f32_to_bf16x8(z + 8 * q);
       }
     }
+    if (tma) {
+      fence_proxy_async_shared();  // this lane's staging writes, visible to the TMA store
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(map_y, smem_u32(stage), col0 + c, t.row0 + warp_row0);
+        bulk_commit_group();
+      }
+      continue;
+    }
     __syncwarp();
     // the warp's rows: 4 rows x 128 bytes per store instruction
 #pragma unroll
@@ -265,8 +282,8 @@ template <bool FP8, int NPHASE>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
     const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_b0,
     const __grid_constant__ CUtensorMap map_a1, const __grid_constant__ CUtensorMap map_b1,
-    const int32_t* __restrict__ counts, const Phase p0, const Phase p1, int E, int a_max, int* done,
-    unsigned int* err) {
+    const __grid_constant__ CUtensorMap map_y, const int32_t* __restrict__ counts, const Phase p0, const Phase p1,
+    int E, int a_max, int* done, unsigned int* err) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -494,7 +511,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   } else {
     // ---------------------------------------------------------- epilogue
     const int sub = warp & 3;                // TMEM lane quarter this warp may access
-    uint8_t* scratch = smem + SmemLayout::epi + (warp - 2) * kEpiWarpBytes;
+    uint8_t* stage = smem + SmemLayout::epi + (warp - 2) * kEpiStageBytes;
+    float* wsc_s = reinterpret_cast<float*>(smem + SmemLayout::epi + 4 * kEpiStageBytes + (warp - 2) * kEpiScaleBytes);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
@@ -508,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
       }
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * kBN);
-      epilogue_tile<FP8>(p, t, sub * 32, lane, tbase, scratch, err);
+      epilogue_tile<FP8>(p, t, sub * 32, lane, tbase, stage, wsc_s, &map_y, err);
       tc_fence_before();
       if (NPHASE == 2 && ph == 0) {
         // publish this warp's share of the tile's z rows to the phase-1 producers
@@ -526,6 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
         acc_phase ^= 1u;
       }
     }
+    if (lane == 0) bulk_wait_group0();  // this warp's TMA stores are complete before the block exits
   }
 
   // ---- teardown
@@ -562,7 +581,7 @@ constexpr int kPairStageBytes = kPairABytes + kPairBBytes;  // 32 KB
 struct PairSmem {
   static constexpr int a = 0;
   static constexpr int b = a + kPairStages * kPairABytes;
-  static constexpr int epi = b + kPairStages * kPairBBytes;   // [4 epilogue warps][kEpiWarpBytes]
+  static constexpr int epi = b + kPairStages * kPairBBytes;   // epilogue staging blocks and scales
   static constexpr int bars = epi + kEpiBytes;                // full[S], empty[S], tfull[2], tempty[2], drain
   static constexpr int nbars = 2 * kPairStages + 2 * kAccBufs + 1;
   static constexpr int misc = bars + nbars * 8;
@@ -625,7 +644,8 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
 template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
     const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-    const int32_t* __restrict__ counts, const Phase p, int E, int a_max, unsigned int* err) {
+    const __grid_constant__ CUtensorMap map_y, const int32_t* __restrict__ counts, const Phase p, int E, int a_max,
+    unsigned int* err) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -843,7 +863,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
   } else {
     // ---------------------------------------------------------- epilogue (both CTAs)
     const int sub = warp & 3;
-    uint8_t* scratch = smem + PairSmem::epi + (warp - 2) * kEpiWarpBytes;
+    uint8_t* stage = smem + PairSmem::epi + (warp - 2) * kEpiStageBytes;
+    float* wsc_s = reinterpret_cast<float*>(smem + PairSmem::epi + 4 * kEpiStageBytes + (warp - 2) * kEpiScaleBytes);
     const uint32_t tempty_leader0 = map_to_rank(bar_tempty(0), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -856,7 +877,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
       }
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * kBN);
-      epilogue_tile<FP8>(p, t, (int)rank * kBM + sub * 32, lane, tbase, scratch, err);
+      epilogue_tile<FP8>(p, t, (int)rank * kBM + sub * 32, lane, tbase, stage, wsc_s, &map_y, err);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty_leader0 + (uint32_t)(acc * 8));
@@ -865,6 +886,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
         acc_phase ^= 1u;
       }
     }
+    if (lane == 0) bulk_wait_group0();  // this warp's TMA stores are complete before the block exits
   }
 
   // ---- teardown: the pair meets, then frees its tensor memory together
@@ -899,13 +921,14 @@ Phase make_phase(int N, int K, int epi, bool fp8, void* y, const float* xs, cons
   p.scatter = nullptr;
   p.T_out = 0;
   p.accumulate = 0;
+  p.tma_store = 0;
   return p;
 }
 
 template <bool FP8, int NPHASE>
 cudaError_t launch_phases(const CUtensorMap& a0, const CUtensorMap& b0, const CUtensorMap& a1,
-                          const CUtensorMap& b1, const int32_t* counts, const Phase& p0, const Phase& p1, int E,
-                          int a_max, int* done, unsigned int* err, cudaStream_t s) {
+                          const CUtensorMap& b1, const CUtensorMap& y, const int32_t* counts, const Phase& p0,
+                          const Phase& p1, int E, int a_max, int* done, unsigned int* err, cudaStream_t s) {
   const int smem = SmemLayout::bytes_for(E) + 1024;
   auto kern = grouped_gemm_kernel<FP8, NPHASE>;
   // The attribute is per device; setting it on every call is cheap and keeps multi-device use correct.
@@ -930,14 +953,14 @@ cudaError_t launch_phases(const CUtensorMap& a0, const CUtensorMap& b0, const CU
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  e = cudaLaunchKernelEx(&cfg, kern, a0, b0, a1, b1, counts, p0, p1, E, a_max, done, err);
+  e = cudaLaunchKernelEx(&cfg, kern, a0, b0, a1, b1, y, counts, p0, p1, E, a_max, done, err);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 template <bool FP8>
-cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const int32_t* counts, const Phase& p, int E,
-                        int a_max, unsigned int* err, cudaStream_t s) {
+cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& y, const int32_t* counts,
+                        const Phase& p, int E, int a_max, unsigned int* err, cudaStream_t s) {
   const int smem = PairSmem::bytes_for(E) + 1024;
   auto kern = grouped_gemm_pair_kernel<FP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -961,7 +984,7 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const int32_
   const int64_t tiles_ub = ((int64_t)(a_max + kPairBM - 1) / kPairBM + E) * p.n_tiles;
   const int nclusters = (int)(tiles_ub < max_clusters ? tiles_ub : max_clusters);
   cfg.gridDim = dim3(2 * nclusters);
-  e = cudaLaunchKernelEx(&cfg, kern, a, b, counts, p, E, a_max, err);
+  e = cudaLaunchKernelEx(&cfg, kern, a, b, y, counts, p, E, a_max, err);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -977,12 +1000,15 @@ cudaError_t launch_grouped_gemm(const GemmArgs& g, cudaStream_t s) {
   p.scatter = g.scatter;
   p.T_out = g.T_out;
   p.accumulate = g.accumulate;
+  // rows stored in place (no combine): full 32-row chunks go out as TMA stores when y admits a map
+  CUtensorMap my = mb;
+  if (!g.scatter) p.tma_store = make_map_sw128(&my, g.y, g.a_max, p.n_out, false, 32) ? 1 : 0;
   if (g.pairs) {
-    if (g.fp8) return launch_pair<true>(ma, mb, g.counts, p, g.E, g.a_max, g.err, s);
-    return launch_pair<false>(ma, mb, g.counts, p, g.E, g.a_max, g.err, s);
+    if (g.fp8) return launch_pair<true>(ma, mb, my, g.counts, p, g.E, g.a_max, g.err, s);
+    return launch_pair<false>(ma, mb, my, g.counts, p, g.E, g.a_max, g.err, s);
   }
-  if (g.fp8) return launch_phases<true, 1>(ma, mb, ma, mb, g.counts, p, p, g.E, g.a_max, nullptr, g.err, s);
-  return launch_phases<false, 1>(ma, mb, ma, mb, g.counts, p, p, g.E, g.a_max, nullptr, g.err, s);
+  if (g.fp8) return launch_phases<true, 1>(ma, mb, ma, mb, my, g.counts, p, p, g.E, g.a_max, nullptr, g.err, s);
+  return launch_phases<false, 1>(ma, mb, ma, mb, my, g.counts, p, p, g.E, g.a_max, nullptr, g.err, s);
 }
 
 size_t expert_mlp_workspace_bytes(int E) { return ((size_t)E * sizeof(int) + 255) / 256 * 256; }
@@ -1001,7 +1027,7 @@ cudaError_t launch_expert_mlp(const MlpArgs& g, cudaStream_t s) {
   int* done = static_cast<int*>(g.ws);
   cudaError_t e = cudaMemsetAsync(done, 0, sizeof(int) * g.E, s);
   if (e != cudaSuccess) return e;
-  return launch_phases<false, 2>(a0, b0, a1, b1, g.counts, p0, p1, g.E, g.a_max, done, g.err, s);
+  return launch_phases<false, 2>(a0, b0, a1, b1, b1, g.counts, p0, p1, g.E, g.a_max, done, g.err, s);
 }
 
 }  // namespace moe
