@@ -555,9 +555,10 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
 # summarised under profiles/, with the hash of the kernel sources they were taken
 # on: when those sources change the figure no longer applies and is reported as null.
 TRAFFIC: dict = {
-    ("decode", "expert_mlp"): (4_037_737_472 + 5_864_704, "grouped_gemm.cu", "b630aad71443"),
-    ("prefill_fp8", "gemm_w13"): (1_386_704_128 + 249_189_632, "grouped_gemm.cu", "b630aad71443"),
-    ("padded_fp8", "gather_quant"): (93_194_752 + 118_310_400, "rowwise.cu", "4a5af973a02e"),
+    ("decode", "expert_mlp"): (4_037_187_072 + 5_716_480, "grouped_gemm.cu", "63842ba06724"),
+    ("prefill_fp8", "gemm_w13"): (1_386_034_432 + 251_709_184, "grouped_gemm.cu", "63842ba06724"),
+    ("fine_grained", "gemm_w13_silu"): (2_638_180_608 + 134_259_968, "grouped_gemm.cu", "63842ba06724"),
+    ("padded_fp8", "gemm_w13"): (1_793_399_552 + 257_138_176, "grouped_gemm.cu", "63842ba06724"),
 }
 
 
