@@ -329,9 +329,12 @@ int moe_grouped_gemm_fp8_rowwise(const void* x, const void* w, const int32_t* co
  * of e has stored its z rows, so the w2 work fills the tail of the w13 work.
  * x [a_max, D], w13 [E, 2H, D], w2 [E, D, H], z [a_max, H] (written: it is
  * the intermediate), y [a_max, D]; all bf16.  counts [E] device int32.
- * ws: device workspace of moe_expert_mlp_workspace_size(E) bytes (contents on
- * entry do not matter).  All CTAs must be resident at once (a cooperative
- * launch); MOE_ERR_CUDA if the device cannot host them.  D, H multiples of 16.
+ * ws: device workspace of moe_expert_mlp_workspace_size(E) bytes: per-expert
+ * counters that must be zero before the first call (cudaMemset); every call
+ * leaves them zero again, including one that stops on a device error, so a
+ * workspace is zeroed once and reused.  One workspace serves one call at a time.
+ * All CTAs must be resident at once (a cooperative launch); MOE_ERR_CUDA if the
+ * device cannot host them.  D, H multiples of 16.
  * scatter_indices, T_out, accumulate: the fused top_k = 1 combine of the w2
  * GEMM, as in moe_grouped_gemm (y is then out [T_out, D]).
  */

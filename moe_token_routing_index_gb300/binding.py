@@ -325,8 +325,8 @@ def moe_expert_mlp(x, w13, w2, counts, *, z=None, out=None, scatter_indices=None
     if out is None:
         out = torch.empty(a_max, D, dtype=torch.bfloat16, device=x.device)
     _need(out, out.dtype, "out")
-    if workspace is None:
-        workspace = torch.empty(moe_expert_mlp_workspace_size(E), dtype=torch.uint8, device=x.device)
+    if workspace is None:   # zero on first use; each call leaves it zero
+        workspace = torch.zeros(moe_expert_mlp_workspace_size(E), dtype=torch.uint8, device=x.device)
     st = _lib.moe_expert_mlp(_ptr(x), _ptr(w13), _ptr(w2), _ptr(counts), E, a_max, D, H, _ptr(z), _ptr(out),
                              _ptr(si), t_out, acc, _ptr(workspace), workspace.numel(), _stream(stream))
     _check("moe_expert_mlp", st)

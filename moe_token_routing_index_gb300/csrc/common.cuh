@@ -64,6 +64,25 @@ __device__ __forceinline__ bool grid_barrier(unsigned int* counter, unsigned int
   return s_ok != 0;
 }
 
+// Programmatic dependent launch.  launch_dependents: the next kernel of the
+// stream may start now (its blocks run their prologue beside this grid);
+// wait: block until the previous kernel of the stream has completed and its
+// writes are visible.  Both are no-ops in a kernel launched without the
+// programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Host: the launch attribute that lets a kernel start while the previous one in
+// the stream runs (it must pdl_wait() before touching that kernel's results).
+inline cudaLaunchAttribute pdl_attribute() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
 // A routing score; NULL scores read as 1.0 (the gathers then copy rows unscaled).
 __device__ __forceinline__ float load_score(const void* scores, int dtype, int64_t off) {
   if (!scores) return 1.0f;

@@ -553,6 +553,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   tc_fence_after();
   if (warp == 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols) : "memory");
+  if (NPHASE == 2 && threadIdx.x == 0) {
+    // The last CTA to finish (every other CTA is past its waits on the counters)
+    // leaves done[0..E] zero for the next launch, on every path including aborts.
+    __threadfence();
+    if (atomicAdd(done + E, 1) == (int)gridDim.x - 1) {
+      for (int e = 0; e <= E; ++e) done[e] = 0;
+      __threadfence();
+    }
+  }
 }
 
 // ------------------------------------------------- CTA-pair kernel (2 SMs)
@@ -1011,7 +1020,8 @@ cudaError_t launch_grouped_gemm(const GemmArgs& g, cudaStream_t s) {
   return launch_phases<false, 1>(ma, mb, ma, mb, my, g.counts, p, p, g.E, g.a_max, nullptr, g.err, s);
 }
 
-size_t expert_mlp_workspace_bytes(int E) { return ((size_t)E * sizeof(int) + 255) / 256 * 256; }
+// Per-expert z-row counters and an exit counter; zero between launches.
+size_t expert_mlp_workspace_bytes(int E) { return ((size_t)(E + 1) * sizeof(int) + 255) / 256 * 256; }
 
 cudaError_t launch_expert_mlp(const MlpArgs& g, cudaStream_t s) {
   if (g.E > kMaxExperts) return cudaErrorNotSupported;
@@ -1024,9 +1034,7 @@ cudaError_t launch_expert_mlp(const MlpArgs& g, cudaStream_t s) {
   p1.scatter = g.scatter;
   p1.T_out = g.T_out;
   p1.accumulate = g.accumulate;
-  int* done = static_cast<int*>(g.ws);
-  cudaError_t e = cudaMemsetAsync(done, 0, sizeof(int) * g.E, s);
-  if (e != cudaSuccess) return e;
+  int* done = static_cast<int*>(g.ws);  // zero on entry, left zero by the kernel
   return launch_phases<false, 2>(a0, b0, a1, b1, b1, g.counts, p0, p1, g.E, g.a_max, done, g.err, s);
 }
 

@@ -174,6 +174,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_coop_kernel(
   __shared__ int s_a[1024];          // select: histogram; emit: expert offsets
   __shared__ unsigned int s_bits[1024];
   __shared__ int s_part[kRouteThreads];
+  pdl_launch_dependents();  // the gather may launch and wait for this grid
   const int Tv = read_count(num_valid, T, err);
   const int nchunks = (Tv + kTokBlock - 1) / kTokBlock;
   // chunks past the valid tokens still publish an empty histogram
@@ -243,6 +244,7 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
   int* s_hist = reinterpret_cast<int*>(s_key + (size_t)T * E);        // [warps][E]: counts, then bases
   int* s_off = s_hist + kSmallWarps * E;                               // [E + 1]
   uint16_t* s_chosen = reinterpret_cast<uint16_t*>(s_off + E + 1);     // [T][k]
+  pdl_launch_dependents();  // the gather may launch and wait for this grid
   const int Tv = read_count(num_valid, T, err);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < Tv * E; i += kSmallThreads) {

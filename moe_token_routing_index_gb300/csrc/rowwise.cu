@@ -91,6 +91,8 @@ __global__ void __launch_bounds__(kThreads) gather_scale_kernel(
     const uint4* __restrict__ x, int T, int D8, const int32_t* __restrict__ ti, const int32_t* __restrict__ ei,
     int a, const void* __restrict__ scores, int dtype, int64_t st, int64_t se, int E,
     const int32_t* __restrict__ valid_p, uint4* __restrict__ out, unsigned int* err) {
+  pdl_launch_dependents();  // the next kernel may start its prologue
+  pdl_wait();               // the routing written by the previous kernel is visible
   const int valid = read_count(valid_p, a, err);
   const int lane = threadIdx.x & 31;
   const int chunks = (D8 + kGatherChunk - 1) / kGatherChunk;
@@ -309,6 +311,8 @@ __global__ void __launch_bounds__(kStagedMaxWarps * 32, 1) gather_staged_kernel(
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);                      // [warps][NB]
   int* s_tok = reinterpret_cast<int*>(smem + nwb * NB * 8);                // [warps][NB]: staged token or -1
   uint8_t* slots = smem + ((nwb * NB * 16 + 127) / 128) * 128;             // [warps][NB][row_bytes]
+  pdl_launch_dependents();  // the next kernel may start its prologue
+  pdl_wait();               // the routing written by the previous kernel is visible
   const int valid = read_count(valid_p, a, err);
   const int nrows = inv ? k : 1;  // routed rows per item
   int items = valid;
@@ -484,9 +488,18 @@ cudaError_t launch_staged(const GatherArgs& g, StagedShape sh, cudaStream_t s) {
   const int64_t items = g.inv ? std::min<int64_t>(g.a / g.top_k, g.T) : g.a;
   const int64_t need = (items + sh.warps - 1) / sh.warps;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(need, device_sm_count()));
-  kern<<<grid, sh.warps * 32, smem, s>>>(static_cast<const uint4*>(g.x), g.T, D8, g.token_indices,
-                                         g.expert_indices, g.inv, g.top_k, g.a, g.scores, g.dtype, g.stride_t,
-                                         g.stride_e, g.E, g.valid, g.scale_ub, g.out, g.out_scale, nb, g.err);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(sh.warps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};  // may start while the router's kernel runs
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, static_cast<const uint4*>(g.x), g.T, D8, g.token_indices, g.expert_indices,
+                         g.inv, g.top_k, g.a, g.scores, g.dtype, g.stride_t, g.stride_e, g.E, g.valid, g.scale_ub,
+                         g.out, g.out_scale, nb, g.err);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -843,9 +856,17 @@ cudaError_t launch_gather_scale(const GatherArgs& g, cudaStream_t s) {
   }
   const int grid =
       persistent_grid(gather_scale_kernel, (int64_t)g.a * ((g.D / 8 + kGatherChunk - 1) / kGatherChunk), kWarps);
-  gather_scale_kernel<<<grid, kThreads, 0, s>>>(static_cast<const uint4*>(g.x), g.T, g.D / 8, g.token_indices,
-                                                g.expert_indices, g.a, g.scores, g.dtype, g.stride_t, g.stride_e,
-                                                g.E, g.valid, static_cast<uint4*>(g.out), g.err);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};  // may start while the router's kernel runs
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gather_scale_kernel, static_cast<const uint4*>(g.x), g.T, g.D / 8,
+                                     g.token_indices, g.expert_indices, g.a, g.scores, g.dtype, g.stride_t,
+                                     g.stride_e, g.E, g.valid, static_cast<uint4*>(g.out), g.err);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -160,7 +160,8 @@ class MoELayer:
         if self.weighting == "output":
             route["topk_weights"] = torch.zeros(a, **f32)
         ws = torch.empty(max(mb.moe_route_workspace_size(T, E, k), 256), dtype=torch.uint8, device=device)
-        mlp_ws = torch.empty(mb.moe_expert_mlp_workspace_size(max(E, 1)), dtype=torch.uint8, device=device)
+        # zero on first use; the expert MLP leaves it zero
+        mlp_ws = torch.zeros(mb.moe_expert_mlp_workspace_size(max(E, 1)), dtype=torch.uint8, device=device)
         if self.fp8:
             b = _Buffers(T, route, ws, mlp_ws, torch.empty(a, D, **e4), torch.empty(a, **f32),
                          torch.empty(a, 2 * H, **bf), torch.empty(a, H, **e4), torch.empty(a, **f32),
@@ -179,7 +180,7 @@ class MoELayer:
             x["ident"] = torch.arange(T, **i32)
             if self.weighting == "output":
                 x["sh_out"] = torch.empty(T, D, **bf)           # the finalize adds it to the weighted sum
-            x["sh_mlp_ws"] = torch.empty(mb.moe_expert_mlp_workspace_size(1), dtype=torch.uint8, device=device)
+            x["sh_mlp_ws"] = torch.zeros(mb.moe_expert_mlp_workspace_size(1), dtype=torch.uint8, device=device)
             if self.fp8:
                 x["zero"] = torch.zeros(T, **i32)
                 x["unit"] = torch.ones(T, 1, **f32)           # unit scores: the gather's product is exact

@@ -200,6 +200,32 @@ def test_expert_mlp_one_launch_equals_two(E, counts, D, H, a_max):
     assert is_sentinel(y[a:])
 
 
+def test_expert_mlp_leaves_its_workspace_zero():
+    """The per-expert counters of moe_expert_mlp start at zero and every call leaves them
+    zero (the last block to finish resets them): three route -> gather -> MLP passes on one
+    workspace agree bit for bit, and the workspace reads zero after each."""
+    mb = _mb()
+    g = torch.Generator().manual_seed(11)
+    E, D, H, T = 16, 512, 1024, 128
+    x = torch.randn(T, D, generator=g).to(torch.bfloat16).cuda()
+    s = torch.rand(T, E, generator=g).to(torch.bfloat16).cuda()
+    w13 = (torch.randn(E, 2 * H, D, generator=g) * 0.1).to(torch.bfloat16).cuda()
+    w2 = (torch.randn(E, D, H, generator=g) * 0.1).to(torch.bfloat16).cuda()
+    ws = torch.zeros(mb.moe_expert_mlp_workspace_size(E), dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(3):
+        r = mb.moe_route(s, 1)
+        xr = mb.moe_gather_scale(x, r["token_indices"], r["expert_indices"], s)
+        outs.append(mb.moe_expert_mlp(xr, w13, w2, r["counts"], workspace=ws).clone())
+        torch.cuda.synchronize()
+        assert int(ws.count_nonzero()) == 0
+    assert mb.device_error() == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    cnt = r["counts"][:E]
+    z_ref = mb.moe_grouped_gemm(xr, w13, cnt, epilogue=mb.MOE_EPILOGUE_SILU_MUL)
+    assert torch.equal(outs[0], mb.moe_grouped_gemm(z_ref, w2, cnt))
+
+
 @pytest.mark.parametrize("name", ["decode", "fine_grained"])
 def test_expert_mlp_workloads_equal_two_launches(name):
     mb = _mb()
