@@ -237,6 +237,10 @@ int moe_route_no_alloc(const void* scores, int scores_dtype, int64_t stride_t, i
  * (and top_k > 1) the rows are produced token by token, each x row read from
  * HBM once for its top_k routed rows; valid_token_count must then be
  * Tv * top_k.  The output is the same either way.
+ * Launch: with programmatic stream serialization, so the kernel may start
+ * while the previous kernel in the stream (moe_route) still runs.  It waits for
+ * that kernel to finish before reading anything, so stream order holds for
+ * every input.
  */
 int moe_gather_scale(const void* x, int T, int D, const int32_t* token_indices,
                      const int32_t* expert_indices, int a, const void* scores, int scores_dtype,
@@ -253,7 +257,7 @@ int moe_gather_scale(const void* x, int T, int D, const int32_t* token_indices,
  *   out[i, j] = e4m3( clamp(v_j * s, -448, 448) ), round to nearest even.
  * All arithmetic is IEEE fp32 (correctly rounded division and reciprocal).
  * out [a, D] e4m3, out_scale [a] fp32.  Rows i >= valid are not written.
- * inv_rows, top_k: as in moe_gather_scale.
+ * inv_rows, top_k, launch: as in moe_gather_scale.
  */
 int moe_gather_scale_quant(const void* x, int T, int D, const int32_t* token_indices,
                            const int32_t* expert_indices, int a, const void* scores,
