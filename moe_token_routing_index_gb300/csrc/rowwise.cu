@@ -6,10 +6,12 @@
 //   per-row FP8 quantisation of weight matrices
 //
 // Every kernel moves rows in 16-byte vectors (8 bf16 / 16 e4m3 / 4 fp32),
-// coalesced across a warp, on a persistent grid of (SMs x 8) 256-thread
-// blocks.  Plain stages give one warp a row; quantising stages give a group
-// of 1-8 warps a row, held in registers between the row-max reduction and
-// the quantisation, so each input byte is read from HBM once.
+// coalesced across a warp, on a persistent grid sized to the blocks the SMs
+// hold at once.  Plain stages give a warp (row, chunk) items; the register
+// quantising stages give a group of 1-8 warps a row, held in registers between
+// the row-max reduction and the quantisation.  The staged gathers (one block of
+// 8-16 warps per SM) copy whole x rows into shared memory with bulk copies.
+// Each input byte is read from HBM once.
 #include <algorithm>
 
 #include "common.cuh"
