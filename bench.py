@@ -555,17 +555,28 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
 # summarised under profiles/, with the hash of the kernel sources they were taken
 # on: when those sources change the figure no longer applies and is reported as null.
 TRAFFIC: dict = {
-    ("decode", "expert_mlp"): (4_037_415_680 + 5_957_120, "grouped_gemm.cu", "b430d0018ee8"),
-    ("prefill_fp8", "gemm_w13"): (1_385_645_312 + 251_086_848, "grouped_gemm.cu", "b430d0018ee8"),
-    ("fine_grained", "gemm_w13_silu"): (2_396_568_064 + 133_899_264, "grouped_gemm.cu", "b430d0018ee8"),
-    ("padded_fp8", "gemm_w13"): (1_793_024_256 + 256_110_336, "grouped_gemm.cu", "b430d0018ee8"),
+    ("decode", "expert_mlp"): (4_037_415_680 + 5_957_120, "grouped_gemm.cu", "22ff66a37199"),
+    ("prefill_fp8", "gemm_w13"): (1_385_645_312 + 251_086_848, "grouped_gemm.cu", "22ff66a37199"),
+    ("fine_grained", "gemm_w13_silu"): (2_396_568_064 + 133_899_264, "grouped_gemm.cu", "22ff66a37199"),
+    ("padded_fp8", "gemm_w13"): (1_793_024_256 + 256_110_336, "grouped_gemm.cu", "22ff66a37199"),
 }
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without comments and with whitespace runs collapsed, so that an edit
+    of comments or layout does not retire a figure taken on the same code."""
+    import re
+
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(name: str) -> str:
-    """sha1 (12 hex digits) of a kernel source and every local header it reaches through
-    `#include "..."`, in first-reach order: counters captured on one build are reported only
-    while none of those files has changed."""
+    """sha1 (12 hex digits) of the code of a kernel source and of every local header it
+    reaches through `#include "..."`, in first-reach order (comments and whitespace
+    dropped): counters captured on one build are reported only while that code is
+    unchanged."""
     import hashlib
     import re
 
@@ -584,7 +595,7 @@ def kernel_source_hash(name: str) -> str:
     visit(csrc / name)
     h = hashlib.sha1()
     for f in order:
-        h.update(f.read_bytes())
+        h.update(_code_only(f.read_text()).encode())
     return h.hexdigest()[:12]
 
 

@@ -1,6 +1,7 @@
 """The traffic figures bench.py reports: each names a kernel source that exists and a
-(workload, stage) pair the bench can report, and the source hash covers every local
-header the source includes, so a change to any of them retires the figure."""
+(workload, stage) pair the bench can report, and the source hash covers the code of every
+local header the source includes, so a code change in any of them retires the figure
+while an edit of comments does not."""
 import re
 
 import bench
@@ -32,6 +33,8 @@ def test_source_hash_follows_includes(tmp_path, monkeypatch):
     h0 = bench.kernel_source_hash("k.cu")
     (pkg / "unrelated.cuh").write_text("int u2;\n")
     assert bench.kernel_source_hash("k.cu") == h0
+    (tmp_path / "include" / "x.h").write_text("// a comment\nint   x; /* and another */\n")
+    assert bench.kernel_source_hash("k.cu") == h0          # comments and layout do not count
     (tmp_path / "include" / "x.h").write_text("int x2;\n")
     assert bench.kernel_source_hash("k.cu") != h0
 
