@@ -712,7 +712,12 @@ __global__ void __launch_bounds__(kThreads) scatter_add_rows_kernel(uint4* __res
 // With the inverse permutation: a warp owns a (token, chunk) item and adds
 // the token's top_k rows in ascending row order into an fp32 accumulator
 // started from out[t] (ACC) or from zero.
-template <bool ACC>
+// top_k > 1 with the inverse permutation: a warp owns a (token, chunk) item and
+// sums the token's top_k rows in slot order, in fp32, onto out (ACC) or zero.
+// K > 0: top_k fixed at compile time, so every row load of the item is issued
+// before the first add (K rows x U vectors per lane in flight); K == 0: any
+// top_k, one row at a time.  U: 16-byte vectors per lane per row.
+template <bool ACC, int K, int U>
 __global__ void __launch_bounds__(kThreads) scatter_add_tokens_kernel(uint4* __restrict__ out,
                                                                       const uint4* __restrict__ in,
                                                                       const int32_t* __restrict__ inv, int k, int a,
@@ -725,11 +730,12 @@ __global__ void __launch_bounds__(kThreads) scatter_add_tokens_kernel(uint4* __r
   int Tv = valid / k;
   if (Tv > T) Tv = T;
   const int lane = threadIdx.x & 31;
-  const int chunks = (D8 + kChunk - 1) / kChunk;
+  constexpr int kItem = 32 * U;  // vectors of a row per item
+  const int chunks = (D8 + kItem - 1) / kItem;
   const int64_t items = (int64_t)Tv * chunks;
   for (int64_t it = global_warp(); it < items; it += num_warps()) {
     const int t = (int)(it / chunks);
-    const int c0 = (int)(it - (int64_t)t * chunks) * kChunk + lane;
+    const int c0 = (int)(it - (int64_t)t * chunks) * kItem + lane;
     int my_row = 0;
     bool bad = false;
     if (lane < k) {
@@ -741,9 +747,9 @@ __global__ void __launch_bounds__(kThreads) scatter_add_tokens_kernel(uint4* __r
       continue;
     }
     uint4* o = out + (int64_t)t * D8;
-    float acc[kUnroll][8];
+    float acc[U][8];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
       if (ACC && c0 + 32 * u < D8) {
         bf16x8_to_f32(o[c0 + 32 * u], acc[u]);
       } else {
@@ -751,28 +757,44 @@ __global__ void __launch_bounds__(kThreads) scatter_add_tokens_kernel(uint4* __r
         for (int i = 0; i < 8; ++i) acc[u][i] = 0.0f;
       }
     }
-    for (int j = 0; j < k; ++j) {
-      const int r = (j < 32) ? __shfl_sync(0xffffffffu, my_row, j) : __ldg(inv + (int64_t)t * k + j);
-      if ((unsigned)r >= (unsigned)a) {  // only reachable for top_k > 32
-        flag_error(err, MOE_DEVERR_BAD_INDEX);
-        continue;
-      }
-      const uint4* src = in + (int64_t)r * D8;
-      uint4 v[kUnroll];
+    auto add_row = [&](const uint4* v) {
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u)
-        if (c0 + 32 * u < D8) v[u] = __ldg(src + c0 + 32 * u);
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u)
+      for (int u = 0; u < U; ++u)
         if (c0 + 32 * u < D8) {
           float fi[8];
           bf16x8_to_f32(v[u], fi);
 #pragma unroll
           for (int i = 0; i < 8; ++i) acc[u][i] = __fadd_rn(acc[u][i], fi[i]);
         }
+    };
+    if constexpr (K > 0) {
+      uint4 v[K][U];
+#pragma unroll
+      for (int j = 0; j < K; ++j) {
+        const uint4* src = in + (int64_t)__shfl_sync(0xffffffffu, my_row, j) * D8;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (c0 + 32 * u < D8) v[j][u] = __ldg(src + c0 + 32 * u);
+      }
+#pragma unroll
+      for (int j = 0; j < K; ++j) add_row(v[j]);
+    } else {
+      for (int j = 0; j < k; ++j) {
+        const int r = (j < 32) ? __shfl_sync(0xffffffffu, my_row, j) : __ldg(inv + (int64_t)t * k + j);
+        if ((unsigned)r >= (unsigned)a) {  // only reachable for top_k > 32
+          flag_error(err, MOE_DEVERR_BAD_INDEX);
+          continue;
+        }
+        const uint4* src = in + (int64_t)r * D8;
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (c0 + 32 * u < D8) v[u] = __ldg(src + c0 + 32 * u);
+        add_row(v);
+      }
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
+    for (int u = 0; u < U; ++u)
       if (c0 + 32 * u < D8) o[c0 + 32 * u] = f32_to_bf16x8(acc[u]);
   }
 }
@@ -944,10 +966,21 @@ cudaError_t launch_silu_mul_quant(const SiluArgs& g, cudaStream_t s) {
 cudaError_t launch_scatter_add(const ScatterArgs& g, cudaStream_t s) {
   const int D8 = g.D / 8;
   if (g.inv) {
-    auto k = g.accumulate ? scatter_add_tokens_kernel<true> : scatter_add_tokens_kernel<false>;
-    const int grid = persistent_grid(k, (int64_t)g.T * ((D8 + kChunk - 1) / kChunk), kWarps);
-    k<<<grid, kThreads, 0, s>>>(static_cast<uint4*>(g.out), static_cast<const uint4*>(g.in), g.inv, g.top_k, g.a,
-                                g.T, D8, g.valid, g.sum_counts, g.E, g.err);
+    // the common top_k values get every row load of an item in flight at once
+#define MOE_SCATTER_TOKENS(K, U)                                                                                   \
+  do {                                                                                                             \
+    auto k = g.accumulate ? scatter_add_tokens_kernel<true, K, U> : scatter_add_tokens_kernel<false, K, U>;         \
+    const int grid = persistent_grid(k, (int64_t)g.T * ((D8 + 32 * U - 1) / (32 * U)), kWarps);                   \
+    k<<<grid, kThreads, 0, s>>>(static_cast<uint4*>(g.out), static_cast<const uint4*>(g.in), g.inv, g.top_k, g.a, \
+                                g.T, D8, g.valid, g.sum_counts, g.E, g.err);                                       \
+  } while (0)
+    switch (g.top_k) {
+      case 2: MOE_SCATTER_TOKENS(2, 4); break;
+      case 4: MOE_SCATTER_TOKENS(4, 4); break;
+      case 8: MOE_SCATTER_TOKENS(8, 2); break;
+      default: MOE_SCATTER_TOKENS(0, 4); break;
+    }
+#undef MOE_SCATTER_TOKENS
   } else {
     auto k = g.accumulate ? scatter_add_rows_kernel<true> : scatter_add_rows_kernel<false>;
     const int grid = persistent_grid(k, (int64_t)g.a * ((D8 + kChunk - 1) / kChunk), kWarps);

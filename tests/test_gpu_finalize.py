@@ -65,7 +65,8 @@ def test_unit_score_gathers_copy_rows(quant, name):
 @pytest.mark.parametrize("n,D,M,k,Mv,wdt,with_shared",
                          [(500, 256, 300, 4, 300, "f32", True), (44000, 4096, 11000, 4, 11000, "f32", False),
                           (70, 7168, 40, 8, 33, "bf16", True), (9, 16, 5, 1, 5, "f32", False),
-                          (64, 2064, 64, 2, 60, "bf16", False)])
+                          (64, 2064, 64, 2, 60, "bf16", False), (120, 512, 50, 3, 47, "f32", True),
+                          (300, 272, 90, 5, 90, "bf16", False), (200, 128, 12, 40, 11, "f32", True)])
 def test_topk_finalize_bit_exact(n, D, M, k, Mv, wdt, with_shared):
     mb = _mb()
     g = torch.Generator().manual_seed(n + D + M)

@@ -171,6 +171,28 @@ def test_scatter_add_bit_exact(name, use_inv):
     assert torch.equal(out2[Tv:].cpu(), init[Tv:])
 
 
+@pytest.mark.parametrize("T,D,E,k", [(300, 256, 8, 2), (97, 2064, 12, 3), (64, 512, 16, 5), (13, 144, 48, 40)])
+@pytest.mark.parametrize("accumulate", [False, True])
+def test_scatter_add_inverse_any_top_k(T, D, E, k, accumulate):
+    """The inverse-permutation combine for top_k values with and without a specialised
+    kernel (2, and 3, 5, 40 on the generic one): bit-exact against the oracle, in both
+    the overwrite and the accumulate mode."""
+    mb = _mb()
+    g = torch.Generator().manual_seed(T + D + k)
+    s = torch.rand(T, E, generator=g).to(torch.bfloat16)
+    r = oracle.route(bits(s), k)
+    a = T * k
+    rows = (torch.randn(a, D, generator=g) * 3).to(torch.bfloat16)
+    init = torch.randn(T, D, generator=g).to(torch.bfloat16)
+    out = init.cuda()
+    mb.moe_scatter_add(out, rows.cuda(), _idx(r["token_indices"]), _idx(r["inv"].ravel()), k,
+                       torch.tensor([a], dtype=torch.int32, device="cuda"), accumulate=accumulate)
+    assert mb.device_error() == 0
+    base = bits(init).copy() if accumulate else np.zeros((T, D), np.uint16)   # overwrite = adding into zeros
+    ref = oracle.scatter_add(base, bits(rows), r["token_indices"])
+    np.testing.assert_array_equal(bits(out), ref)
+
+
 @pytest.mark.parametrize("name", ["fine_grained", "padded_fp8", "tiny"])
 @pytest.mark.parametrize("quant", [False, True])
 def test_token_major_gather_equals_row_major(name, quant):
