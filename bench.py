@@ -382,18 +382,22 @@ def run_e2e(args, cfg, layer, x, s, nv, out, world):
     step copies its inputs host -> device and its result device -> host.  Steps
     are pipelined over two buffer slots, as a serving loop would run them: the
     inputs of step i+1 and the result of step i-1 move on two copy streams
-    while step i computes.  The timed region spans all K steps, copies included."""
+    while step i computes.  The timed region spans all K steps, copies included.
+    Only the valid tokens move (the first Tv rows of x, of the scores and of the
+    result): the padding rows of a fixed-size token buffer are neither inputs nor
+    results (the layer leaves them untouched)."""
     import torch
     import torch.distributed as dist
 
     K = args.steps
     slots = 2
+    Tv = cfg.valid_tokens
     comp = torch.cuda.current_stream()
     h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
-    xh = [x.cpu().pin_memory() for _ in range(slots)]
-    sh = [None if s is None else s.cpu().pin_memory() for _ in range(slots)]   # the whole layer routes itself
+    xh = [x[:Tv].cpu().pin_memory() for _ in range(slots)]
+    sh = [None if s is None else s[:Tv].cpu().pin_memory() for _ in range(slots)]   # the whole layer routes itself
     nvh = [None if nv is None else nv.cpu().pin_memory() for _ in range(slots)]
-    outh = [torch.empty(cfg.T, cfg.D, dtype=torch.bfloat16).pin_memory() for _ in range(slots)]
+    outh = [torch.empty(Tv, cfg.D, dtype=torch.bfloat16).pin_memory() for _ in range(slots)]
     xd = [torch.empty_like(x) for _ in range(slots)]
     sd = [None if s is None else torch.empty_like(s) for _ in range(slots)]
     nvd = [None if nv is None else torch.empty_like(nv) for _ in range(slots)]
@@ -409,9 +413,9 @@ def run_e2e(args, cfg, layer, x, s, nv, out, world):
         j = i % slots
         with torch.cuda.stream(h2d_s):
             h2d_s.wait_event(ev_comp[j])           # the compute that read this slot is done
-            xd[j].copy_(xh[j], non_blocking=True)
+            xd[j][:Tv].copy_(xh[j], non_blocking=True)
             if sd[j] is not None:
-                sd[j].copy_(sh[j], non_blocking=True)
+                sd[j][:Tv].copy_(sh[j], non_blocking=True)
             if nvd[j] is not None:
                 nvd[j].copy_(nvh[j], non_blocking=True)
             ev_in[j].record(h2d_s)
@@ -421,7 +425,7 @@ def run_e2e(args, cfg, layer, x, s, nv, out, world):
         ev_comp[j].record(comp)
         with torch.cuda.stream(d2h_s):
             d2h_s.wait_event(ev_comp[j])
-            outh[j].copy_(outd[j], non_blocking=True)
+            outh[j].copy_(outd[j][:Tv], non_blocking=True)
             ev_out[j].record(d2h_s)
 
     for i in range(max(2, min(args.warmup, 10))):
