@@ -70,6 +70,13 @@ extern "C" {
  * experts hold many rows; an expert whose rows end mid-tile still pays for the
  * whole 256-row tile. */
 #define MOE_GEMM_CTA_PAIRS 0x100
+/* OR-ed into `epilogue` of the grouped GEMMs (and passed in `flags` of
+ * moe_expert_mlp): w points to weights in the tile-packed layout of
+ * moe_pack_weights instead of row-major [E, N, K].  Same results; the weights
+ * stream from HBM as contiguous 16 KB boxes instead of 128-byte pieces of 128
+ * rows (decode expert MLP: 602 -> 564 us).  Needs N % 128 == 0 (and (N / 2) % 128
+ * with MOE_EPILOGUE_SILU_MUL). */
+#define MOE_WEIGHTS_PACKED 0x200
 
 /* Device-side error bits (moe_device_error). */
 #define MOE_DEVERR_BAD_INDEX 0x1   /* a token or expert index outside its range was skipped */
@@ -341,11 +348,30 @@ int moe_grouped_gemm_fp8_rowwise(const void* x, const void* w, const int32_t* co
  * device cannot host them.  D, H multiples of 16.
  * scatter_indices, T_out, accumulate: the fused top_k = 1 combine of the w2
  * GEMM, as in moe_grouped_gemm (y is then out [T_out, D]).
+ * flags: 0, or MOE_WEIGHTS_PACKED when w13 and w2 are tile-packed (then H and D
+ * must be multiples of 128); other bits: MOE_ERR_INVALID.
  */
 int moe_expert_mlp_workspace_size(int E, size_t* bytes);
 int moe_expert_mlp(const void* x, const void* w13, const void* w2, const int32_t* counts, int E, int a_max,
                    int D, int H, void* z, void* y, const int32_t* scatter_indices, int T_out, int accumulate,
-                   void* ws, size_t ws_bytes, cudaStream_t stream);
+                   void* ws, size_t ws_bytes, int flags, cudaStream_t stream);
+
+/*
+ * Tile-packed weights (a layout of this library, not of the pages): the
+ * weights [E, N, K] of a grouped GEMM, viewed as R = E * N rows of K elements
+ * (dtype MOE_DTYPE_BF16 or MOE_DTYPE_E4M3), cut into boxes of 128 rows x 128
+ * bytes: box (b, c) holds rows 128 b .. 128 b + 127 and bytes 128 c .. 128 c +
+ * 127 of each row, zero where a row or a byte lies past R or K.  Boxes are
+ * stored whole, 16 KB each, in (row block b, column block c) order, with
+ * ceil(K * elem / 128) column blocks per row block.  Each is the unit the
+ * GEMMs' TMA loads fetch, so packed weights stream from HBM sequentially.
+ * moe_pack_weights_size: bytes of the packed copy (K % 16 == 0, else
+ * MOE_ERR_UNSUPPORTED).  moe_pack_weights: write it from row-major w (device,
+ * 16-byte aligned; packed must not overlap w).  Asynchronous on stream.  The
+ * scales of FP8 weights are not affected.
+ */
+int moe_pack_weights_size(int E, int N, int K, int dtype, size_t* bytes);
+int moe_pack_weights(const void* w, int E, int N, int K, int dtype, void* packed, cudaStream_t stream);
 
 /* ------------------------------------------------------ dense GEMM (shared expert) */
 

@@ -23,6 +23,7 @@ MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_WORKSPACE = 
 MOE_DTYPE_BF16, MOE_DTYPE_F32, MOE_DTYPE_E4M3 = 0, 1, 2
 MOE_EPILOGUE_NONE, MOE_EPILOGUE_SILU_MUL = 0, 1
 MOE_GEMM_CTA_PAIRS = 0x100
+MOE_WEIGHTS_PACKED = 0x200
 MOE_DEVERR_BAD_INDEX, MOE_DEVERR_BAD_COUNT, MOE_DEVERR_TIMEOUT = 1, 2, 4
 
 
@@ -59,7 +60,9 @@ def _load() -> ctypes.CDLL:
         "moe_expert_mlp_workspace_size": ([I, ctypes.POINTER(S)], I),
         "moe_scatter_add_padded": ([P, P, P, I, P, P, I, I, I, I, I, P], I),
         "moe_topk_finalize": ([P, L, I, P, I, P, I, I, P, P, P, P], I),
-        "moe_expert_mlp": ([P, P, P, P, I, I, I, I, P, P, P, I, I, P, S, P], I),
+        "moe_expert_mlp": ([P, P, P, P, I, I, I, I, P, P, P, I, I, P, S, I, P], I),
+        "moe_pack_weights_size": ([I, I, I, I, ctypes.POINTER(S)], I),
+        "moe_pack_weights": ([P, I, I, I, I, P, P], I),
         "moe_grouped_gemm_fp8_rowwise": ([P, P, P, P, P, I, I, I, I, P, I, P, I, I, P], I),
         "moe_silu_mul": ([P, P, L, I, I, P, P, P], I),
         "moe_silu_mul_quant": ([P, P, L, I, I, P, P, P, P, P], I),
@@ -264,6 +267,49 @@ def _scatter_args(scatter_indices, out, accumulate):
     return scatter_indices, out.shape[0], int(accumulate)
 
 
+class PackedWeights:
+    """Weights [E, N, K] (bf16 or e4m3) in the tile-packed layout of moe_pack_weights:
+    `data` holds the packed bytes on the device; `shape` and `dtype` are the logical
+    ones.  Accepted wherever the grouped GEMMs and moe_expert_mlp take weights."""
+
+    def __init__(self, data: torch.Tensor, shape, dtype):
+        self.data, self.shape, self.dtype = data, tuple(shape), dtype
+
+    @property
+    def device(self):
+        return self.data.device
+
+
+def moe_pack_weights_size(E: int, N: int, K: int, dtype: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check("moe_pack_weights_size", _lib.moe_pack_weights_size(E, N, K, dtype, ctypes.byref(n)))
+    return n.value
+
+
+def moe_pack_weights(w: torch.Tensor, stream=None) -> PackedWeights:
+    """Tile-packed copy of w [E, N, K] bf16 or e4m3 (every 128-row x 128-byte box contiguous)."""
+    E, N, K = w.shape
+    if w.dtype not in (torch.bfloat16, torch.float8_e4m3fn):
+        raise TypeError(f"w must be bf16 or e4m3, got {w.dtype}")
+    _need(w, w.dtype, "w")
+    dt = MOE_DTYPE_E4M3 if w.dtype == torch.float8_e4m3fn else MOE_DTYPE_BF16
+    data = torch.empty(moe_pack_weights_size(E, N, K, dt), dtype=torch.uint8, device=w.device)
+    _check("moe_pack_weights", _lib.moe_pack_weights(_ptr(w), E, N, K, dt, _ptr(data), _stream(stream)))
+    return PackedWeights(data, (E, N, K), w.dtype)
+
+
+def _weights_arg(w, dtype, name: str, flags: int):
+    """Pointer and flags of a weights argument: a row-major [E, N, K] tensor or PackedWeights."""
+    if isinstance(w, PackedWeights):
+        if w.dtype != dtype:
+            raise TypeError(f"{name} must be {dtype}, got packed {w.dtype}")
+        if not w.data.is_cuda:
+            raise TypeError(f"{name} must be on a CUDA device")
+        return _ptr(w.data), flags | MOE_WEIGHTS_PACKED
+    _need(w, dtype, name)
+    return _ptr(w), flags
+
+
 def moe_grouped_gemm(x, w, counts, *, epilogue: int = MOE_EPILOGUE_NONE, out=None, scatter_indices=None,
                      accumulate: bool = True, stream=None):
     """x[a_max, K] bf16, w[E, N, K] bf16, counts[>= E] int32 -> y[a_max, N or N/2].
@@ -272,13 +318,13 @@ def moe_grouped_gemm(x, w, counts, *, epilogue: int = MOE_EPILOGUE_NONE, out=Non
     E, N, K2 = w.shape
     assert K == K2
     _need(x, torch.bfloat16, "x")
-    _need(w, torch.bfloat16, "w")
+    w_ptr, epilogue = _weights_arg(w, torch.bfloat16, "w", epilogue)
     n_out = N // 2 if (epilogue & 0xFF) == MOE_EPILOGUE_SILU_MUL else N
     si, t_out, acc = _scatter_args(scatter_indices, out, accumulate)
     if out is None:
         out = torch.empty(a_max, n_out, dtype=torch.bfloat16, device=x.device)
     _need(out, out.dtype, "out")
-    st = _lib.moe_grouped_gemm(_ptr(x), _ptr(w), _ptr(counts), E, a_max, N, K, _ptr(out), epilogue, _ptr(si),
+    st = _lib.moe_grouped_gemm(_ptr(x), w_ptr, _ptr(counts), E, a_max, N, K, _ptr(out), epilogue, _ptr(si),
                                t_out, acc, _stream(stream))
     _check("moe_grouped_gemm", st)
     return out
@@ -290,13 +336,13 @@ def moe_grouped_gemm_fp8_rowwise(x, w, counts, x_scale, w_scale, *, epilogue: in
     E, N, K2 = w.shape
     assert K == K2
     _need(x, torch.float8_e4m3fn, "x")
-    _need(w, torch.float8_e4m3fn, "w")
+    w_ptr, epilogue = _weights_arg(w, torch.float8_e4m3fn, "w", epilogue)
     n_out = N // 2 if (epilogue & 0xFF) == MOE_EPILOGUE_SILU_MUL else N
     si, t_out, acc = _scatter_args(scatter_indices, out, accumulate)
     if out is None:
         out = torch.empty(a_max, n_out, dtype=torch.bfloat16, device=x.device)
     _need(out, out.dtype, "out")
-    st = _lib.moe_grouped_gemm_fp8_rowwise(_ptr(x), _ptr(w), _ptr(counts), _ptr(x_scale), _ptr(w_scale), E, a_max,
+    st = _lib.moe_grouped_gemm_fp8_rowwise(_ptr(x), w_ptr, _ptr(counts), _ptr(x_scale), _ptr(w_scale), E, a_max,
                                            N, K, _ptr(out), epilogue, _ptr(si), t_out, acc, _stream(stream))
     _check("moe_grouped_gemm_fp8_rowwise", st)
     return out
@@ -316,8 +362,11 @@ def moe_expert_mlp(x, w13, w2, counts, *, z=None, out=None, scatter_indices=None
     E, n2, D2 = w13.shape
     H = n2 // 2
     assert D == D2 and tuple(w2.shape) == (E, D, H)
-    for t, n in ((x, "x"), (w13, "w13"), (w2, "w2")):
-        _need(t, torch.bfloat16, n)
+    _need(x, torch.bfloat16, "x")
+    if isinstance(w13, PackedWeights) != isinstance(w2, PackedWeights):
+        raise TypeError("w13 and w2 must both be packed or both be row-major")
+    w13_ptr, flags = _weights_arg(w13, torch.bfloat16, "w13", 0)
+    w2_ptr, _ = _weights_arg(w2, torch.bfloat16, "w2", 0)
     if z is None:
         z = torch.empty(a_max, H, dtype=torch.bfloat16, device=x.device)
     _need(z, z.dtype, "z")
@@ -327,8 +376,8 @@ def moe_expert_mlp(x, w13, w2, counts, *, z=None, out=None, scatter_indices=None
     _need(out, out.dtype, "out")
     if workspace is None:   # zero on first use; each call leaves it zero
         workspace = torch.zeros(moe_expert_mlp_workspace_size(E), dtype=torch.uint8, device=x.device)
-    st = _lib.moe_expert_mlp(_ptr(x), _ptr(w13), _ptr(w2), _ptr(counts), E, a_max, D, H, _ptr(z), _ptr(out),
-                             _ptr(si), t_out, acc, _ptr(workspace), workspace.numel(), _stream(stream))
+    st = _lib.moe_expert_mlp(_ptr(x), w13_ptr, w2_ptr, _ptr(counts), E, a_max, D, H, _ptr(z), _ptr(out),
+                             _ptr(si), t_out, acc, _ptr(workspace), workspace.numel(), flags, _stream(stream))
     _check("moe_expert_mlp", st)
     return out
 

@@ -331,7 +331,8 @@ static int grouped_gemm_common(const void* x, const void* w, const int32_t* coun
                                cudaStream_t stream) {
   if (E < 1 || a_max < 0 || N < 0 || K < 0) return MOE_ERR_INVALID;
   const bool pairs = (epilogue & MOE_GEMM_CTA_PAIRS) != 0;
-  epilogue &= ~MOE_GEMM_CTA_PAIRS;
+  const bool packed = (epilogue & MOE_WEIGHTS_PACKED) != 0;
+  epilogue &= ~(MOE_GEMM_CTA_PAIRS | MOE_WEIGHTS_PACKED);
   if (epilogue != MOE_EPILOGUE_NONE && epilogue != MOE_EPILOGUE_SILU_MUL) return MOE_ERR_INVALID;
   if (a_max == 0 || N == 0) return MOE_OK;
   if (!x || !w || !counts || !y) return MOE_ERR_INVALID;
@@ -341,7 +342,10 @@ static int grouped_gemm_common(const void* x, const void* w, const int32_t* coun
   if (epilogue == MOE_EPILOGUE_SILU_MUL && (N % 32 != 0)) return MOE_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return MOE_ERR_UNSUPPORTED;
   if (scatter && (epilogue != MOE_EPILOGUE_NONE || T_out < 0)) return MOE_ERR_INVALID;
-  moe::GemmArgs g{x, w, counts, x_scale, w_scale, E, a_max, N, K, y, epilogue, fp8, pairs, scatter, T_out,
+  // packed weights: every weight box starts at a 128-row block (SiLU*mul: both halves)
+  if (packed && (N % 128 != 0 || (epilogue == MOE_EPILOGUE_SILU_MUL && (N / 2) % 128 != 0)))
+    return MOE_ERR_UNSUPPORTED;
+  moe::GemmArgs g{x, w, counts, x_scale, w_scale, E, a_max, N, K, y, epilogue, fp8, pairs, packed, scatter, T_out,
                   accumulate, nullptr};
   int rc = device_error_word(&g.err);
   if (rc != MOE_OK) return rc;
@@ -359,7 +363,7 @@ int moe_expert_mlp_workspace_size(int E, size_t* bytes) {
 
 int moe_expert_mlp(const void* x, const void* w13, const void* w2, const int32_t* counts, int E, int a_max, int D,
                    int H, void* z, void* y, const int32_t* scatter_indices, int T_out, int accumulate, void* ws,
-                   size_t ws_bytes, cudaStream_t stream) {
+                   size_t ws_bytes, int flags, cudaStream_t stream) {
   size_t need;
   int rc = moe_expert_mlp_workspace_size(E, &need);
   if (rc != MOE_OK) return rc;
@@ -371,12 +375,32 @@ int moe_expert_mlp(const void* x, const void* w13, const void* w2, const int32_t
   if (!aligned16(x) || !aligned16(w13) || !aligned16(w2) || !aligned16(z) || !aligned16(y) || !aligned16(ws))
     return MOE_ERR_UNSUPPORTED;
   if (scatter_indices && T_out < 0) return MOE_ERR_INVALID;
-  moe::MlpArgs g{x, w13, w2, counts, E, a_max, D, H, z, y, ws, scatter_indices, T_out, accumulate, nullptr};
+  if (flags & ~MOE_WEIGHTS_PACKED) return MOE_ERR_INVALID;
+  const bool packed = (flags & MOE_WEIGHTS_PACKED) != 0;
+  if (packed && (H % 128 != 0 || D % 128 != 0)) return MOE_ERR_UNSUPPORTED;
+  moe::MlpArgs g{x, w13, w2, counts, E, a_max, D, H, z, y, ws, scatter_indices, T_out, accumulate, nullptr, packed};
   rc = device_error_word(&g.err);
   if (rc != MOE_OK) return rc;
   cudaError_t e = moe::launch_expert_mlp(g, stream);
   if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
   return finish(e);
+}
+
+int moe_pack_weights_size(int E, int N, int K, int dtype, size_t* bytes) {
+  if (!bytes || E < 1 || N < 1 || K < 1) return MOE_ERR_INVALID;
+  if (dtype != MOE_DTYPE_BF16 && dtype != MOE_DTYPE_E4M3) return MOE_ERR_INVALID;
+  if (K % 16 != 0) return MOE_ERR_UNSUPPORTED;
+  *bytes = moe::packed_weights_bytes((int64_t)E * N, K, dtype == MOE_DTYPE_E4M3);
+  return MOE_OK;
+}
+
+int moe_pack_weights(const void* w, int E, int N, int K, int dtype, void* packed, cudaStream_t stream) {
+  size_t need;
+  int rc = moe_pack_weights_size(E, N, K, dtype, &need);
+  if (rc != MOE_OK) return rc;
+  if (!w || !packed) return MOE_ERR_INVALID;
+  if (!aligned16(w) || !aligned16(packed)) return MOE_ERR_UNSUPPORTED;
+  return finish(moe::launch_pack_weights(w, (int64_t)E * N, K, dtype == MOE_DTYPE_E4M3, packed, stream));
 }
 
 int moe_grouped_gemm(const void* x, const void* w, const int32_t* counts, int E, int a_max, int N, int K, void* y,

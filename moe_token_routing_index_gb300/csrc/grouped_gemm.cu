@@ -120,7 +120,22 @@ struct Phase {
   int T_out;               // rows of y when scattering
   int accumulate;          // scatter: add into y (fp32 add of the bf16 row, one rounding) or overwrite
   int tma_store;           // y has a store tensor map (rows of a_max, 32 x 64 boxes): full row chunks use TMA
+  int packed;              // weights in the tile-packed layout (every 128-row x 128-byte box contiguous)
 };
+
+// TMA coordinates of the weight box (first row `row`, a multiple of 128 when
+// packed; K block kb, first element kc).  Row-major weights: (kc, row).  Packed
+// weights are a [boxes * 128, 128-byte] matrix whose box (row / 128, kb) starts
+// at row ((row / 128) * num_kb + kb) * 128.
+__device__ __forceinline__ void weight_box(const Phase& p, int row, int kb, int kc, int* c0, int* c1) {
+  if (p.packed) {
+    *c0 = 0;
+    *c1 = ((row >> 7) * p.num_kb + kb) * kBM;
+  } else {
+    *c0 = kc;
+    *c1 = row;
+  }
+}
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
   int v;
@@ -437,8 +452,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
           mbar_arrive_expect_tx(bar_full(s), kStageBytes);
           const int kc = kb * elems_per_kb;
           tma_load_2d(a_dst, ma, bar_full(s), kc, t.row0);
-          tma_load_2d(b_dst, mb, bar_full(s), kc, b_row0);
-          tma_load_2d(b_dst + kBBytes / 2, mb, bar_full(s), kc, b_row1);
+          int w0, w1;
+          weight_box(p, b_row0, kb, kc, &w0, &w1);
+          tma_load_2d(b_dst, mb, bar_full(s), w0, w1);
+          weight_box(p, b_row1, kb, kc, &w0, &w1);
+          tma_load_2d(b_dst + kBBytes / 2, mb, bar_full(s), w0, w1);
           issued_mask |= 1u << s;
           issued_parity = (issued_parity & ~(1u << s)) | (phase << s);
           if (++s == kStages) {
@@ -798,7 +816,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
           const uint32_t full_leader = full_leader0 + (uint32_t)(s * 8);
           const int kc = kb * elems_per_kb;
           tma_load_2d_pair(sbase + PairSmem::a + s * kPairABytes, &map_a, full_leader, kc, a_row);
-          tma_load_2d_pair(sbase + PairSmem::b + s * kPairBBytes, &map_b, full_leader, kc, b_row);
+          int w0, w1;
+          weight_box(p, b_row, kb, kc, &w0, &w1);
+          tma_load_2d_pair(sbase + PairSmem::b + s * kPairBBytes, &map_b, full_leader, w0, w1);
           issued_mask |= 1u << s;
           issued_parity = (issued_parity & ~(1u << s)) | (phase << s);
           if (++s == kPairStages) {
@@ -914,6 +934,31 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, bo
   return make_map_sw128(map, base, rows, cols, fp8, kBM);
 }
 
+// Weights [rows, K], row-major or tile-packed (see pack_weights_kernel).
+bool make_weight_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, bool fp8, bool packed) {
+  if (!packed) return make_map(map, base, rows, K, fp8);
+  const int64_t kb = (K * (fp8 ? 1 : 2) + kBKBytes - 1) / kBKBytes;
+  return make_map(map, base, (rows + kBM - 1) / kBM * kb * kBM, kBKBytes / (fp8 ? 1 : 2), fp8);
+}
+
+// Tile-packed weights: for rows r of a [rows, K] matrix and 128-byte column
+// blocks c (kb of them, the last zero-padded), box (r / 128, c) holds rows
+// r / 128 * 128 .. + 127 (zero rows past the end) as 128 contiguous 128-byte rows,
+// boxes in (row block, column block) order.  One thread per 16-byte piece.
+__global__ void pack_weights_kernel(const uint8_t* __restrict__ w, int64_t rows, int64_t row_bytes, int64_t kb,
+                                    uint4* __restrict__ out, int64_t pieces) {
+  for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < pieces; u += (int64_t)gridDim.x * blockDim.x) {
+    const int piece = (int)(u & 7);
+    const int64_t box_row = (u >> 3) & (kBM - 1);
+    const int64_t box = u >> 10;  // 8 pieces x 128 rows per box
+    const int64_t c = box % kb, rb = box / kb;
+    const int64_t r = rb * kBM + box_row, off = c * kBKBytes + piece * 16;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (r < rows && off < row_bytes) v = *reinterpret_cast<const uint4*>(w + r * row_bytes + off);
+    out[u] = v;
+  }
+}
+
 Phase make_phase(int N, int K, int epi, bool fp8, void* y, const float* xs, const float* ws) {
   Phase p;
   p.N = N;
@@ -931,6 +976,7 @@ Phase make_phase(int N, int K, int epi, bool fp8, void* y, const float* xs, cons
   p.T_out = 0;
   p.accumulate = 0;
   p.tma_store = 0;
+  p.packed = 0;
   return p;
 }
 
@@ -1000,12 +1046,30 @@ cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtens
 
 }  // namespace
 
+size_t packed_weights_bytes(int64_t rows, int64_t K, bool fp8) {
+  const int64_t kb = (K * (fp8 ? 1 : 2) + kBKBytes - 1) / kBKBytes;
+  return (size_t)((rows + kBM - 1) / kBM * kb) * kBM * kBKBytes;
+}
+
+cudaError_t launch_pack_weights(const void* w, int64_t rows, int64_t K, bool fp8, void* out, cudaStream_t s) {
+  const int64_t row_bytes = K * (fp8 ? 1 : 2);
+  const int64_t kb = (row_bytes + kBKBytes - 1) / kBKBytes;
+  const int64_t pieces = (int64_t)packed_weights_bytes(rows, K, fp8) / 16;
+  if (pieces == 0) return cudaSuccess;
+  const int64_t want = (pieces + 255) / 256, cap = (int64_t)device_sm_count() * 16;
+  pack_weights_kernel<<<(int)(want < cap ? want : cap), 256, 0, s>>>(static_cast<const uint8_t*>(w), rows, row_bytes,
+                                                                    kb, static_cast<uint4*>(out), pieces);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_grouped_gemm(const GemmArgs& g, cudaStream_t s) {
   if (g.E > kMaxExperts) return cudaErrorNotSupported;
   CUtensorMap ma, mb;
-  if (!make_map(&ma, g.x, g.a_max, g.K, g.fp8) || !make_map(&mb, g.w, (int64_t)g.E * g.N, g.K, g.fp8))
+  if (!make_map(&ma, g.x, g.a_max, g.K, g.fp8) ||
+      !make_weight_map(&mb, g.w, (int64_t)g.E * g.N, g.K, g.fp8, g.packed))
     return cudaErrorInvalidValue;
   Phase p = make_phase(g.N, g.K, g.epilogue, g.fp8, g.y, g.x_scale, g.w_scale);
+  p.packed = g.packed ? 1 : 0;
   p.scatter = g.scatter;
   p.T_out = g.T_out;
   p.accumulate = g.accumulate;
@@ -1026,11 +1090,14 @@ size_t expert_mlp_workspace_bytes(int E) { return ((size_t)(E + 1) * sizeof(int)
 cudaError_t launch_expert_mlp(const MlpArgs& g, cudaStream_t s) {
   if (g.E > kMaxExperts) return cudaErrorNotSupported;
   CUtensorMap a0, b0, a1, b1;
-  if (!make_map(&a0, g.x, g.a_max, g.D, false) || !make_map(&b0, g.w13, (int64_t)g.E * 2 * g.H, g.D, false) ||
-      !make_map(&a1, g.z, g.a_max, g.H, false) || !make_map(&b1, g.w2, (int64_t)g.E * g.D, g.H, false))
+  if (!make_map(&a0, g.x, g.a_max, g.D, false) ||
+      !make_weight_map(&b0, g.w13, (int64_t)g.E * 2 * g.H, g.D, false, g.packed) ||
+      !make_map(&a1, g.z, g.a_max, g.H, false) ||
+      !make_weight_map(&b1, g.w2, (int64_t)g.E * g.D, g.H, false, g.packed))
     return cudaErrorInvalidValue;
-  const Phase p0 = make_phase(2 * g.H, g.D, MOE_EPILOGUE_SILU_MUL, false, g.z, nullptr, nullptr);
+  Phase p0 = make_phase(2 * g.H, g.D, MOE_EPILOGUE_SILU_MUL, false, g.z, nullptr, nullptr);
   Phase p1 = make_phase(g.D, g.H, MOE_EPILOGUE_NONE, false, g.y, nullptr, nullptr);
+  p0.packed = p1.packed = g.packed ? 1 : 0;
   p1.scatter = g.scatter;
   p1.T_out = g.T_out;
   p1.accumulate = g.accumulate;

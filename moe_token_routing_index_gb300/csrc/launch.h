@@ -137,6 +137,7 @@ struct GemmArgs {
   int epilogue;
   bool fp8;
   bool pairs;              // 256-row tiles on CTA pairs (cta_group::2)
+  bool packed;             // w in the tile-packed layout (launch_pack_weights)
   const int32_t* scatter;  // nullable: combine row r into y[scatter[r]] (top_k = 1)
   int T_out;               // rows of y when scattering
   int accumulate;
@@ -159,9 +160,13 @@ struct MlpArgs {
   int T_out;
   int accumulate;
   unsigned int* err;
+  bool packed;          // w13 and w2 in the tile-packed layout
 };
 
 size_t expert_mlp_workspace_bytes(int E);
+// Tile-packed weights (every 128-row x 128-byte TMA box contiguous): size and packing.
+size_t packed_weights_bytes(int64_t rows, int64_t K, bool fp8);
+cudaError_t launch_pack_weights(const void* w, int64_t rows, int64_t K, bool fp8, void* out, cudaStream_t s);
 cudaError_t launch_expert_mlp(const MlpArgs& a, cudaStream_t s);
 
 // Number of SMs of the current device (cached per device).

@@ -65,6 +65,9 @@ class MoELayer:
     router: bf16 [E, D], router_DE transposed (None: the caller passes scores).
     shared_w13 [2Hs, D], shared_w2 [D, Hs]: the shared expert, in the layer's
     dtype (e4m3 with scales shared_w13_scale [2Hs], shared_w2_scale [D]).
+    pack_weights: hold w13 and w2 in the tile-packed layout (moe_pack_weights), so
+    that the grouped GEMMs stream them as contiguous boxes; None packs them when H
+    and D are multiples of 128.  The output is the same bit for bit either way.
     """
 
     def __init__(self, top_k: int, w13: torch.Tensor, w2: torch.Tensor, w13_scale: torch.Tensor | None = None,
@@ -73,7 +76,7 @@ class MoELayer:
                  router: torch.Tensor | None = None, shared_w13: torch.Tensor | None = None,
                  shared_w2: torch.Tensor | None = None, shared_w13_scale: torch.Tensor | None = None,
                  shared_w2_scale: torch.Tensor | None = None, overlap_shared: bool = True,
-                 weighting: str = "input"):
+                 weighting: str = "input", pack_weights: bool | None = None):
         self.E, n2, self.D = w13.shape
         self.H = n2 // 2
         assert w2.shape == (self.E, self.D, self.H), "w2 must be [E, D, H]"
@@ -82,6 +85,10 @@ class MoELayer:
         if self.fp8:
             assert w13_scale is not None and w2_scale is not None
         self.w13, self.w2 = w13.contiguous(), w2.contiguous()
+        if pack_weights is None:
+            pack_weights = self.H % 128 == 0 and self.D % 128 == 0 and w13.is_cuda
+        if pack_weights:   # resident weights: packed once, the row-major copies are not kept
+            self.w13, self.w2 = mb.moe_pack_weights(self.w13), mb.moe_pack_weights(self.w2)
         self.w13_scale = None if w13_scale is None else w13_scale.contiguous()
         self.w2_scale = None if w2_scale is None else w2_scale.contiguous()
         dev = w13.device

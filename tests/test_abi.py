@@ -77,8 +77,27 @@ def test_host_side_validation_without_gpu(lib):
     assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 32, 64, fake, 1, fake, 8, 1, None) == lib.MOE_ERR_INVALID
     n = ctypes.c_size_t(0)
     assert L.moe_expert_mlp_workspace_size(0, ctypes.byref(n)) == lib.MOE_ERR_INVALID
-    assert L.moe_expert_mlp(fake, fake, fake, fake, 4, 64, 32, 32, fake, fake, None, 0, 0, fake, 0, None) \
+    assert L.moe_expert_mlp(fake, fake, fake, fake, 4, 64, 32, 32, fake, fake, None, 0, 0, fake, 0, 0, None) \
         == lib.MOE_ERR_WORKSPACE
+    # expert MLP: unknown flag bits; packed weights need H and D multiples of 128
+    assert L.moe_expert_mlp(fake, fake, fake, fake, 4, 64, 128, 128, fake, fake, None, 0, 0, fake, 1 << 20, 0x400,
+                            None) == lib.MOE_ERR_INVALID
+    assert L.moe_expert_mlp(fake, fake, fake, fake, 4, 64, 128, 96, fake, fake, None, 0, 0, fake, 1 << 20,
+                            lib.MOE_WEIGHTS_PACKED, None) == lib.MOE_ERR_UNSUPPORTED
+    # packed weights: N (and its halves with SiLU*mul) a multiple of 128
+    assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 96, 64, fake, lib.MOE_WEIGHTS_PACKED, None, 0, 0, None) \
+        == lib.MOE_ERR_UNSUPPORTED
+    assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 128, 64, fake, lib.MOE_WEIGHTS_PACKED | 1, None, 0, 0,
+                              None) == lib.MOE_ERR_UNSUPPORTED                    # SiLU halves of 64 rows
+    # pack size: bf16 [2, 256, 208] -> 4 row blocks x ceil(416 / 128) = 4 column blocks of 16 KB
+    assert L.moe_pack_weights_size(2, 256, 208, lib.MOE_DTYPE_BF16, ctypes.byref(n)) == lib.MOE_OK
+    assert n.value == 4 * 4 * 16384
+    # e4m3 [3, 100, 256]: 300 rows -> 3 row blocks (zero rows past the end) x 2 column blocks
+    assert L.moe_pack_weights_size(3, 100, 256, lib.MOE_DTYPE_E4M3, ctypes.byref(n)) == lib.MOE_OK
+    assert n.value == 3 * 2 * 16384
+    assert L.moe_pack_weights_size(2, 256, 208, lib.MOE_DTYPE_F32, ctypes.byref(n)) == lib.MOE_ERR_INVALID
+    assert L.moe_pack_weights_size(2, 256, 24, lib.MOE_DTYPE_BF16, ctypes.byref(n)) == lib.MOE_ERR_UNSUPPORTED
+    assert L.moe_pack_weights(None, 2, 256, 64, lib.MOE_DTYPE_BF16, fake, None) == lib.MOE_ERR_INVALID
     # router scores: shape limits, workspace, empty batch
     assert L.moe_router_workspace_size(-1, 64, 8, ctypes.byref(n)) == lib.MOE_ERR_INVALID
     assert L.moe_router_workspace_size(64, 64, 300, ctypes.byref(n)) == lib.MOE_ERR_UNSUPPORTED

@@ -368,3 +368,92 @@ def test_dense_splitk_gemm(M, K, N, valid):
         assert mb.device_error() == 0
         assert torch.equal(z[:valid], z_ref)
         assert is_sentinel(z[valid:])
+
+
+def _ref_pack(w: torch.Tensor) -> torch.Tensor:
+    """The tile-packed layout written out with reshapes: rows cut into 128-row blocks and
+    bytes into 128-byte blocks (zero-padded), boxes in (row block, byte block) order."""
+    E, N, K = w.shape
+    rb = w.contiguous().view(torch.uint8).reshape(E * N, -1)
+    R, B = rb.shape
+    nr, nc = (R + 127) // 128, (B + 127) // 128
+    pad = torch.zeros(nr * 128, nc * 128, dtype=torch.uint8, device=w.device)
+    pad[:R, :B] = rb
+    return pad.view(nr, 128, nc, 128).permute(0, 2, 1, 3).contiguous().view(-1)
+
+
+@pytest.mark.parametrize("E,N,K,fp8", [(3, 256, 208, False), (2, 384, 256, True), (3, 100, 64, False),
+                                       (1, 128, 4096, True), (5, 256, 5120, False)])
+def test_pack_weights_layout(E, N, K, fp8):
+    mb = _mb()
+    g = torch.Generator().manual_seed(E * N + K)
+    w = torch.randn(E, N, K, generator=g)
+    w = (w * 0.5).to(torch.float8_e4m3fn) if fp8 else w.to(torch.bfloat16)
+    p = mb.moe_pack_weights(w.cuda())
+    torch.cuda.synchronize()
+    assert p.shape == (E, N, K) and p.dtype == w.dtype
+    assert torch.equal(p.data, _ref_pack(w.cuda()))
+
+
+@pytest.mark.parametrize("E,counts,N,K,fp8,silu,pairs", [
+    (4, [130, 0, 257, 64], 512, 256, False, True, False),
+    (4, [130, 0, 257, 64], 512, 256, False, False, True),
+    (3, [300, 17, 256], 256, 208, False, False, False),      # a partial last K block (416 bytes)
+    (3, [300, 17, 256], 768, 512, True, True, False),
+    (2, [600, 90], 384, 256, True, False, True),
+    (16, [512] * 16, 1024, 5120, True, False, False),
+])
+def test_packed_weights_gemm_equals_row_major(E, counts, N, K, fp8, silu, pairs):
+    """Packed weights give the grouped GEMMs bit-identical results (the same boxes land in
+    shared memory), over bf16 and FP8, plain and SiLU*mul epilogues, single-CTA and
+    CTA-pair tiles, ragged counts and a partial K block."""
+    mb = _mb()
+    g = torch.Generator().manual_seed(N + K + E)
+    a = int(sum(counts))
+    cd = torch.tensor(counts, dtype=torch.int32, device="cuda")
+    epi = (mb.MOE_EPILOGUE_SILU_MUL if silu else mb.MOE_EPILOGUE_NONE) | (mb.MOE_GEMM_CTA_PAIRS if pairs else 0)
+    if fp8:
+        x = (torch.randn(a, K, generator=g) * 0.5).to(torch.float8_e4m3fn).cuda()
+        w = (torch.randn(E, N, K, generator=g) * 0.5).to(torch.float8_e4m3fn).cuda()
+        xs = (torch.rand(a, generator=g) + 0.5).cuda()
+        ws = (torch.rand(E * N, generator=g) + 0.5).cuda()
+        y0 = mb.moe_grouped_gemm_fp8_rowwise(x, w, cd, xs, ws, epilogue=epi)
+        y1 = mb.moe_grouped_gemm_fp8_rowwise(x, mb.moe_pack_weights(w), cd, xs, ws, epilogue=epi)
+    else:
+        x = torch.randn(a, K, generator=g).to(torch.bfloat16).cuda()
+        w = (torch.randn(E, N, K, generator=g) * 0.1).to(torch.bfloat16).cuda()
+        y0 = mb.moe_grouped_gemm(x, w, cd, epilogue=epi)
+        y1 = mb.moe_grouped_gemm(x, mb.moe_pack_weights(w), cd, epilogue=epi)
+    torch.cuda.synchronize()
+    assert mb.device_error() == 0
+    assert torch.equal(y0, y1)
+
+
+@pytest.mark.parametrize("accumulate", [False, True])
+def test_packed_weights_fused_combine_and_expert_mlp(accumulate):
+    """The fused top_k = 1 combine and the one-launch expert MLP with packed weights equal
+    their row-major runs bit for bit."""
+    mb = _mb()
+    g = torch.Generator().manual_seed(21)
+    E, D, H, T = 16, 512, 1024, 128
+    x = torch.randn(T, D, generator=g).to(torch.bfloat16).cuda()
+    w13 = (torch.randn(E, 2 * H, D, generator=g) * 0.1).to(torch.bfloat16).cuda()
+    w2 = (torch.randn(E, D, H, generator=g) * 0.1).to(torch.bfloat16).cuda()
+    cd = torch.tensor([8] * 12 + [0, 20, 12, 0], dtype=torch.int32, device="cuda")
+    perm = torch.randperm(T, generator=g).to(torch.int32).cuda()
+    init = torch.randn(T, D, generator=g).to(torch.bfloat16).cuda()
+    outs = []
+    for pack in (False, True):
+        a13 = mb.moe_pack_weights(w13) if pack else w13
+        a2 = mb.moe_pack_weights(w2) if pack else w2
+        o = init.clone()
+        mb.moe_expert_mlp(x, a13, a2, cd, out=o, scatter_indices=perm, accumulate=accumulate)
+        z = mb.moe_grouped_gemm(x, a13, cd, epilogue=mb.MOE_EPILOGUE_SILU_MUL)
+        o2 = init.clone()
+        mb.moe_grouped_gemm(z, a2, cd, out=o2, scatter_indices=perm, accumulate=accumulate)
+        outs.append((o, o2, z))
+    torch.cuda.synchronize()
+    assert mb.device_error() == 0
+    for u, v in zip(outs[0], outs[1]):
+        assert torch.equal(u, v)
+    assert torch.equal(outs[1][0], outs[1][1])
