@@ -173,3 +173,25 @@ def test_forward_accumulates_into_existing_output(name, with_shared):
     assert rms(f64(res["out"]) - f64(ref)) > 0              # the starting output did take part
     if Tv < cfg.T:
         assert torch.equal(out[Tv:].cpu(), init[Tv:]), "padding tokens keep their values"
+
+
+@pytest.mark.parametrize("name", ["decode", "fine_grained", "padded_fp8"])
+def test_layer_with_packed_weights_equals_row_major(name):
+    """MoELayer packs its resident weights by default (H and D multiples of 128); the
+    forward equals the row-major layer's bit for bit."""
+    from moe_token_routing_index_gb300 import binding as mb
+    from moe_token_routing_index_gb300.forward import MoELayer
+
+    cfg = workloads.CONFIGS[name]
+    x = workloads.make_tokens(cfg).cuda()
+    s = workloads.make_scores(cfg).cuda()
+    nv = None if cfg.Tv is None else torch.tensor([cfg.Tv], dtype=torch.int32, device="cuda")
+    w13, w2 = workloads.make_weights(cfg, device="cuda")
+    packed = MoELayer.from_weights(cfg, w13, w2)
+    plain = MoELayer.from_weights(cfg, w13, w2, pack_weights=False)
+    assert isinstance(packed.w13, mb.PackedWeights) and not isinstance(plain.w13, mb.PackedWeights)
+    o1 = packed(x, s, nv).clone()
+    o2 = plain(x, s, nv)
+    torch.cuda.synchronize()
+    assert mb.device_error() == 0
+    assert torch.equal(o1, o2)
