@@ -7,9 +7,10 @@ inputs resident in HBM.  Prints one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
 
-Default workload: the decode-shaped layer (T=128, D=5120, H=8192, E=16,
-top_k=1, bf16).  --config prefill_fp8 | fine_grained | padded_fp8 | tiny |
-decode_zero measures the other workloads.  Under torchrun (N > 1) every rank
+Default workload: the largest one, the fine-grained-experts layer (T=4096,
+D=7168, H=2048, E=128, top_k=8, bf16, Zipf-skewed routing: 2.89 TFLOP and
+11.3 GB of expert weights per step).  --config decode | prefill_fp8 |
+padded_fp8 | tiny | decode_zero measures the other workloads.  Under torchrun (N > 1) every rank
 runs an independent replica on its own GPU (no data-path collective); the
 timing is the max over ranks and the value counts the tokens of all ranks.
 
@@ -684,7 +685,7 @@ def main(argv=None):
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=500)
     p.add_argument("--warmup", type=int, default=20)
-    p.add_argument("--config", default="decode")
+    p.add_argument("--config", default="fine_grained")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU-baseline leg")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU work of the oracle baseline sample")

@@ -232,7 +232,28 @@ def silu_mul(y, H: int, valid_rows: int | None = None):
     return z
 
 
-def silu_mul_quant(y, H: int, scale_ub: float | None = None, valid_rows: int | None = None):
+def silu_mul_quant(y, H: int, scale_ub: float | None = None, valid_rows: int | None = None, *,
+                   z_bf16: bool = False):
+    """y[a, 2H] bf16 bits -> (z[a, H] e4m3 codes, z_scale[a] f32): z = silu(y0) * y1
+    quantised per row with the gathers' row rule (bound ``scale_ub``).
+
+    z_bf16=False: the row rule acts on the fp32 value of z (silu_mul_quant of
+    MetaShufflingMoE._fused_silu_mul, one rounding).  z_bf16=True: z is first
+    rounded to bf16, as silu_mul writes it, and the row rule acts on those bf16
+    values; this is the dense reference's order (BaselineMoE._forward forms
+    routed_z as a bf16 tensor and _fake_quant quantises its rows) and the
+    grouped GEMM's fused SiLU*mul + quantisation epilogue.  Rows >= valid_rows
+    are zero.
+    """
+    if z_bf16:
+        a = y.shape[0]
+        v = a if valid_rows is None else int(valid_rows)
+        zq = np.zeros((a, H), np.uint8)
+        zs = np.zeros(a, np.float32)
+        if v > 0:
+            zb = silu_mul(y, H, v)
+            zq[:v], zs[:v] = quantize_rows(bf16_to_f32(zb[:v]), scale_ub)
+        return zq, zs
     y = _c(y, np.uint16)
     a = y.shape[0]
     v = a if valid_rows is None else int(valid_rows)
@@ -277,7 +298,7 @@ def router_scores(x, w_router, valid_tokens: int | None = None, logits: bool = F
 # ------------------------------------------------------------------- forward
 
 def moe_forward(x, scores, top_k: int, weights, *, fp8: bool, valid_tokens: int | None = None,
-                out_init=None, scale_ub: float | None = None, H: int | None = None):
+                out_init=None, scale_ub: float | None = None, H: int | None = None, z_bf16: bool = False):
     """The routed-expert forward of MetaShufflingMoE._no_comm_forward (one GPU,
     no shared expert), on the CPU.
 
@@ -285,7 +306,9 @@ def moe_forward(x, scores, top_k: int, weights, *, fp8: bool, valid_tokens: int 
     the weights of the experts ``ids`` (ascending) as (w13[n, 2H, D],
     w2[n, D, H]): bf16 bits, or fp32 when ``fp8`` (quantised per row here).
     out_init[T, D] (bf16 bits) is the tensor the routed rows are added into
-    (zeros when None).  Returns the final output and every intermediate.
+    (zeros when None).  z_bf16: on the FP8 path, z is rounded to bf16 before its
+    row quantisation (see silu_mul_quant).  Returns the final output and every
+    intermediate.
     """
     T, D = x.shape
     E = scores.shape[1]
@@ -312,7 +335,7 @@ def moe_forward(x, scores, top_k: int, weights, *, fp8: bool, valid_tokens: int 
         w2q, w2s = quantize_rows(w2)
         xq, xs = gather_scale_quant(x, r["token_indices"], r["expert_indices"], scores, scale_ub)
         y = grouped_gemm_fp8(xq, w13q, cu, xs, w13s)
-        zq, zs = silu_mul_quant(y, Hd, scale_ub)
+        zq, zs = silu_mul_quant(y, Hd, scale_ub, z_bf16=z_bf16)
         o = grouped_gemm_fp8(zq, w2q, cu, zs, w2s)
         res.update(x_routed=xq, x_scale=xs, y=y, z=zq, z_scale=zs, o=o,
                    w13q=w13q, w13s=w13s, w2q=w2q, w2s=w2s)
@@ -322,7 +345,7 @@ def moe_forward(x, scores, top_k: int, weights, *, fp8: bool, valid_tokens: int 
 
 
 def moe_forward_tokens(tokens, x, scores, top_k: int, weights, *, fp8: bool, out_init=None,
-                       scale_ub: float | None = None):
+                       scale_ub: float | None = None, z_bf16: bool = False):
     """The forward's output rows for a sample of tokens only.
 
     Every stage of the forward works row by row (routing per token, gather and
@@ -335,7 +358,7 @@ def moe_forward_tokens(tokens, x, scores, top_k: int, weights, *, fp8: bool, out
     xs = np.ascontiguousarray(x[tokens])
     ss = np.ascontiguousarray(scores[tokens])
     oi = None if out_init is None else np.ascontiguousarray(out_init[tokens])
-    res = moe_forward(xs, ss, top_k, weights, fp8=fp8, out_init=oi, scale_ub=scale_ub)
+    res = moe_forward(xs, ss, top_k, weights, fp8=fp8, out_init=oi, scale_ub=scale_ub, z_bf16=z_bf16)
     return res["out"], res
 
 
@@ -368,7 +391,7 @@ def topk_finalize(rows, weights, idx, shared=None):
 
 
 def moe_forward_output_weighted(x, scores, top_k: int, weights, *, fp8: bool, valid_tokens: int | None = None,
-                                shared_out=None, scale_ub: float | None = None):
+                                shared_out=None, scale_ub: float | None = None, z_bf16: bool = False):
     """The routed experts with the routing weights applied to the expert outputs
     (top-k finalize) instead of their inputs: route -> gather (unit scores) ->
     grouped GEMM w13 -> silu_mul(_quant) -> grouped GEMM w2 -> topk_finalize with
@@ -400,7 +423,7 @@ def moe_forward_output_weighted(x, scores, top_k: int, weights, *, fp8: bool, va
         w13q, w13s = quantize_rows(w13)
         w2q, w2s = quantize_rows(w2)
         xq, xs = gather_scale_quant(x, r["token_indices"], r["expert_indices"], unit, scale_ub)
-        zq, zs = silu_mul_quant(grouped_gemm_fp8(xq, w13q, cu, xs, w13s), Hd, scale_ub)
+        zq, zs = silu_mul_quant(grouped_gemm_fp8(xq, w13q, cu, xs, w13s), Hd, scale_ub, z_bf16=z_bf16)
         o = grouped_gemm_fp8(zq, w2q, cu, zs, w2s)
     wts = topk_weights(scores, r)
     out[:v] = topk_finalize(o, wts, r["inv"], None if shared_out is None else shared_out[:v])
@@ -410,13 +433,15 @@ def moe_forward_output_weighted(x, scores, top_k: int, weights, *, fp8: bool, va
 
 # ------------------------------------------------------------ shared expert
 
-def shared_expert(x, w13, w2, *, fp8: bool, scale_ub: float | None = None, valid_tokens: int | None = None):
+def shared_expert(x, w13, w2, *, fp8: bool, scale_ub: float | None = None, valid_tokens: int | None = None,
+                  z_bf16: bool = False):
     """The shared expert of MetaShufflingMoE._shared_expert_part1 / _part2 on
     the valid token rows: y = x @ w13.T, z = silu_mul(y0, y1), out = z @ w2.T.
 
     w13[2H, D], w2[D, H]: bf16 bits, or fp32 when ``fp8``.  On the FP8-rowwise
     path the weights are quantised per row here, x per row with the gathers'
-    row rule at unit score (bound ``scale_ub``), and z by silu_mul_quant.
+    row rule at unit score (bound ``scale_ub``), and z by silu_mul_quant
+    (``z_bf16`` as there).
     Returns out[T, D] bf16 bits; rows >= valid_tokens stay zero.
     """
     T, D = x.shape
@@ -435,40 +460,43 @@ def shared_expert(x, w13, w2, *, fp8: bool, scale_ub: float | None = None, valid
         w2q, w2s = quantize_rows(w2)
         xq, xs = quantize_rows(bf16_to_f32(x[:v]), scale_ub)
         y = grouped_gemm_fp8(xq, w13q[None], counts, xs, w13s)
-        zq, zs = silu_mul_quant(y, H, scale_ub)
+        zq, zs = silu_mul_quant(y, H, scale_ub, z_bf16=z_bf16)
         out[:v] = grouped_gemm_fp8(zq, w2q[None], counts, zs, w2s)
     return out
 
 
 def moe_layer_forward(x, w_router, top_k: int, weights, *, fp8: bool, shared=None,
-                      valid_tokens: int | None = None, scale_ub: float | None = None, weighting: str = "input"):
+                      valid_tokens: int | None = None, scale_ub: float | None = None, weighting: str = "input",
+                      z_bf16: bool = False):
     """The whole MoE layer of MetaShufflingMoE._no_comm_forward on one GPU:
     router scores, the shared expert (``shared`` = (w13, w2), or None for a
     layer without one), and the routed experts added into its output
     (``weighting`` "input": scores scale the expert inputs; "output": the top-k
-    finalize weights the expert outputs and adds the shared output).
+    finalize weights the expert outputs and adds the shared output;
+    ``z_bf16`` as in silu_mul_quant, for the routed and the shared expert).
     Returns the routed forward's dict plus ``scores`` and ``shared_out``.
     """
     scores = router_scores(x, w_router, valid_tokens)
     base = None
     if shared is not None:
-        base = shared_expert(x, shared[0], shared[1], fp8=fp8, scale_ub=scale_ub, valid_tokens=valid_tokens)
+        base = shared_expert(x, shared[0], shared[1], fp8=fp8, scale_ub=scale_ub, valid_tokens=valid_tokens,
+                             z_bf16=z_bf16)
     if weighting == "output":
         res = moe_forward_output_weighted(x, scores, top_k, weights, fp8=fp8, valid_tokens=valid_tokens,
-                                          shared_out=base, scale_ub=scale_ub)
+                                          shared_out=base, scale_ub=scale_ub, z_bf16=z_bf16)
     else:
         res = moe_forward(x, scores, top_k, weights, fp8=fp8, valid_tokens=valid_tokens, out_init=base,
-                          scale_ub=scale_ub)
+                          scale_ub=scale_ub, z_bf16=z_bf16)
     res["scores"] = scores
     res["shared_out"] = base
     return res
 
 
 def moe_layer_forward_tokens(tokens, x, w_router, top_k: int, weights, *, fp8: bool, shared=None,
-                             scale_ub: float | None = None, weighting: str = "input"):
+                             scale_ub: float | None = None, weighting: str = "input", z_bf16: bool = False):
     """moe_layer_forward's output rows for a sample of valid tokens: every stage,
     the router and the shared expert included, works token by token."""
     tokens = np.asarray(tokens, np.int64)
     res = moe_layer_forward(np.ascontiguousarray(x[tokens]), w_router, top_k, weights, fp8=fp8, shared=shared,
-                            scale_ub=scale_ub, weighting=weighting)
+                            scale_ub=scale_ub, weighting=weighting, z_bf16=z_bf16)
     return res["out"], res

@@ -82,8 +82,10 @@ def _fake_quant_rows(v):
     return q / s
 
 
-def dense_forward_fake_quant(x, scores, w13, w2, top_k):
-    """BaselineMoE._forward with _fake_quant on both GEMMs, float64 elsewhere."""
+def dense_forward_fake_quant(x, scores, w13, w2, top_k, z_bf16=False):
+    """BaselineMoE._forward with _fake_quant on both GEMMs, float64 elsewhere
+    (z_bf16: z rounded to bf16 before its quantisation, as routed_z is a bf16
+    tensor there)."""
     T, D = x.shape
     E = scores.shape[1]
     H = w2.shape[2]
@@ -95,15 +97,19 @@ def dense_forward_fake_quant(x, scores, w13, w2, top_k):
         xt = _fake_quant_rows(x * masked[:, e:e + 1])
         y = xt @ _fake_quant_rows(w13[e]).T
         y0, y1 = y[:, :H], y[:, H:]
-        z = _fake_quant_rows(y0 * (1 / (1 + np.exp(-y0))) * y1)
+        z = y0 * (1 / (1 + np.exp(-y0))) * y1
+        if z_bf16:
+            z = torch.from_numpy(z).to(torch.bfloat16).double().numpy()
+        z = _fake_quant_rows(z)
         out += z @ _fake_quant_rows(w2[e]).T
     return out
 
 
-def test_fp8_forward_matches_dense_formulation():
+@pytest.mark.parametrize("z_bf16", [False, True])
+def test_fp8_forward_matches_dense_formulation(z_bf16):
     cfg, x, s, w13, w2 = _problem(6, T=40, D=64, H=48, E=4, k=2, std=0.15, fp8=True)
     weights = lambda ids: (w13[ids].numpy(), w2[ids].numpy())
-    res = oracle.moe_forward(bits(x), bits(s), 2, weights, fp8=True, scale_ub=1200.0)
+    res = oracle.moe_forward(bits(x), bits(s), 2, weights, fp8=True, scale_ub=1200.0, z_bf16=z_bf16)
     got = f64(res["out"])
     args = (x.double().numpy(), s.double().numpy(), w13.double().numpy(), w2.double().numpy(), 2)
     # Against the unquantised math the four e4m3 roundings (3 mantissa bits
@@ -111,7 +117,11 @@ def test_fp8_forward_matches_dense_formulation():
     _close(got, dense_forward(*args, cfg.T), 0.1, 0.6)
     # Against the same math with the fake-quantised GEMMs only the bf16
     # roundings between stages remain.
-    _close(got, dense_forward_fake_quant(*args), 2e-2, 0.2)
+    _close(got, dense_forward_fake_quant(*args, z_bf16=z_bf16), 2e-2, 0.2)
+    if z_bf16:   # the bf16 z is the one quantised: the composition's z stage equals silu_mul's output
+        zq, zs = oracle.quantize_rows(oracle.bf16_to_f32(oracle.silu_mul(res["y"], 48)), 1200.0)
+        np.testing.assert_array_equal(res["z"], zq)
+        np.testing.assert_array_equal(res["z_scale"], zs)
 
 
 def test_scaling_is_applied_to_the_expert_input():
@@ -141,14 +151,15 @@ def test_out_init_is_accumulated_into():
     np.testing.assert_allclose(f64(b["out"]), f64(a["out"]) + 3.0, atol=2 ** -6 * 4)
 
 
-@pytest.mark.parametrize("fp8", [False, True])
-def test_sampled_tokens_equal_the_full_forward(fp8):
+@pytest.mark.parametrize("fp8,z_bf16", [(False, False), (True, False), (True, True)])
+def test_sampled_tokens_equal_the_full_forward(fp8, z_bf16):
     cfg, x, s, w13, w2 = _problem(9, T=30, D=32, H=16, E=6, k=2, std=0.1, fp8=fp8)
     if fp8:
         weights = lambda ids: (w13[ids].numpy(), w2[ids].numpy())
     else:
         weights = lambda ids: (bits(w13[ids]), bits(w2[ids]))
-    full = oracle.moe_forward(bits(x), bits(s), 2, weights, fp8=fp8, scale_ub=1200.0)
+    full = oracle.moe_forward(bits(x), bits(s), 2, weights, fp8=fp8, scale_ub=1200.0, z_bf16=z_bf16)
     sample = np.array([0, 7, 8, 29])
-    part, _ = oracle.moe_forward_tokens(sample, bits(x), bits(s), 2, weights, fp8=fp8, scale_ub=1200.0)
+    part, _ = oracle.moe_forward_tokens(sample, bits(x), bits(s), 2, weights, fp8=fp8, scale_ub=1200.0,
+                                        z_bf16=z_bf16)
     np.testing.assert_array_equal(part, full["out"][sample])

@@ -128,10 +128,11 @@ def test_shared_expert_equals_one_expert_with_unit_scores():
     T, D, H = 12, 64, 48
     x = _rand_bf16(rng, T, D)
     ones = _bf16(np.ones((T, 1)))
-    for fp8 in (False, True):
+    for fp8, z_bf16 in ((False, False), (True, False), (True, True)):
         w13, w2 = _expert(rng, D, H, fp8)
-        got = oracle.shared_expert(x, w13, w2, fp8=fp8, scale_ub=30.0)
-        ref = oracle.moe_forward(x, ones, 1, lambda ids: (w13[None], w2[None]), fp8=fp8, scale_ub=30.0)["out"]
+        got = oracle.shared_expert(x, w13, w2, fp8=fp8, scale_ub=30.0, z_bf16=z_bf16)
+        ref = oracle.moe_forward(x, ones, 1, lambda ids: (w13[None], w2[None]), fp8=fp8, scale_ub=30.0,
+                                 z_bf16=z_bf16)["out"]
         np.testing.assert_array_equal(got, ref)
 
 
@@ -198,7 +199,9 @@ def test_layer_forward_tokens_equals_full_rows():
     w2 = rng.standard_normal((E, D, H)).astype(np.float32) * 0.05
     sh = _expert(rng, D, H, True)
     wf = lambda ids: (w13[ids], w2[ids])
-    full = oracle.moe_layer_forward(x, wr, k, wf, fp8=True, shared=sh, scale_ub=20.0)["out"]
     tok = np.array([0, 3, 7, 19])
-    part, _ = oracle.moe_layer_forward_tokens(tok, x, wr, k, wf, fp8=True, shared=sh, scale_ub=20.0)
-    np.testing.assert_array_equal(part, full[tok])
+    for z_bf16 in (False, True):
+        full = oracle.moe_layer_forward(x, wr, k, wf, fp8=True, shared=sh, scale_ub=20.0, z_bf16=z_bf16)["out"]
+        part, _ = oracle.moe_layer_forward_tokens(tok, x, wr, k, wf, fp8=True, shared=sh, scale_ub=20.0,
+                                                  z_bf16=z_bf16)
+        np.testing.assert_array_equal(part, full[tok])

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from tests.helpers import bf16_from_bits, bits, f64, parse_golden
+from tests.helpers import bf16_from_bits, bits, e4m3_step_diff, f64, parse_golden
 
 
 def _rand_bf16(rng, *shape, scale=1.0):
@@ -146,6 +146,32 @@ def test_silu_mul_quant_consistent_with_silu_and_quant_rule():
     err = np.abs(deq - z[:9])
     assert np.all(err <= 2.0 ** -4 * np.abs(z[:9]) + 2.0 ** -10 * m[:9, None] / 448 * 1.01)
     assert np.all(zq[9] == 0) and zs[9] == 0
+
+
+def test_silu_mul_quant_of_bf16_z_is_the_row_rule_on_silu_mul_output():
+    """z_bf16=True quantises the bf16 z that silu_mul writes: here the row rule is
+    applied by PyTorch (fp32 max, IEEE division and reciprocal, its own e4m3 cast)
+    to the oracle's silu_mul output, and codes and scales must match exactly."""
+    rng = np.random.default_rng(16)
+    a, H, v = 12, 160, 11
+    y = _rand_bf16(rng, a, 2 * H, scale=2.5)
+    y[3, :H] = bits(torch.full((H,), 40.0, dtype=torch.bfloat16))      # a large row: the bound 1200 binds
+    y[3, H:] = bits(torch.full((H,), 64.0, dtype=torch.bfloat16))
+    y[5] = 0                                                             # an all-zero row: m = EPS
+    zq, zs = oracle.silu_mul_quant(y, H, scale_ub=1200.0, valid_rows=v, z_bf16=True)
+    zb = bf16_from_bits(oracle.silu_mul(y, H, v)[:v]).float()
+    m = torch.clamp(zb.abs().amax(dim=1), min=1e-12)
+    m = torch.minimum(m, torch.tensor(1200.0))
+    s = torch.tensor(448.0) / m
+    q = (zb * s[:, None]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+    np.testing.assert_array_equal(zq[:v], q.view(torch.uint8).numpy())
+    np.testing.assert_array_equal(zs[:v], (1.0 / s).numpy())
+    assert zs[3] == np.float32(1) / (np.float32(448) / np.float32(1200))
+    assert np.all(zq[v:] == 0) and np.all(zs[v:] == 0)
+    # the fp32-z reading differs on a few codes (double rounding), by one step at most
+    zq32, zs32 = oracle.silu_mul_quant(y, H, scale_ub=1200.0, valid_rows=v)
+    diff = e4m3_step_diff(zq[:v], zq32[:v])
+    assert diff.max() <= 1 and 0 < (diff > 0).mean() < 0.05
 
 
 # ------------------------------------------------------------- scatter-add
