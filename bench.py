@@ -161,12 +161,15 @@ def oracle_forward_tokens(cfg, toks, xb, sb, weights, layer, weighting: str):
     import oracle
 
     if layer is not None:
-        return oracle.moe_layer_forward_tokens(toks, xb, layer[0], cfg.top_k, weights, fp8=cfg.fp8, shared=layer[1],
+        return oracle.moe_layer_forward_tokens(toks, xb, layer[0], cfg.top_k, weights, fp8=cfg.fp8, z_bf16=cfg.fp8,
+                                               shared=layer[1],
                                                scale_ub=cfg.scale_ub, weighting=weighting)[0]
     if weighting == "output":
         return oracle.moe_forward_output_weighted(np.ascontiguousarray(xb[toks]), np.ascontiguousarray(sb[toks]),
-                                                  cfg.top_k, weights, fp8=cfg.fp8, scale_ub=cfg.scale_ub)["out"]
-    return oracle.moe_forward_tokens(toks, xb, sb, cfg.top_k, weights, fp8=cfg.fp8, scale_ub=cfg.scale_ub)[0]
+                                                  cfg.top_k, weights, fp8=cfg.fp8, z_bf16=cfg.fp8,
+                                                  scale_ub=cfg.scale_ub)["out"]
+    return oracle.moe_forward_tokens(toks, xb, sb, cfg.top_k, weights, fp8=cfg.fp8, z_bf16=cfg.fp8,
+                                     scale_ub=cfg.scale_ub)[0]
 
 
 def oracle_tokens_per_s(cfg, x, s, w13, w2, seconds: float, max_tokens: int | None = None, layer=None,
@@ -462,32 +465,32 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
     value = job_tokens_per_s(cfg.valid_tokens, world, ms)
 
     # algorithmic work per stage (one launch each per step)
-    gemm1 = "gemm_w13" if cfg.fp8 else "gemm_w13_silu"
+    gemm1 = "gemm_w13_silu_quant" if cfg.fp8 else "gemm_w13_silu"
     mlp_bytes = (active * 3 * H * D * wb + a * D * wb + a * H * 2 * 2 + a * D * 2)
     work = {
         "route": ("hbm", cfg.valid_tokens * E * 2 + a * 12 + 8 * (E + 1)),
         "expert_mlp": ("gemm", mlp_bytes, 2.0 * a * 3 * H * D),
         ("gather_quant" if cfg.fp8 else "gather"): ("hbm", cfg.valid_tokens * D * 2 + a * D * wb + a * (14 if cfg.fp8 else 10)),
-        gemm1: ("gemm", active * 2 * H * D * wb + a * D * wb + a * (2 * H * 2 if cfg.fp8 else H * 2),
+        # FP8: the SILU_MUL_QUANT epilogue writes bf16 z, and its row pass reads it and writes e4m3 z + scales
+        gemm1: ("gemm", active * 2 * H * D * wb + a * D * wb + a * (H * 2 * 2 + H + 8 if cfg.fp8 else H * 2),
                 2.0 * a * 2 * H * D),
         "gemm_w2": ("gemm", active * D * H * wb + a * H * wb + a * D * 2, 2.0 * a * D * H),
         "scatter": ("hbm", a * D * 2 + cfg.valid_tokens * D * 2 + (a * 4 if k > 1 else 0)),
     }
-    if cfg.fp8:
-        work["silu_quant"] = ("hbm", a * 2 * H * 2 + a * H + a * 4)
     # top-k finalize: the weighted rows, weights and indices in, the tokens out (+ the shared output read)
     work["finalize"] = ("hbm", a * D * 2 + a * 8 + cfg.valid_tokens * D * 2 * (2 if layer.shared else 1))
     full = args.layer == "full"
     if full:
         Tv = cfg.valid_tokens
         Hs = layer.Hs
-        work["router"] = ("hbm", Tv * D * 2 + E * D * 2 + Tv * E * 2)
+        # the router GEMM with the top-k selection in its epilogue, and the routing's emit kernel
+        work["router_route"] = ("hbm", Tv * D * 2 + E * D * 2 + Tv * E * 2 + a * 12 + 8 * (E + 1))
         work["shared_mlp"] = ("gemm", 3 * Hs * D * 2 + Tv * D * 2 + Tv * Hs * 2 * 2 + Tv * D * 2,
                               2.0 * Tv * 3 * Hs * D)
         work["shared_w13_silu"] = ("gemm", 2 * Hs * D * 2 + Tv * D * 2 + Tv * Hs * 2, 2.0 * Tv * 2 * Hs * D)
         work["shared_quant"] = ("hbm", Tv * D * 2 + Tv * D + Tv * 16)
-        work["shared_w13"] = ("gemm", 2 * Hs * D + Tv * D + Tv * 2 * Hs * 2, 2.0 * Tv * 2 * Hs * D)
-        work["shared_silu_quant"] = ("hbm", Tv * 2 * Hs * 2 + Tv * Hs + Tv * 4)
+        work["shared_w13_silu_quant"] = ("gemm", 2 * Hs * D + Tv * D + Tv * 4 + Tv * (Hs * 2 * 2 + Hs + 4),
+                                         2.0 * Tv * 2 * Hs * D)
         work["shared_w2"] = ("gemm", D * Hs * wb + Tv * Hs * wb + Tv * D * 2, 2.0 * Tv * D * Hs)
         # the routed combine adds into the shared expert's output: one more read of it
         comb = layer.combine_stage(names)
@@ -561,9 +564,7 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
 # on: when those sources change the figure no longer applies and is reported as null.
 TRAFFIC: dict = {
     ("decode", "expert_mlp"): (4_037_701_632 + 5_910_016, "grouped_gemm.cu", "f88d8b86b567"),
-    ("prefill_fp8", "gemm_w13"): (1_385_865_472 + 251_826_944, "grouped_gemm.cu", "f88d8b86b567"),
     ("fine_grained", "gemm_w13_silu"): (2_559_575_552 + 133_741_824, "grouped_gemm.cu", "f88d8b86b567"),
-    ("padded_fp8", "gemm_w13"): (1_793_144_576 + 256_664_576, "grouped_gemm.cu", "f88d8b86b567"),
 }
 
 

@@ -6,6 +6,8 @@
  * mslk/moe/layers.py, MetaShufflingMoE._no_comm_forward:
  *
  *   moe_router_scores         router scores sigmoid(tokens @ router_DE), bf16
+ *   moe_router_route          ... with the top-k selection in the router's
+ *                             epilogue, then the by-expert permutation
  *   moe_route                 top-k routing into per-expert counts and a
  *                             by-expert token permutation (index_shuffling)
  *   moe_gather_scale          gather token rows and multiply by the score
@@ -65,6 +67,7 @@ extern "C" {
 /* Grouped-GEMM epilogues. */
 #define MOE_EPILOGUE_NONE 0     /* y[r, n] = (x_r . w_e[n]) (times the two scales for FP8), bf16 */
 #define MOE_EPILOGUE_SILU_MUL 1 /* with N = 2H: y[r, j] = silu(v_j) * v_{H+j}, j < H, bf16 */
+#define MOE_EPILOGUE_SILU_MUL_QUANT 2 /* SILU_MUL, then each row of y quantised to e4m3 (z_out, z_scale) */
 /* OR-ed into `epilogue` of the grouped GEMMs: compute 256-row x 256-column tiles on
  * pairs of SMs (a 2-CTA cluster, tcgen05 cta_group::2).  Same results; faster when
  * experts hold many rows; an expert whose rows end mid-tile still pays for the
@@ -149,6 +152,31 @@ int moe_selftest_bounded_wait(int which, int64_t limit_ns, cudaStream_t stream);
 /* ------------------------------------------------------------------ routing */
 
 /*
+ * The router and the routing in two kernels: moe_router_scores with the top-k
+ * selection of moe_route folded into its reduction epilogue (mslk/moe/layers.py,
+ * MetaShufflingMoE._route: sigmoid(linear(tokens, router_DE.T)) followed by
+ * index_shuffling).  The CTA that sums a 32-token chunk of router logits over
+ * its thread-block cluster forms the chunk's bf16 scores, stores them, picks
+ * each token's top_k experts and writes the chunk's expert histogram to the
+ * workspace; one cooperative kernel then scans the histograms and emits the
+ * routed rows (one grid barrier, against two after a separate moe_route).
+ *
+ * x, T, D, w_router, E, num_valid_tokens: as moe_router_scores (E <= 256).
+ * scores: bf16 [T, E] (required): written exactly as moe_router_scores writes it.
+ * counts, expert_offsets, expert_indices, token_indices, inv_rows (nullable),
+ * topk_weights (nullable), top_k: as moe_route on those scores, bit for bit.
+ * ws, ws_bytes: device workspace of moe_router_route_workspace_size bytes,
+ * 256-byte aligned; its contents on entry do not matter.
+ * T == 0 writes zero counts and offsets.  The result is deterministic.
+ */
+int moe_router_route_workspace_size(int T, int D, int E, int top_k, size_t* bytes);
+int moe_router_route(const void* x, int T, int D, const void* w_router, int E, int top_k,
+                     const int32_t* num_valid_tokens, void* scores, int32_t* counts,
+                     int32_t* expert_offsets, int32_t* expert_indices, int32_t* token_indices,
+                     int32_t* inv_rows, float* topk_weights, void* ws, size_t ws_bytes,
+                     cudaStream_t stream);
+
+/*
  * Bytes of device workspace moe_route needs for T token rows, E experts and
  * top_k (host call, no GPU use).
  */
@@ -210,13 +238,23 @@ int moe_route(const void* scores, int scores_dtype, int64_t stride_t, int64_t st
  *   MOE_ROUTE_NO_ALLOC_SCRATCH_BYTES (1 MiB).  For example T = 16384,
  *   top_k = 4, E = 128 needs 0.5 MiB and fits; T = 65536, top_k = 1,
  *   E = 128 needs 1.25 MiB and is rejected.
- * - Set-up: the first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress, with that device current) and keeps it; make that
- *   first call before any stream capture.  A failed lookup returns
- *   MOE_ERR_CUDA with the code in moe_last_cuda_error().
+ * - Set-up: the first call on each device (with that device current) looks up
+ *   the array's device address (cudaGetSymbolAddress) and loads the routing
+ *   kernels, and keeps the address.  CUDA loads a library's device code
+ *   lazily, so that first call is when the driver places this array and the
+ *   routing code in device memory: an allocation made by the driver, not by
+ *   the caller, which an out-of-memory situation can make fail (MOE_ERR_CUDA).
+ *   Make that first call at start-up, before the code that must not allocate
+ *   and before any stream capture; a call with T = 0 (valid counts and
+ *   expert_offsets pointers) does the set-up, writes zero counts and launches
+ *   no routing kernel.  After the device's context changes (cudaDeviceReset)
+ *   the next call sets up again.  A failed set-up returns MOE_ERR_CUDA with the
+ *   code in moe_last_cuda_error().
  * - Sharing: every call on a device uses the same array and leaves its
  *   contents behind.  The routing kernels write every scratch word before
- *   reading it, so nothing needs clearing between calls, but calls whose
+ *   reading it, except the grid-barrier counter of the large-batch kernel,
+ *   which each call zeroes with an asynchronous memset on the stream before
+ *   that kernel starts; so nothing needs clearing between calls.  Calls whose
  *   kernels overlap on the GPU (for example on two streams without ordering
  *   between them) race on the array and give wrong results: order them.
  * Arguments, outputs and results are those of moe_route.
@@ -312,10 +350,30 @@ int moe_quantize_rows(const float* w, int64_t rows, int cols, const float* scale
  * f32(o)) with accumulate != 0 (moe_scatter_add's arithmetic), y = o with
  * accumulate == 0.  Rows of y that no routed row names are not touched; an
  * index outside [0, T_out) is skipped and flagged.
+ *
+ * epilogue MOE_EPILOGUE_SILU_MUL_QUANT: the SiLU*mul epilogue followed by the
+ *   FP8-rowwise quantisation of z that the FP8 w2 GEMM takes, the
+ *   silu_mul_quant(y0, y1, scale_ub) step of _routed_expert's FP8 branch.  y
+ *   [a_max, H] bf16 receives z = bf16(silu(y0) * y1) exactly as with SILU_MUL
+ *   (the row max spans every N tile of the row, which different CTAs compute,
+ *   so z crosses HBM once, as bf16: 2 bytes per element instead of the 4 of
+ *   the unfused y0, y1); then each routed row of z is quantised with the rule
+ *   of moe_gather_scale_quant at unit score: m = max_j |z_j|, clamped to
+ *   [1e-12, *scale_ub] (scale_ub: device fp32, nullable: no upper bound),
+ *   s = 448 / m, z_scale[r] = 1 / s, z_out[r, j] = e4m3(clamp(z_j * s, +-448)).
+ *   z_out [a_max, H] e4m3 and z_scale [a_max] fp32; rows past sum(counts) are
+ *   not written.  The bf16 rounding of z before its quantisation is the order
+ *   of BaselineMoE._forward, where routed_z is a bf16 tensor when _fake_quant
+ *   quantises it; the result equals SILU_MUL followed by moe_gather_scale_quant
+ *   of y with identity indices and unit scores, bit for bit.  H <= 16384.
+ *   Two kernels run on the stream: the GEMM, then a row pass over y.
+ * scale_ub, z_out, z_scale: used by MOE_EPILOGUE_SILU_MUL_QUANT only (z_out and
+ *   z_scale are then required, 16-byte aligned z_out); ignored otherwise.
  */
 int moe_grouped_gemm(const void* x, const void* w, const int32_t* counts, int E, int a_max, int N,
                      int K, void* y, int epilogue, const int32_t* scatter_indices, int T_out,
-                     int accumulate, cudaStream_t stream);
+                     int accumulate, const float* scale_ub, void* z_out, float* z_scale,
+                     cudaStream_t stream);
 
 /*
  * grouped_gemm_fp8_rowwise(x, w, counts, x_scale, w_scale) of
@@ -323,12 +381,17 @@ int moe_grouped_gemm(const void* x, const void* w, const int32_t* counts, int E,
  *   v[r, n] = (sum_k x[r, k] * w[e, n, k]) * x_scale[r] * w_scale[e * N + n]
  * (fp32; the dequantisation order of BaselineMoE._fake_quant).
  * x [a_max, K] e4m3, w [E, N, K] e4m3, x_scale [a_max] fp32, w_scale [E * N]
- * fp32.  Epilogues and the fused combine as in moe_grouped_gemm.
+ * fp32.  Epilogues and the fused combine as in moe_grouped_gemm; with
+ * MOE_EPILOGUE_SILU_MUL_QUANT the v above (dequantised, then rounded to bf16)
+ * are the y0, y1 of SiLU*mul, and z_out, z_scale feed the FP8 w2 GEMM as its
+ * x, x_scale (_routed_expert's grouped_gemm_fp8_rowwise -> silu_mul_quant ->
+ * grouped_gemm_fp8_rowwise).
  */
 int moe_grouped_gemm_fp8_rowwise(const void* x, const void* w, const int32_t* counts,
                                  const float* x_scale, const float* w_scale, int E, int a_max,
                                  int N, int K, void* y, int epilogue, const int32_t* scatter_indices,
-                                 int T_out, int accumulate, cudaStream_t stream);
+                                 int T_out, int accumulate, const float* scale_ub, void* z_out,
+                                 float* z_scale, cudaStream_t stream);
 
 /*
  * Both grouped GEMMs of the bf16 routed experts in one persistent launch:

@@ -21,7 +21,7 @@ HEADER = _PKG.parent / "include" / "moe.h"
 
 MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_WORKSPACE = 0, -1, -2, -3, -4
 MOE_DTYPE_BF16, MOE_DTYPE_F32, MOE_DTYPE_E4M3 = 0, 1, 2
-MOE_EPILOGUE_NONE, MOE_EPILOGUE_SILU_MUL = 0, 1
+MOE_EPILOGUE_NONE, MOE_EPILOGUE_SILU_MUL, MOE_EPILOGUE_SILU_MUL_QUANT = 0, 1, 2
 MOE_GEMM_CTA_PAIRS = 0x100
 MOE_WEIGHTS_PACKED = 0x200
 MOE_DEVERR_BAD_INDEX, MOE_DEVERR_BAD_COUNT, MOE_DEVERR_TIMEOUT = 1, 2, 4
@@ -48,6 +48,8 @@ def _load() -> ctypes.CDLL:
         "moe_device_error": ([U, P], I),
         "moe_router_workspace_size": ([I, I, I, ctypes.POINTER(S)], I),
         "moe_router_scores": ([P, I, I, P, I, P, P, P, S, P], I),
+        "moe_router_route_workspace_size": ([I, I, I, I, ctypes.POINTER(S)], I),
+        "moe_router_route": ([P, I, I, P, I, I, P, P, P, P, P, P, P, P, P, S, P], I),
         "moe_dense_gemm": ([P, I, I, P, I, P, P, I, P], I),
         "moe_selftest_bounded_wait": ([I, L, P], I),
         "moe_route_workspace_size": ([I, I, I, ctypes.POINTER(S)], I),
@@ -56,14 +58,14 @@ def _load() -> ctypes.CDLL:
         "moe_gather_scale": ([P, I, I, P, P, I, P, I, L, L, I, P, P, I, P, P], I),
         "moe_gather_scale_quant": ([P, I, I, P, P, I, P, I, L, L, I, P, P, I, P, P, P, P], I),
         "moe_quantize_rows": ([P, L, I, P, P, P, P], I),
-        "moe_grouped_gemm": ([P, P, P, I, I, I, I, P, I, P, I, I, P], I),
+        "moe_grouped_gemm": ([P, P, P, I, I, I, I, P, I, P, I, I, P, P, P, P], I),
         "moe_expert_mlp_workspace_size": ([I, ctypes.POINTER(S)], I),
         "moe_scatter_add_padded": ([P, P, P, I, P, P, I, I, I, I, I, P], I),
         "moe_topk_finalize": ([P, L, I, P, I, P, I, I, P, P, P, P], I),
         "moe_expert_mlp": ([P, P, P, P, I, I, I, I, P, P, P, I, I, P, S, I, P], I),
         "moe_pack_weights_size": ([I, I, I, I, ctypes.POINTER(S)], I),
         "moe_pack_weights": ([P, I, I, I, I, P, P], I),
-        "moe_grouped_gemm_fp8_rowwise": ([P, P, P, P, P, I, I, I, I, P, I, P, I, I, P], I),
+        "moe_grouped_gemm_fp8_rowwise": ([P, P, P, P, P, I, I, I, I, P, I, P, I, I, P, P, P, P], I),
         "moe_silu_mul": ([P, P, L, I, I, P, P, P], I),
         "moe_silu_mul_quant": ([P, P, L, I, I, P, P, P, P, P], I),
         "moe_scatter_add": ([P, P, P, P, I, I, I, I, P, I, P], I),
@@ -156,6 +158,49 @@ def moe_router_scores(x: torch.Tensor, w_router: torch.Tensor, num_valid_tokens:
                                 _ptr(workspace), workspace.numel(), _stream(stream))
     _check("moe_router_scores", st)
     return out
+
+
+def moe_router_route_workspace_size(T: int, D: int, E: int, top_k: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check("moe_router_route_workspace_size", _lib.moe_router_route_workspace_size(T, D, E, top_k, ctypes.byref(n)))
+    return n.value
+
+
+def moe_router_route(x: torch.Tensor, w_router: torch.Tensor, top_k: int, num_valid_tokens=None, *,
+                     scores: torch.Tensor | None = None, with_weights: bool = False, out: dict | None = None,
+                     workspace: torch.Tensor | None = None, stream=None):
+    """Router scores and routing in two kernels (the top-k selection in the router's
+    epilogue).  Returns (scores[T, E] bf16, the dict of moe_route)."""
+    T, D = x.shape
+    E = w_router.shape[0]
+    _need(x, torch.bfloat16, "x")
+    _need(w_router, torch.bfloat16, "w_router")
+    if num_valid_tokens is not None:
+        _need(num_valid_tokens, torch.int32, "num_valid_tokens")
+    if scores is None:
+        scores = torch.empty(T, E, dtype=torch.bfloat16, device=x.device)
+    _need(scores, torch.bfloat16, "scores")
+    dev = x.device
+    o = dict(out or {})
+    i32 = dict(dtype=torch.int32, device=dev)
+    o.setdefault("counts", torch.empty(E + 1, **i32))
+    o.setdefault("expert_offsets", torch.empty(E + 1, **i32))
+    o.setdefault("expert_indices", torch.empty(T * top_k, **i32))
+    o.setdefault("token_indices", torch.empty(T * top_k, **i32))
+    o.setdefault("inv_rows", torch.empty(T * top_k, **i32))
+    if with_weights:
+        o.setdefault("topk_weights", torch.empty(T * top_k, dtype=torch.float32, device=dev))
+    else:
+        o["topk_weights"] = None
+    ws_bytes = moe_router_route_workspace_size(T, D, E, top_k)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    st = _lib.moe_router_route(_ptr(x), T, D, _ptr(w_router), E, top_k, _ptr(num_valid_tokens), _ptr(scores),
+                               _ptr(o["counts"]), _ptr(o["expert_offsets"]), _ptr(o["expert_indices"]),
+                               _ptr(o["token_indices"]), _ptr(o["inv_rows"]), _ptr(o["topk_weights"]),
+                               _ptr(workspace), workspace.numel(), _stream(stream))
+    _check("moe_router_route", st)
+    return scores, o
 
 
 def moe_route_workspace_size(T: int, E: int, top_k: int) -> int:
@@ -310,42 +355,62 @@ def _weights_arg(w, dtype, name: str, flags: int):
     return _ptr(w), flags
 
 
+def _gemm_outputs(x, N, epilogue, out, z_out, z_scale):
+    """The bf16 output (y, or z for the SiLU epilogues) and, with SILU_MUL_QUANT,
+    the e4m3 z and its row scales; allocated when not given."""
+    a_max = x.shape[0]
+    kind = epilogue & 0xFF
+    n_out = N // 2 if kind in (MOE_EPILOGUE_SILU_MUL, MOE_EPILOGUE_SILU_MUL_QUANT) else N
+    if out is None:
+        out = torch.empty(a_max, n_out, dtype=torch.bfloat16, device=x.device)
+    _need(out, out.dtype, "out")
+    if kind != MOE_EPILOGUE_SILU_MUL_QUANT:
+        return out, None, None
+    if z_out is None:
+        z_out = torch.empty(a_max, n_out, dtype=torch.float8_e4m3fn, device=x.device)
+    _need(z_out, torch.float8_e4m3fn, "z_out")
+    if z_scale is None:
+        z_scale = torch.empty(a_max, dtype=torch.float32, device=x.device)
+    _need(z_scale, torch.float32, "z_scale")
+    return out, z_out, z_scale
+
+
 def moe_grouped_gemm(x, w, counts, *, epilogue: int = MOE_EPILOGUE_NONE, out=None, scatter_indices=None,
-                     accumulate: bool = True, stream=None):
+                     accumulate: bool = True, scale_ub=None, z_out=None, z_scale=None, stream=None):
     """x[a_max, K] bf16, w[E, N, K] bf16, counts[>= E] int32 -> y[a_max, N or N/2].
-    With scatter_indices (top_k = 1), routed row r lands in out[scatter_indices[r]]."""
+    With scatter_indices (top_k = 1), routed row r lands in out[scatter_indices[r]].
+    With MOE_EPILOGUE_SILU_MUL_QUANT, out receives the bf16 z and the call returns
+    (z_out e4m3 [a_max, N/2], z_scale fp32 [a_max]) instead."""
     a_max, K = x.shape
     E, N, K2 = w.shape
     assert K == K2
     _need(x, torch.bfloat16, "x")
     w_ptr, epilogue = _weights_arg(w, torch.bfloat16, "w", epilogue)
-    n_out = N // 2 if (epilogue & 0xFF) == MOE_EPILOGUE_SILU_MUL else N
     si, t_out, acc = _scatter_args(scatter_indices, out, accumulate)
-    if out is None:
-        out = torch.empty(a_max, n_out, dtype=torch.bfloat16, device=x.device)
-    _need(out, out.dtype, "out")
+    out, z_out, z_scale = _gemm_outputs(x, N, epilogue, out, z_out, z_scale)
     st = _lib.moe_grouped_gemm(_ptr(x), w_ptr, _ptr(counts), E, a_max, N, K, _ptr(out), epilogue, _ptr(si),
-                               t_out, acc, _stream(stream))
+                               t_out, acc, _ptr(scale_ub), _ptr(z_out), _ptr(z_scale), _stream(stream))
     _check("moe_grouped_gemm", st)
-    return out
+    return out if z_out is None else (z_out, z_scale)
 
 
 def moe_grouped_gemm_fp8_rowwise(x, w, counts, x_scale, w_scale, *, epilogue: int = MOE_EPILOGUE_NONE, out=None,
-                                 scatter_indices=None, accumulate: bool = True, stream=None):
+                                 scatter_indices=None, accumulate: bool = True, scale_ub=None, z_out=None,
+                                 z_scale=None, stream=None):
+    """As moe_grouped_gemm on e4m3 x[a_max, K] and w[E, N, K] with fp32 row scales
+    x_scale[a_max] and w_scale[E, N]."""
     a_max, K = x.shape
     E, N, K2 = w.shape
     assert K == K2
     _need(x, torch.float8_e4m3fn, "x")
     w_ptr, epilogue = _weights_arg(w, torch.float8_e4m3fn, "w", epilogue)
-    n_out = N // 2 if (epilogue & 0xFF) == MOE_EPILOGUE_SILU_MUL else N
     si, t_out, acc = _scatter_args(scatter_indices, out, accumulate)
-    if out is None:
-        out = torch.empty(a_max, n_out, dtype=torch.bfloat16, device=x.device)
-    _need(out, out.dtype, "out")
+    out, z_out, z_scale = _gemm_outputs(x, N, epilogue, out, z_out, z_scale)
     st = _lib.moe_grouped_gemm_fp8_rowwise(_ptr(x), w_ptr, _ptr(counts), _ptr(x_scale), _ptr(w_scale), E, a_max,
-                                           N, K, _ptr(out), epilogue, _ptr(si), t_out, acc, _stream(stream))
+                                           N, K, _ptr(out), epilogue, _ptr(si), t_out, acc, _ptr(scale_ub),
+                                           _ptr(z_out), _ptr(z_scale), _stream(stream))
     _check("moe_grouped_gemm_fp8_rowwise", st)
-    return out
+    return out if z_out is None else (z_out, z_scale)
 
 
 def moe_expert_mlp_workspace_size(E: int) -> int:

@@ -1,5 +1,7 @@
 // The C ABI of libmoe_gb300 (declared in include/moe.h): argument checks on
 // the host, then the launchers of the kernel translation units.
+#include <cuda.h>
+
 #include <map>
 #include <mutex>
 #include <utility>
@@ -31,17 +33,22 @@ int current_device(int* dev) {
   return MOE_OK;
 }
 
-// Device address of the error word on the current device (looked up once per device).
+unsigned long long g_err_ctx[kMaxDevices] = {};
+
+// Device address of the error word on the current device: looked up once per
+// device and context (again after the context changed, e.g. after cudaDeviceReset).
 int device_error_word(unsigned int** out) {
   int dev;
   int rc = current_device(&dev);
   if (rc != MOE_OK) return rc;
+  const unsigned long long ctx = moe::current_context_id();
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_err_ptr[dev]) {
+  if (!g_err_ptr[dev] || ctx == 0 || ctx != g_err_ctx[dev]) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_moe_device_error);
     if (e != cudaSuccess) return cuda_fail(e);
     g_err_ptr[dev] = static_cast<unsigned int*>(p);
+    g_err_ctx[dev] = moe::current_context_id();  // the lookup made the primary context current if it was not
   }
   *out = g_err_ptr[dev];
   return MOE_OK;
@@ -63,6 +70,31 @@ int check_scores(const void* scores, int dtype, int E) {
 
 namespace moe {
 void record_cuda_error(int e) { t_last_cuda_error = e; }
+
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+    cudaGetLastError();  // a failed lookup leaves no sticky error behind
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
 
 int resident_blocks_per_sm(const void* kernel, int threads) {
   int dev = 0;
@@ -169,6 +201,38 @@ int moe_router_scores(const void* x, int T, int D, const void* w_router, int E, 
   rc = device_error_word(&a.err);
   if (rc != MOE_OK) return rc;
   return finish(moe::launch_router_scores(a, stream));
+}
+
+int moe_router_route_workspace_size(int T, int D, int E, int top_k, size_t* bytes) {
+  size_t router = 0;
+  int rc = moe_router_workspace_size(T, D, E, &router);
+  if (rc != MOE_OK) return rc;
+  return moe_route_workspace_size(T, E, top_k, bytes);
+}
+
+int moe_router_route(const void* x, int T, int D, const void* w_router, int E, int top_k,
+                     const int32_t* num_valid_tokens, void* scores, int32_t* counts, int32_t* expert_offsets,
+                     int32_t* expert_indices, int32_t* token_indices, int32_t* inv_rows, float* topk_weights,
+                     void* ws, size_t ws_bytes, cudaStream_t stream) {
+  size_t need;
+  int rc = moe_router_route_workspace_size(T, D, E, top_k, &need);
+  if (rc != MOE_OK) return rc;
+  if (!counts || !expert_offsets) return MOE_ERR_INVALID;
+  if (T > 0 && (!x || !w_router || !scores || !expert_indices || !token_indices || !ws)) return MOE_ERR_INVALID;
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_INVALID;
+  if (T > 0 && (!aligned16(x) || !aligned16(w_router) || (reinterpret_cast<uintptr_t>(scores) & 1u)))
+    return MOE_ERR_UNSUPPORTED;
+  moe::RouteArgs r{scores,         MOE_DTYPE_BF16, E,       1,        T,  E,      top_k,
+                   num_valid_tokens, counts,       expert_offsets, expert_indices, token_indices, inv_rows,
+                   topk_weights,   ws,             nullptr};
+  rc = device_error_word(&r.err);
+  if (rc != MOE_OK) return rc;
+  if (T == 0) return finish(moe::launch_route(r, stream));  // zero counts and offsets
+  moe::RouterArgs a{x, T, D, w_router, E, num_valid_tokens, scores, nullptr, r.err};
+  cudaError_t e = moe::launch_router_route(a, top_k, moe::route_workspace(ws, T, top_k), stream);
+  if (e != cudaSuccess) return finish(e);
+  return finish(moe::launch_route_emit(r, stream));
 }
 
 int moe_dense_gemm(const void* x, int M, int K, const void* w, int N, const int32_t* valid_rows, void* y,
@@ -327,31 +391,39 @@ int moe_topk_finalize(const void* rows, int64_t n_rows, int D, const void* exper
 
 static int grouped_gemm_common(const void* x, const void* w, const int32_t* counts, const float* x_scale,
                                const float* w_scale, int E, int a_max, int N, int K, void* y, int epilogue,
-                               const int32_t* scatter, int T_out, int accumulate, bool fp8,
-                               cudaStream_t stream) {
+                               const int32_t* scatter, int T_out, int accumulate, const float* scale_ub,
+                               void* z_out, float* z_scale, bool fp8, cudaStream_t stream) {
   if (E < 1 || a_max < 0 || N < 0 || K < 0) return MOE_ERR_INVALID;
   const bool pairs = (epilogue & MOE_GEMM_CTA_PAIRS) != 0;
   const bool packed = (epilogue & MOE_WEIGHTS_PACKED) != 0;
   epilogue &= ~(MOE_GEMM_CTA_PAIRS | MOE_WEIGHTS_PACKED);
-  if (epilogue != MOE_EPILOGUE_NONE && epilogue != MOE_EPILOGUE_SILU_MUL) return MOE_ERR_INVALID;
+  if (epilogue != MOE_EPILOGUE_NONE && epilogue != MOE_EPILOGUE_SILU_MUL && epilogue != MOE_EPILOGUE_SILU_MUL_QUANT)
+    return MOE_ERR_INVALID;
+  const bool quant = epilogue == MOE_EPILOGUE_SILU_MUL_QUANT;
+  const bool silu = epilogue != MOE_EPILOGUE_NONE;
   if (a_max == 0 || N == 0) return MOE_OK;
   if (!x || !w || !counts || !y) return MOE_ERR_INVALID;
   if (fp8 && (!x_scale || !w_scale)) return MOE_ERR_INVALID;
+  if (quant && (!z_out || !z_scale)) return MOE_ERR_INVALID;
   if (E > 1024) return MOE_ERR_UNSUPPORTED;
   if (N % 16 != 0 || K % 16 != 0 || K == 0) return MOE_ERR_UNSUPPORTED;
-  if (epilogue == MOE_EPILOGUE_SILU_MUL && (N % 32 != 0)) return MOE_ERR_UNSUPPORTED;
+  if (silu && (N % 32 != 0)) return MOE_ERR_UNSUPPORTED;
+  if (quant && (N / 2 > 16384 || !aligned16(z_out))) return MOE_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return MOE_ERR_UNSUPPORTED;
   if (scatter && (epilogue != MOE_EPILOGUE_NONE || T_out < 0)) return MOE_ERR_INVALID;
   // packed weights: every weight box starts at a 128-row block (SiLU*mul: both halves)
-  if (packed && (N % 128 != 0 || (epilogue == MOE_EPILOGUE_SILU_MUL && (N / 2) % 128 != 0)))
-    return MOE_ERR_UNSUPPORTED;
-  moe::GemmArgs g{x, w, counts, x_scale, w_scale, E, a_max, N, K, y, epilogue, fp8, pairs, packed, scatter, T_out,
-                  accumulate, nullptr};
+  if (packed && (N % 128 != 0 || (silu && (N / 2) % 128 != 0))) return MOE_ERR_UNSUPPORTED;
+  // the GEMM runs the SiLU*mul epilogue into y; SILU_MUL_QUANT then quantises y's rows
+  moe::GemmArgs g{x, w, counts, x_scale, w_scale, E, a_max, N, K, y, silu ? MOE_EPILOGUE_SILU_MUL : epilogue, fp8,
+                  pairs, packed, scatter, T_out, accumulate, nullptr};
   int rc = device_error_word(&g.err);
   if (rc != MOE_OK) return rc;
   cudaError_t e = moe::launch_grouped_gemm(g, stream);
   if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
-  return finish(e);
+  if (e != cudaSuccess || !quant) return finish(e);
+  const int H = N / 2;
+  moe::SiluArgs q{y, nullptr, H, a_max, H, nullptr, scale_ub, z_out, z_scale, g.err, counts, E};
+  return finish(moe::launch_quantize_rows_bf16(q, stream));
 }
 
 int moe_expert_mlp_workspace_size(int E, size_t* bytes) {
@@ -404,16 +476,18 @@ int moe_pack_weights(const void* w, int E, int N, int K, int dtype, void* packed
 }
 
 int moe_grouped_gemm(const void* x, const void* w, const int32_t* counts, int E, int a_max, int N, int K, void* y,
-                     int epilogue, const int32_t* scatter_indices, int T_out, int accumulate, cudaStream_t stream) {
+                     int epilogue, const int32_t* scatter_indices, int T_out, int accumulate, const float* scale_ub,
+                     void* z_out, float* z_scale, cudaStream_t stream) {
   return grouped_gemm_common(x, w, counts, nullptr, nullptr, E, a_max, N, K, y, epilogue, scatter_indices, T_out,
-                             accumulate, false, stream);
+                             accumulate, scale_ub, z_out, z_scale, false, stream);
 }
 
 int moe_grouped_gemm_fp8_rowwise(const void* x, const void* w, const int32_t* counts, const float* x_scale,
                                  const float* w_scale, int E, int a_max, int N, int K, void* y, int epilogue,
-                                 const int32_t* scatter_indices, int T_out, int accumulate, cudaStream_t stream) {
+                                 const int32_t* scatter_indices, int T_out, int accumulate, const float* scale_ub,
+                                 void* z_out, float* z_scale, cudaStream_t stream) {
   return grouped_gemm_common(x, w, counts, x_scale, w_scale, E, a_max, N, K, y, epilogue, scatter_indices, T_out,
-                             accumulate, true, stream);
+                             accumulate, scale_ub, z_out, z_scale, true, stream);
 }
 
 }  // extern "C"

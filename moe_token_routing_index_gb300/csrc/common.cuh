@@ -90,6 +90,14 @@ __device__ __forceinline__ float load_score(const void* scores, int dtype, int64
   return __bfloat162float(__ldg(reinterpret_cast<const __nv_bfloat16*>(scores) + off));
 }
 
+// Monotone map of a score to uint32 (larger score -> larger key), -0 folded onto
+// +0: the order in which top-k routing compares scores.
+__device__ __forceinline__ uint32_t route_order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // 8 bf16 in a uint4 <-> 8 floats.
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float* f) {
   const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);

@@ -27,6 +27,20 @@ struct RouteArgs {
 size_t route_workspace_bytes(int T, int E, int top_k);
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 
+// The routing workspace: the grid-barrier counter, the chosen experts of each
+// token [T * top_k] (selection order) and the per-chunk expert histograms
+// [E][ceil(T / 32)] (hist_t[e * nblk + c]: tokens of 32-token chunk c choosing e).
+struct RouteWorkspace {
+  unsigned int* barrier;
+  int32_t* chosen;
+  int32_t* hist_t;
+};
+RouteWorkspace route_workspace(void* ws, int T, int top_k);
+// The scan and emit phases of routing (one cooperative launch, one grid barrier),
+// after the router GEMM's epilogue has filled the workspace's chosen experts and
+// chunk histograms and zeroed its barrier counter.
+cudaError_t launch_route_emit(const RouteArgs& a, cudaStream_t s);
+
 struct RouterArgs {
   const void* x;       // bf16 [T, D]
   int T, D;
@@ -40,6 +54,12 @@ struct RouterArgs {
 
 size_t router_workspace_bytes(int T, int D, int E);
 cudaError_t launch_router_scores(const RouterArgs& a, cudaStream_t s);
+
+// Router scores with the routing selection in the reduction epilogue: scores as
+// launch_router_scores, plus the chosen experts, chunk histograms and zeroed
+// barrier counter of `w` (the routing workspace of T tokens and top_k) for
+// launch_route_emit.
+cudaError_t launch_router_route(const RouterArgs& a, int top_k, const RouteWorkspace& w, cudaStream_t s);
 
 struct DenseArgs {
   const void* x;             // bf16 [M, K]
@@ -90,10 +110,15 @@ struct SiluArgs {
   void* z;
   float* z_scale;         // quantising variant only
   unsigned int* err;
+  const int32_t* sum_counts;  // nullable: the valid row count is sum(sum_counts[0, E)) instead of *valid
+  int E;
 };
 
 cudaError_t launch_silu_mul(const SiluArgs& a, cudaStream_t s);
 cudaError_t launch_silu_mul_quant(const SiluArgs& a, cudaStream_t s);
+// Per-row FP8 quantisation of the bf16 rows x0 (row stride ld; x1 unused) with the
+// rule of silu_mul_quant: the second half of the SILU_MUL_QUANT GEMM epilogue.
+cudaError_t launch_quantize_rows_bf16(const SiluArgs& a, cudaStream_t s);
 
 struct ScatterArgs {
   void* out;
@@ -178,5 +203,14 @@ int resident_blocks_per_sm(const void* kernel, int threads);
 
 // Make `e` (a cudaError_t) what moe_last_cuda_error() reports on this thread.
 void record_cuda_error(int e);
+
+// A process-unique id of the calling thread's current CUDA context, 0 when there is
+// none or the driver cannot tell.  Device addresses cached per device are looked up
+// again when it changes (cudaDeviceReset replaces a device's primary context).
+unsigned long long current_context_id();
+
+// Load the routing kernels' device code on the current device (CUDA loads modules
+// lazily, at first use); no launch.
+cudaError_t preload_route_kernels();
 
 }  // namespace moe

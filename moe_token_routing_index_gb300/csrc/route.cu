@@ -27,13 +27,6 @@ constexpr int kTokBlock = 32;     // tokens per block (one bitmap word per exper
 constexpr int kRouteThreads = 1024;  // 32 warps: one token of a 32-token chunk per warp
 constexpr int kWarps = kRouteThreads / 32;
 
-// Monotone map of a float to uint32 (larger float -> larger key), -0 folded onto +0.
-__device__ __forceinline__ uint32_t order_key(float f) {
-  uint32_t u = __float_as_uint(f);
-  if (u == 0x80000000u) u = 0u;
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
 // Phase 1 for chunk c: select the top_k experts of its valid tokens.
 template <int EPL>
 __device__ void route_select_chunk(int c, const void* __restrict__ scores, int dtype, int64_t st, int64_t se, int E,
@@ -51,7 +44,7 @@ __device__ void route_select_chunk(int c, const void* __restrict__ scores, int d
       const int e = lane + 32 * i;
       key[i] = 0u;
       if (e < E) {
-        key[i] = order_key(load_score(scores, dtype, (int64_t)t * st + (int64_t)e * se));
+        key[i] = route_order_key(load_score(scores, dtype, (int64_t)t * st + (int64_t)e * se));
         live |= 1u << i;
       }
     }
@@ -110,18 +103,19 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_part, int* tot
   return excl;
 }
 
-// Phase 2 for expert e: exclusive scan of hist_t[e, 0..nblk) in place; counts[e] = total.
-__device__ void route_scan_expert(int e, int32_t* __restrict__ hist_t, int nblk, int32_t* __restrict__ counts,
-                                  int* s_part) {
+// Phase 2 for expert e: exclusive scan of hist_t[e, 0..nchunks) in place (rows of
+// hist_t are nblk long); counts[e] = total.
+__device__ void route_scan_expert(int e, int32_t* __restrict__ hist_t, int nblk, int nchunks,
+                                  int32_t* __restrict__ counts, int* s_part) {
   int32_t* h = hist_t + (int64_t)e * nblk;
-  const int per = (nblk + kRouteThreads - 1) / kRouteThreads;
+  const int per = (nchunks + kRouteThreads - 1) / kRouteThreads;
   const int b0 = threadIdx.x * per;
   int sum = 0;
   // data written by other blocks before a grid barrier is read at L2 (.cg), past any stale L1 line
-  for (int b = b0; b < b0 + per && b < nblk; ++b) sum += __ldcg(h + b);
+  for (int b = b0; b < b0 + per && b < nchunks; ++b) sum += __ldcg(h + b);
   int total;
   int run = block_exclusive_scan(sum, s_part, &total);
-  for (int b = b0; b < b0 + per && b < nblk; ++b) {
+  for (int b = b0; b < b0 + per && b < nchunks; ++b) {
     const int v = __ldcg(h + b);
     h[b] = run;
     run += v;
@@ -164,7 +158,11 @@ __device__ void route_emit_chunk(int c, int E, int k, int Tv, const int32_t* __r
   __syncthreads();
 }
 
-template <int EPL>
+// SELECT: all three phases from the scores.  Otherwise the selection was done by
+// the router GEMM's epilogue (moe_router_route), which left the chosen experts
+// and the chunk histograms in the workspace and zeroed the barrier counter: the
+// launch starts at the scan, with one grid barrier.
+template <int EPL, bool SELECT>
 __global__ void __launch_bounds__(kRouteThreads) route_coop_kernel(
     const void* __restrict__ scores, int dtype, int64_t st, int64_t se, int T, int E, int k,
     const int32_t* __restrict__ num_valid, int32_t* __restrict__ chosen, int32_t* __restrict__ hist_t, int nblk,
@@ -177,20 +175,19 @@ __global__ void __launch_bounds__(kRouteThreads) route_coop_kernel(
   pdl_launch_dependents();  // the gather may launch and wait for this grid
   const int Tv = read_count(num_valid, T, err);
   const int nchunks = (Tv + kTokBlock - 1) / kTokBlock;
-  // chunks past the valid tokens still publish an empty histogram
-  for (int c = blockIdx.x; c < nblk; c += gridDim.x) {
-    if (c < nchunks) {
+  unsigned int arrivals = 0;
+  if constexpr (SELECT) {
+    for (int c = blockIdx.x; c < nchunks; c += gridDim.x)
       route_select_chunk<EPL>(c, scores, dtype, st, se, E, k, Tv, chosen, hist_t, nblk, s_a);
-    } else {
-      for (int e = threadIdx.x; e < E; e += kRouteThreads) hist_t[(int64_t)e * nblk + c] = 0;
+    arrivals += gridDim.x;
+    if (!grid_barrier(barrier, arrivals)) {
+      if (threadIdx.x == 0) flag_error(err, MOE_DEVERR_TIMEOUT);
+      return;
     }
   }
-  if (!grid_barrier(barrier, gridDim.x)) {
-    if (threadIdx.x == 0) flag_error(err, MOE_DEVERR_TIMEOUT);
-    return;
-  }
-  for (int e = blockIdx.x; e < E; e += gridDim.x) route_scan_expert(e, hist_t, nblk, counts, s_part);
-  if (!grid_barrier(barrier, 2u * gridDim.x)) {
+  for (int e = blockIdx.x; e < E; e += gridDim.x) route_scan_expert(e, hist_t, nblk, nchunks, counts, s_part);
+  arrivals += gridDim.x;
+  if (!grid_barrier(barrier, arrivals)) {
     if (threadIdx.x == 0) flag_error(err, MOE_DEVERR_TIMEOUT);
     return;
   }
@@ -249,7 +246,7 @@ __global__ void __launch_bounds__(kSmallThreads) route_small_kernel(
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < Tv * E; i += kSmallThreads) {
     const int t = i / E, e = i - t * E;
-    s_key[i] = order_key(load_score(scores, dtype, (int64_t)t * st + (int64_t)e * se));
+    s_key[i] = route_order_key(load_score(scores, dtype, (int64_t)t * st + (int64_t)e * se));
   }
   for (int i = tid; i < kSmallWarps * E; i += kSmallThreads) s_hist[i] = 0;
   __syncthreads();
@@ -355,13 +352,15 @@ cudaError_t launch_small(const RouteArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <int EPL>
+// SELECT: zero the barrier counter first (the fused path's router did it already).
+template <int EPL, bool SELECT>
 cudaError_t launch_coop(const RouteArgs& a, int32_t* chosen, int32_t* hist_t, int nblk, unsigned int* barrier,
                         cudaStream_t s) {
-  auto kern = route_coop_kernel<EPL>;
+  auto kern = route_coop_kernel<EPL, SELECT>;
   const int cap = device_sm_count() * resident_blocks_per_sm(reinterpret_cast<const void*>(kern), kRouteThreads);
-  const int grid = nblk < cap ? nblk : cap;
-  cudaError_t e = cudaMemsetAsync(barrier, 0, sizeof(unsigned int), s);
+  const int want = nblk > a.E ? nblk : a.E;   // chunks to select and emit, experts to scan
+  const int grid = want < cap ? want : cap;
+  cudaError_t e = SELECT ? cudaMemsetAsync(barrier, 0, sizeof(unsigned int), s) : cudaSuccess;
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -380,6 +379,25 @@ cudaError_t launch_coop(const RouteArgs& a, int32_t* chosen, int32_t* hist_t, in
 }
 
 }  // namespace
+
+cudaError_t preload_route_kernels() {
+  const void* kernels[] = {
+      reinterpret_cast<const void*>(route_small_kernel<1>), reinterpret_cast<const void*>(route_small_kernel<2>),
+      reinterpret_cast<const void*>(route_small_kernel<4>), reinterpret_cast<const void*>(route_small_kernel<8>),
+      reinterpret_cast<const void*>(route_coop_kernel<1, true>),
+      reinterpret_cast<const void*>(route_coop_kernel<2, true>),
+      reinterpret_cast<const void*>(route_coop_kernel<4, true>),
+      reinterpret_cast<const void*>(route_coop_kernel<8, true>),
+      reinterpret_cast<const void*>(route_coop_kernel<16, true>),
+      reinterpret_cast<const void*>(route_coop_kernel<32, true>),
+      reinterpret_cast<const void*>(route_coop_kernel<1, false>)};
+  for (const void* k : kernels) {
+    cudaFuncAttributes attr;
+    cudaError_t e = cudaFuncGetAttributes(&attr, k);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
 
 // Workspace: [barrier counter | pad to 256] [chosen experts T*k] [histogram E x chunks]
 size_t route_workspace_bytes(int T, int E, int top_k) {
@@ -403,17 +421,29 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
     if (epl <= 4) return launch_small<4>(a, s);
     return launch_small<8>(a, s);
   }
-  char* ws = static_cast<char*>(a.ws);
-  unsigned int* barrier = reinterpret_cast<unsigned int*>(ws);
-  int32_t* chosen = reinterpret_cast<int32_t*>(ws + 256);
-  int32_t* hist_t = reinterpret_cast<int32_t*>(ws + 256 + ((size_t)a.T * a.top_k * 4 + 255) / 256 * 256);
+  RouteWorkspace w = route_workspace(a.ws, a.T, a.top_k);
   const int epl = (a.E + 31) / 32;
-  if (epl <= 1) return launch_coop<1>(a, chosen, hist_t, nblk, barrier, s);
-  if (epl <= 2) return launch_coop<2>(a, chosen, hist_t, nblk, barrier, s);
-  if (epl <= 4) return launch_coop<4>(a, chosen, hist_t, nblk, barrier, s);
-  if (epl <= 8) return launch_coop<8>(a, chosen, hist_t, nblk, barrier, s);
-  if (epl <= 16) return launch_coop<16>(a, chosen, hist_t, nblk, barrier, s);
-  return launch_coop<32>(a, chosen, hist_t, nblk, barrier, s);
+  if (epl <= 1) return launch_coop<1, true>(a, w.chosen, w.hist_t, nblk, w.barrier, s);
+  if (epl <= 2) return launch_coop<2, true>(a, w.chosen, w.hist_t, nblk, w.barrier, s);
+  if (epl <= 4) return launch_coop<4, true>(a, w.chosen, w.hist_t, nblk, w.barrier, s);
+  if (epl <= 8) return launch_coop<8, true>(a, w.chosen, w.hist_t, nblk, w.barrier, s);
+  if (epl <= 16) return launch_coop<16, true>(a, w.chosen, w.hist_t, nblk, w.barrier, s);
+  return launch_coop<32, true>(a, w.chosen, w.hist_t, nblk, w.barrier, s);
+}
+
+cudaError_t launch_route_emit(const RouteArgs& a, cudaStream_t s) {
+  const int nblk = (a.T + kTokBlock - 1) / kTokBlock;
+  RouteWorkspace w = route_workspace(a.ws, a.T, a.top_k);
+  return launch_coop<1, false>(a, w.chosen, w.hist_t, nblk, w.barrier, s);
+}
+
+RouteWorkspace route_workspace(void* ws, int T, int top_k) {
+  char* b = static_cast<char*>(ws);
+  RouteWorkspace w;
+  w.barrier = reinterpret_cast<unsigned int*>(b);
+  w.chosen = reinterpret_cast<int32_t*>(b + 256);
+  w.hist_t = reinterpret_cast<int32_t*>(b + 256 + ((size_t)T * top_k * 4 + 255) / 256 * 256);
+  return w;
 }
 
 }  // namespace moe

@@ -531,6 +531,35 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(const float4* _
   }
 }
 
+// The number of valid routed rows: *valid_p (clamped to a), or, when sum_counts is
+// given, the sum of the E per-expert counts (the padded-token layout, whose valid
+// rows are every expert's rows).  Called by every thread of the block.
+__device__ int valid_rows(const int32_t* valid_p, const int32_t* sum_counts, int E, int a, unsigned int* err) {
+  if (!sum_counts) return read_count(valid_p, a, err);
+  __shared__ int s_rows;
+  if (threadIdx.x < 32) {
+    int v = 0;
+    bool bad = false;
+    for (int e = threadIdx.x; e < E; e += 32) {
+      const int c = __ldg(sum_counts + e);
+      bad |= c < 0;
+      v += c > 0 ? c : 0;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    bad = __any_sync(0xffffffffu, bad);
+    if (threadIdx.x == 0) {
+      if (bad || v > a) {
+        if (blockIdx.x == 0) flag_error(err, MOE_DEVERR_BAD_COUNT);
+        if (v > a) v = a;
+      }
+      s_rows = v;
+    }
+  }
+  __syncthreads();
+  return s_rows;
+}
+
 // ---------------------------------------------------------------- silu_mul
 
 __global__ void __launch_bounds__(kThreads) silu_mul_kernel(const __nv_bfloat16* __restrict__ x0,
@@ -568,19 +597,23 @@ __global__ void __launch_bounds__(kThreads) silu_mul_kernel(const __nv_bfloat16*
 }
 
 // Row groups as in the quantising gather; the fp32 row of z is held in
-// registers and the next row's two packed halves are prefetched.
-template <int G, int VPT>
+// registers and the next row's packed input is prefetched.  SILU: z =
+// silu_mul(x0, x1) (silu_mul_quant); otherwise z = x0, a bf16 row (the row pass
+// of the grouped GEMM's SILU_MUL_QUANT epilogue; x1 unused).  The valid row
+// count is *valid_p, or the sum of the E counts when sum_counts is given.
+template <int G, int VPT, bool SILU>
 __global__ void __launch_bounds__(kThreads) silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ x0,
                                                                   const __nv_bfloat16* __restrict__ x1, int64_t ld,
                                                                   int a, int H8, const int32_t* __restrict__ valid_p,
+                                                                  const int32_t* __restrict__ sum_counts, int E,
                                                                   const float* __restrict__ ub, uint2* __restrict__ z,
                                                                   float* __restrict__ z_scale, unsigned int* err) {
   constexpr int kGroupThreads = 32 * G, kGroups = kThreads / kGroupThreads;
   __shared__ float s_red[kWarps];
-  const int valid = read_count(valid_p, a, err);
+  const int valid = valid_rows(valid_p, sum_counts, E, a, err);
   const int group = threadIdx.x / kGroupThreads, gt = threadIdx.x % kGroupThreads;
   const int stride = gridDim.x * kGroups;
-  uint4 r0[VPT], r1[VPT];
+  uint4 r0[VPT], r1[SILU ? VPT : 1];
   auto fetch = [&](int row) {
     const uint4* p0 = reinterpret_cast<const uint4*>(x0 + (int64_t)row * ld);
     const uint4* p1 = reinterpret_cast<const uint4*>(x1 + (int64_t)row * ld);
@@ -589,7 +622,7 @@ __global__ void __launch_bounds__(kThreads) silu_mul_quant_kernel(const __nv_bfl
       const int c = gt + kGroupThreads * i;
       if (c < H8) {
         r0[i] = __ldg(p0 + c);
-        r1[i] = __ldg(p1 + c);
+        if constexpr (SILU) r1[i] = __ldg(p1 + c);
       }
     }
   };
@@ -602,14 +635,15 @@ __global__ void __launch_bounds__(kThreads) silu_mul_quant_kernel(const __nv_bfl
     for (int i = 0; i < VPT; ++i) {
       const int c = gt + kGroupThreads * i;
       if (c < H8) {
-        float g[8];
         bf16x8_to_f32(r0[i], f[i]);
-        bf16x8_to_f32(r1[i], g);
+        if constexpr (SILU) {
+          float g[8];
+          bf16x8_to_f32(r1[i], g);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          f[i][q] = silu_mul_f32(f[i][q], g[q]);
-          m = fmaxf(m, fabsf(f[i][q]));
+          for (int q = 0; q < 8; ++q) f[i][q] = silu_mul_f32(f[i][q], g[q]);
         }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) m = fmaxf(m, fabsf(f[i][q]));
       }
     }
     if (r + stride < valid) fetch(r + stride);
@@ -632,35 +666,6 @@ __global__ void __launch_bounds__(kThreads) silu_mul_quant_kernel(const __nv_bfl
 }
 
 // ------------------------------------------------------------- scatter-add
-
-// The number of valid routed rows: *valid_p (clamped to a), or, when sum_counts is
-// given, the sum of the E per-expert counts (the padded-token layout, whose valid
-// rows are every expert's rows).  Called by every thread of the block.
-__device__ int valid_rows(const int32_t* valid_p, const int32_t* sum_counts, int E, int a, unsigned int* err) {
-  if (!sum_counts) return read_count(valid_p, a, err);
-  __shared__ int s_rows;
-  if (threadIdx.x < 32) {
-    int v = 0;
-    bool bad = false;
-    for (int e = threadIdx.x; e < E; e += 32) {
-      const int c = __ldg(sum_counts + e);
-      bad |= c < 0;
-      v += c > 0 ? c : 0;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    bad = __any_sync(0xffffffffu, bad);
-    if (threadIdx.x == 0) {
-      if (bad || v > a) {
-        if (blockIdx.x == 0) flag_error(err, MOE_DEVERR_BAD_COUNT);
-        if (v > a) v = a;
-      }
-      s_rows = v;
-    }
-  }
-  __syncthreads();
-  return s_rows;
-}
 
 // top_k == 1 without the inverse permutation: routed row r owns token ti[r].
 // Work items as in the gather: (row, chunk).
@@ -942,14 +947,16 @@ cudaError_t launch_silu_mul(const SiluArgs& g, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-#define MOE_SILU_QUANT(G, VPT)                                                                                  \
-  silu_mul_quant_kernel<G, VPT><<<persistent_grid(silu_mul_quant_kernel<G, VPT>, g.a, kThreads / (32 * G)),   \
-                                  kThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(g.x0),                   \
-                                                          static_cast<const __nv_bfloat16*>(g.x1), g.ld, g.a, H8, \
-                                                          g.valid, g.scale_ub, static_cast<uint2*>(g.z),          \
-                                                          g.z_scale, g.err)
+#define MOE_SILU_QUANT(G, VPT)                                                                              \
+  do {                                                                                                      \
+    auto k = silu_mul_quant_kernel<G, VPT, SILU>;                                                           \
+    k<<<persistent_grid(k, g.a, kThreads / (32 * G)), kThreads, 0, s>>>(                                    \
+        static_cast<const __nv_bfloat16*>(g.x0), static_cast<const __nv_bfloat16*>(g.x1), g.ld, g.a, H8,      \
+        g.valid, g.sum_counts, g.E, g.scale_ub, static_cast<uint2*>(g.z), g.z_scale, g.err);                \
+  } while (0)
 
-cudaError_t launch_silu_mul_quant(const SiluArgs& g, cudaStream_t s) {
+template <bool SILU>
+cudaError_t launch_row_quant(const SiluArgs& g, cudaStream_t s) {
   const int H8 = g.H / 8;
   const int G = pick_group(H8);
   const bool full = H8 > 32 * G * 4;
@@ -962,6 +969,11 @@ cudaError_t launch_silu_mul_quant(const SiluArgs& g, cudaStream_t s) {
   }
   return cudaGetLastError();
 }
+#undef MOE_SILU_QUANT
+
+cudaError_t launch_silu_mul_quant(const SiluArgs& g, cudaStream_t s) { return launch_row_quant<true>(g, s); }
+
+cudaError_t launch_quantize_rows_bf16(const SiluArgs& g, cudaStream_t s) { return launch_row_quant<false>(g, s); }
 
 cudaError_t launch_scatter_add(const ScatterArgs& g, cudaStream_t s) {
   const int D8 = g.D / 8;

@@ -48,12 +48,15 @@ constexpr int kRBKBytes = 128;     // bytes of K per stage: 64 bf16
 constexpr int kRBK = kRBKBytes / 2;
 constexpr int kRThreads = 192;
 constexpr int kMinKb = 8;          // K blocks per split, at least
+constexpr double kFixedKbPerCta = 6.0;  // a CTA's fixed cost (prologue, epilogue, reduction) in K blocks
 constexpr int kMaxSplit = 8;       // portable cluster size
 constexpr int kMaxStages = 8;
 constexpr int kSmemBudget = 200 * 1024;
 constexpr int kRABytes = kRBM * kRBKBytes;  // 16 KB
 
-enum { kEpiSigmoid = 0, kEpiSilu = 1, kEpiPlain = 2 };
+enum { kEpiSigmoid = 0, kEpiSilu = 1, kEpiPlain = 2, kEpiSigmoidTopK = 3 };
+constexpr int kChunkRows = 32;                 // routing chunk: tokens per histogram column
+constexpr int kTileChunks = kRBM / kChunkRows;  // 4 chunks per 128-row tile
 
 struct SplitKParams {
   int rows_hi;     // rows of A (the valid count is clamped to it)
@@ -73,6 +76,12 @@ struct SplitKParams {
   const int32_t* rows_valid;  // nullable: rows_hi
   __nv_bfloat16* out;         // [rows, n_out]
   unsigned int* err;
+  // kEpiSigmoidTopK (the router with the routing selection in its epilogue)
+  int top_k;
+  int32_t* chosen;            // [rows * top_k]: each valid token's experts, in selection order
+  int32_t* hist_t;            // [n_out][nblk]: per 32-token chunk, the tokens that chose each expert
+  int nblk;                   // chunks of rows_hi
+  unsigned int* barrier;      // the routing kernel's grid-barrier counter, zeroed here
 };
 
 struct SplitKSmem {
@@ -125,6 +134,9 @@ __device__ __forceinline__ float sigmoid_of_bf16_logit(float sum) {
 
 __device__ __forceinline__ float round_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
+// Byte offset of the routing chunk histogram in shared memory: past the parked partial tile.
+__host__ __device__ constexpr int topk_hist_offset(int pstride) { return (kRBM * pstride * 4 + 15) / 16 * 16; }
+
 // Store 4 outputs of a row at column c (masked by n_out).
 __device__ __forceinline__ void store4(const SplitKParams& p, __nv_bfloat16* row, int c, float v0, float v1, float v2,
                                        float v3) {
@@ -148,6 +160,71 @@ __device__ __forceinline__ void store4(const SplitKParams& p, __nv_bfloat16* row
   }
 }
 
+// kEpiSigmoidTopK reduction of tile m: chunk q (32 rows) of the tile is reduced
+// by CTA q % S of the cluster.  A warp takes a row: lane l sums columns 4l..4l+3
+// (and 128 + 4l.. when E > 128) of the S partials in rank order, so the scores
+// are those of kEpiSigmoid bit for bit, stores them, and the warp selects the
+// row's top_k experts as moe_route does (the largest bf16 score, the lower expert
+// on equal scores, +0 == -0).  The chunk's expert histogram goes to hist_t[., c];
+// every chunk this launch reduces writes all E entries of its column.
+template <int G>
+__device__ void reduce_sigmoid_topk(const SplitKParams& p, int m, int rank, int S, int Tv, const uint32_t* peer,
+                                    int* s_hist) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.n_out, k = p.top_k;
+  for (int q = rank; q < kTileChunks; q += S) {
+    const int c = m * kTileChunks + q;
+    const int t0 = c * kChunkRows;
+    if (t0 >= Tv) break;  // the same for every thread of the CTA
+    for (int e = threadIdx.x; e < E; e += kRThreads) s_hist[e] = 0;
+    __syncthreads();
+    for (int r = warp; r < kChunkRows; r += kRThreads / 32) {
+      const int t = t0 + r;
+      if (t >= Tv) break;  // warp-uniform
+      const int rr = q * kChunkRows + r;
+      uint32_t key[4 * G];
+      uint32_t live = 0;  // bit 4g + i: expert 128 g + 4 lane + i exists and is not yet chosen
+      __nv_bfloat16* orow = p.out + (int64_t)t * E;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const int c0 = 128 * g + 4 * lane;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c0 < p.n_mma) acc = cluster_sum4(peer, S, (uint32_t)((rr * p.pstride + c0) * 4));
+        const float sv[4] = {sigmoid_of_bf16_logit(acc.x), sigmoid_of_bf16_logit(acc.y),
+                             sigmoid_of_bf16_logit(acc.z), sigmoid_of_bf16_logit(acc.w)};
+        if (c0 < E) store4(p, orow, c0, sv[0], sv[1], sv[2], sv[3]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          key[4 * g + i] = route_order_key(round_bf16(sv[i]));
+          if (c0 + i < E) live |= 1u << (4 * g + i);
+        }
+      }
+      for (int j = 0; j < k; ++j) {
+        uint32_t best = 0u;
+        int best_i = -1;
+#pragma unroll
+        for (int i = 0; i < 4 * G; ++i)  // ascending expert index within the lane
+          if (((live >> i) & 1u) && (best_i < 0 || key[i] > best)) {
+            best = key[i];
+            best_i = i;
+          }
+        const uint32_t wbest = __reduce_max_sync(0xffffffffu, best_i >= 0 ? best : 0u);
+        const uint32_t cand =
+            (best_i >= 0 && best == wbest) ? (uint32_t)(128 * (best_i >> 2) + 4 * lane + (best_i & 3)) : 0xffffffffu;
+        const int we = (int)__reduce_min_sync(0xffffffffu, cand);
+        if (((we & 127) >> 2) == lane) live &= ~(1u << (4 * (we >> 7) + (we & 3)));
+        if (lane == 0) {
+          p.chosen[(int64_t)t * k + j] = we;
+          atomicAdd(&s_hist[we], 1);
+        }
+      }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kRThreads) p.hist_t[(int64_t)e * p.nblk + c] = s_hist[e];
+    __syncthreads();
+  }
+}
+
 __global__ void __launch_bounds__(kRThreads, 1)
     splitk_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                        const SplitKParams p) {
@@ -164,6 +241,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
   const int tile = blockIdx.x / S;
   const int rank = blockIdx.x - tile * S;
   const int m = tile / p.n_tiles, n = tile - (tile / p.n_tiles) * p.n_tiles;
+  // the routing kernel that follows this launch starts its grid barrier from zero
+  if (p.barrier && blockIdx.x == 0 && threadIdx.x == 0) *p.barrier = 0u;
   const int Tv = read_count(p.rows_valid, p.rows_hi, (threadIdx.x == 0 && blockIdx.x == 0) ? p.err : nullptr);
   if (m * kRBM >= Tv) return;
 
@@ -303,7 +382,15 @@ __global__ void __launch_bounds__(kRThreads, 1)
 
   // ---- every CTA's partial is parked: reduce this rank's rows over the cluster
   cluster_sync_all();
-  {
+  if (p.epi == kEpiSigmoidTopK) {
+    uint32_t peer[kMaxSplit];
+#pragma unroll
+    for (int j = 0; j < kMaxSplit; ++j) peer[j] = j < S ? map_to_rank(sbase, (uint32_t)j) : 0u;
+    // the chunk histogram sits past the parked partial tile, which peers are reading
+    int* s_hist = reinterpret_cast<int*>(smem + topk_hist_offset(p.pstride));
+    if (p.n_out > 128) reduce_sigmoid_topk<2>(p, m, rank, S, Tv, peer, s_hist);
+    else reduce_sigmoid_topk<1>(p, m, rank, S, Tv, peer, s_hist);
+  } else {
     const int row0 = (int)((int64_t)rank * kRBM / S), row1 = (int)((int64_t)(rank + 1) * kRBM / S);
     // 4-column groups per row: the router's E columns, 128 z columns, or 256 output columns
     const int cols = p.epi == kEpiSilu ? p.n_mma / 2 : (p.epi == kEpiSigmoid ? p.n_out : p.n_mma);
@@ -391,15 +478,23 @@ SplitKPlan plan_splitk(int rows, int K, int n_mma, int n_tiles) {
   q.m_tiles = (rows + kRBM - 1) / kRBM;
   q.pstride = n_mma + 4;  // 4 floats of padding spread the rows over the banks
   q.smem = SplitKSmem(q.stages, n_mma).bytes + 1024;
-  // splits: the largest cluster size (at most a portable 8, at least kMinKb K blocks per
-  // CTA) at which every tile's cluster is resident at once
+  // splits: the cluster size S (at most a portable 8, at least kMinKb K blocks per CTA)
+  // of the shortest estimated time: waves of resident clusters x (K blocks per CTA +
+  // a fixed cost per CTA for its prologue, epilogue and cluster reduction), the
+  // smaller S on ties.  A second wave of clusters can beat one wave of long CTAs:
+  // 86 tiles on GB300 (152 SMs) run 3-way split in two waves of 50 clusters.
   const int64_t tiles = (int64_t)q.m_tiles * n_tiles;
   q.split = 1;
-  for (int S = kMaxSplit; S > 1; --S) {
-    if (q.num_kb / S < kMinKb) continue;
-    if (tiles <= max_active_clusters(S, q.smem)) {
+  double best = 0.0;
+  for (int S = 1; S <= kMaxSplit; ++S) {
+    if (S > 1 && q.num_kb / S < kMinKb) break;
+    const int64_t clusters = S == 1 ? (int64_t)device_sm_count() : (int64_t)max_active_clusters(S, q.smem);
+    if (clusters < 1) continue;
+    const int64_t waves = (tiles + clusters - 1) / clusters;
+    const double cost = (double)waves * ((double)q.num_kb / S + kFixedKbPerCta);
+    if (S == 1 || cost < best) {
+      best = cost;
       q.split = S;
-      break;
     }
   }
   return q;
@@ -413,8 +508,10 @@ cudaError_t launch_splitk(const CUtensorMap& ma, const CUtensorMap& mb, SplitKPa
   p.split = q.split;
   p.pstride = q.pstride;
   p.n_tiles = n_tiles;
-  // the parked partial tile fits in the operand ring
-  if ((int64_t)kRBM * q.pstride * 4 > SplitKSmem(q.stages, p.n_mma).bars) return cudaErrorInvalidConfiguration;
+  // the parked partial tile (and the routing chunk histogram after it) fits in the operand ring
+  const int64_t parked = p.epi == kEpiSigmoidTopK ? topk_hist_offset(q.pstride) + (int64_t)p.n_out * 4
+                                                 : (int64_t)kRBM * q.pstride * 4;
+  if (parked > SplitKSmem(q.stages, p.n_mma).bars) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(splitk_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, q.smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -456,6 +553,32 @@ cudaError_t launch_router_scores(const RouterArgs& a, cudaStream_t s) {
   p.rows_valid = a.num_valid;
   p.out = static_cast<__nv_bfloat16*>(a.scores);
   p.err = a.err;
+  return launch_splitk(ma, mb, p, q, 1, s);
+}
+
+cudaError_t launch_router_route(const RouterArgs& a, int top_k, const RouteWorkspace& w, cudaStream_t s) {
+  const int n_mma = (a.E + 15) / 16 * 16;
+  const SplitKPlan q = plan_splitk(a.T, a.D, n_mma, 1);
+  CUtensorMap ma, mb;
+  if (!make_map_sw128(&ma, a.x, a.T, a.D, false, kRBM) || !make_map_sw128(&mb, a.w, a.E, a.D, false, n_mma))
+    return cudaErrorInvalidValue;
+  SplitKParams p = {};
+  p.rows_hi = a.T;
+  p.n_mma = n_mma;
+  p.b_box = n_mma;
+  p.b_loads = 1;
+  p.epi = kEpiSigmoidTopK;
+  p.n_out = a.E;
+  p.gate_row0 = 0;
+  p.vec_store = (a.E % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.scores) & 7) == 0);
+  p.rows_valid = a.num_valid;
+  p.out = static_cast<__nv_bfloat16*>(a.scores);
+  p.err = a.err;
+  p.top_k = top_k;
+  p.chosen = w.chosen;
+  p.hist_t = w.hist_t;
+  p.nblk = (a.T + kChunkRows - 1) / kChunkRows;
+  p.barrier = w.barrier;
   return launch_splitk(ma, mb, p, q, 1, s);
 }
 

@@ -8,7 +8,8 @@ Stage order of mslk/moe/layers.py, MetaShufflingMoE._no_comm_forward:
          persistent launch, moe_expert_mlp, when the layer streams its weights:
          T*top_k <= 128*E)
   routed experts, FP8:   route -> gather*score -> e4m3 rows -> grouped GEMM w13
-         (FP8 rowwise) -> silu_mul_quant -> grouped GEMM w2 (FP8 rowwise) -> scatter-add
+         (FP8 rowwise) with the SiLU*mul + quantisation epilogue (bf16 z, then its
+         rows to e4m3) -> grouped GEMM w2 (FP8 rowwise) -> scatter-add
   shared expert (optional): the same MLP over every valid token (one expert,
          unit scores) written into the output first; the routed combine then
          adds into it, as _routed_expert does with shared_output.  Small bf16
@@ -49,7 +50,7 @@ class _Buffers:
     mlp_ws: torch.Tensor
     xr: torch.Tensor              # routed rows: bf16 [T*k, D] or e4m3 [T*k, D]
     xs: torch.Tensor | None       # FP8: row scales [T*k]
-    y: torch.Tensor | None        # FP8: GEMM1 output bf16 [T*k, 2H]
+    y: torch.Tensor | None        # FP8: the w13 epilogue's bf16 z [T*k, H], before its rows are quantised
     z: torch.Tensor               # bf16 [T*k, H] or e4m3 [T*k, H]
     zs: torch.Tensor | None       # FP8: row scales [T*k]
     o: torch.Tensor               # GEMM2 output bf16 [T*k, D]
@@ -84,6 +85,9 @@ class MoELayer:
         self.fp8 = w13.dtype == torch.float8_e4m3fn
         if self.fp8:
             assert w13_scale is not None and w2_scale is not None
+        # FP8 layers quantise z in the w13 GEMM's epilogue, after its bf16 rounding
+        # (MOE_EPILOGUE_SILU_MUL_QUANT): the z_bf16 reading of the CPU oracle
+        self.z_bf16 = self.fp8
         self.w13, self.w2 = w13.contiguous(), w2.contiguous()
         if pack_weights is None:
             pack_weights = self.H % 128 == 0 and self.D % 128 == 0 and w13.is_cuda
@@ -171,7 +175,7 @@ class MoELayer:
         mlp_ws = torch.zeros(mb.moe_expert_mlp_workspace_size(max(E, 1)), dtype=torch.uint8, device=device)
         if self.fp8:
             b = _Buffers(T, route, ws, mlp_ws, torch.empty(a, D, **e4), torch.empty(a, **f32),
-                         torch.empty(a, 2 * H, **bf), torch.empty(a, H, **e4), torch.empty(a, **f32),
+                         torch.empty(a, H, **bf), torch.empty(a, H, **e4), torch.empty(a, **f32),
                          torch.empty(a, D, **bf))
         else:
             b = _Buffers(T, route, ws, mlp_ws, torch.empty(a, D, **bf), None, None, torch.empty(a, H, **bf), None,
@@ -192,7 +196,7 @@ class MoELayer:
                 x["zero"] = torch.zeros(T, **i32)
                 x["unit"] = torch.ones(T, 1, **f32)           # unit scores: the gather's product is exact
                 x["sh_xq"], x["sh_xs"] = torch.empty(T, D, **e4), torch.empty(T, **f32)
-                x["sh_y"] = torch.empty(T, 2 * Hs, **bf)
+                x["sh_y"] = torch.empty(T, Hs, **bf)
                 x["sh_zq"], x["sh_zs"] = torch.empty(T, Hs, **e4), torch.empty(T, **f32)
             else:
                 x["sh_z"] = torch.empty(T, Hs, **bf)
@@ -209,12 +213,15 @@ class MoELayer:
         b = self.buffers(T, x.device)
         ex = b.extra
         st = []
-        if scores is None:
+        routed_by_router = scores is None
+        if routed_by_router:
+            # the router's epilogue selects the experts; one more kernel emits the routing
             if self.router is None:
                 raise ValueError("scores are required for a layer without a router")
             scores = ex["scores"]
-            st.append(("router", lambda: mb.moe_router_scores(x, self.router, num_valid_tokens, out=ex["scores"],
-                                                              workspace=ex["router_ws"]), MAIN))
+            st.append(("router_route", lambda: mb.moe_router_route(
+                x, self.router, self.top_k, num_valid_tokens, scores=ex["scores"],
+                with_weights=self.weighting == "output", out=b.route, workspace=b.ws), MAIN))
         if self.weighting == "output":
             if accumulate:
                 raise ValueError("the top-k finalize writes the output; accumulate is not supported with it")
@@ -222,12 +229,14 @@ class MoELayer:
             if self.shared:
                 sh_out = ex["sh_out"]
                 st += [(n, f, SIDE) for n, f in self._shared_stages(x, num_valid_tokens, sh_out, False)]
-            st += [(n, f, MAIN) for n, f in self._routed_stages(x, scores, num_valid_tokens, out, False, sh_out)]
+            st += [(n, f, MAIN) for n, f in self._routed_stages(x, scores, num_valid_tokens, out, False, sh_out,
+                                                                routed=routed_by_router)]
             return st
         if self.shared:
             st += [(n, f, SIDE) for n, f in self._shared_stages(x, num_valid_tokens, out, accumulate)]
             accumulate = True       # the routed rows are added into the shared expert's output
-        st += [(n, f, MAIN) for n, f in self._routed_stages(x, scores, num_valid_tokens, out, accumulate)]
+        st += [(n, f, MAIN) for n, f in self._routed_stages(x, scores, num_valid_tokens, out, accumulate,
+                                                            routed=routed_by_router)]
         return st
 
     def _shared_stages(self, x, num_valid_tokens, out, accumulate):
@@ -255,15 +264,14 @@ class MoELayer:
         return [
             ("shared_quant", lambda: mb.moe_gather_scale_quant(x, ex["ident"], ex["zero"], ex["unit"], self.scale_ub,
                                                                rows, out=ex["sh_xq"], out_scale=ex["sh_xs"])),
-            ("shared_w13", lambda: mb.moe_grouped_gemm_fp8_rowwise(ex["sh_xq"], self.sw13, rows, ex["sh_xs"],
-                                                                   self.sw13_scale, out=ex["sh_y"])),
-            ("shared_silu_quant", lambda: mb.moe_silu_mul_quant(ex["sh_y"], self.Hs, self.scale_ub, rows,
-                                                                out=ex["sh_zq"], out_scale=ex["sh_zs"])),
+            ("shared_w13_silu_quant", lambda: mb.moe_grouped_gemm_fp8_rowwise(
+                ex["sh_xq"], self.sw13, rows, ex["sh_xs"], self.sw13_scale, epilogue=mb.MOE_EPILOGUE_SILU_MUL_QUANT,
+                out=ex["sh_y"], scale_ub=self.scale_ub, z_out=ex["sh_zq"], z_scale=ex["sh_zs"])),
             ("shared_w2", lambda: mb.moe_grouped_gemm_fp8_rowwise(ex["sh_zq"], self.sw2, rows, ex["sh_zs"],
                                                                   self.sw2_scale, out=out, **add)),
         ]
 
-    def _routed_stages(self, x, scores, num_valid_tokens, out, accumulate, shared_out=None):
+    def _routed_stages(self, x, scores, num_valid_tokens, out, accumulate, shared_out=None, routed=False):
         T = x.shape[0]
         b = self.buffers(T, x.device)
         r = b.route
@@ -277,8 +285,9 @@ class MoELayer:
         pairs = mb.MOE_GEMM_CTA_PAIRS if self.use_cta_pairs(T) else 0
         # the w2 GEMM writes either the routed rows o, or (top_k = 1) the tokens' rows of out
         w2_out = dict(out=out, scatter_indices=ti, accumulate=accumulate) if fuse_combine else dict(out=b.o)
-        st = [("route", lambda: mb.moe_route(scores, k, num_valid_tokens, with_weights=out_w, out=r,
-                                             workspace=b.ws))]
+        # routed: the router stage has routed the tokens already (moe_router_route)
+        st = [] if routed else [("route", lambda: mb.moe_route(scores, k, num_valid_tokens, with_weights=out_w,
+                                                                out=r, workspace=b.ws))]
         gscores = None if out_w else scores    # output weighting: the gathers copy the rows
         if not self.fp8:
             st.append(("gather", lambda: mb.moe_gather_scale(x, ti, ei, gscores, valid, inv_rows=inv, top_k=k,
@@ -298,10 +307,9 @@ class MoELayer:
                 ("gather_quant", lambda: mb.moe_gather_scale_quant(x, ti, ei, gscores, self.scale_ub, valid,
                                                                    inv_rows=inv, top_k=k, out=b.xr,
                                                                    out_scale=b.xs)),
-                ("gemm_w13", lambda: mb.moe_grouped_gemm_fp8_rowwise(b.xr, self.w13, counts, b.xs, self.w13_scale,
-                                                                     epilogue=pairs, out=b.y)),
-                ("silu_quant", lambda: mb.moe_silu_mul_quant(b.y, self.H, self.scale_ub, valid, out=b.z,
-                                                             out_scale=b.zs)),
+                ("gemm_w13_silu_quant", lambda: mb.moe_grouped_gemm_fp8_rowwise(
+                    b.xr, self.w13, counts, b.xs, self.w13_scale, epilogue=mb.MOE_EPILOGUE_SILU_MUL_QUANT | pairs,
+                    out=b.y, scale_ub=self.scale_ub, z_out=b.z, z_scale=b.zs)),
                 ("gemm_w2", lambda: mb.moe_grouped_gemm_fp8_rowwise(b.z, self.w2, counts, b.zs, self.w2_scale,
                                                                     epilogue=pairs, **w2_out)),
             ]
@@ -450,9 +458,10 @@ class MoELayer:
     def kernel_launches(self, T: int | None = None, with_router: bool = False) -> int:
         """Kernels one forward launches: the router (if used), routing (one
         kernel: single-block or cooperative), gather, the GEMMs (1 fused, or 2),
-        silu_mul_quant (FP8), scatter, and the shared expert's."""
+        the row pass of the FP8 w13 GEMM's quantising epilogue, scatter, and the
+        shared expert's."""
         T = self._bufs.T if T is None and self._bufs is not None else (T or 0)
-        route = 1
+        route = 1                 # with the router: its emit kernel
         scatter = 0 if (self.top_k == 1 and self.weighting == "input") else 1   # scatter or finalize
         n = (route + 4 + scatter) if self.fp8 else (route + 1 + (1 if self.use_fused_mlp(T) else 2) + scatter)
         if with_router:

@@ -67,14 +67,28 @@ def test_host_side_validation_without_gpu(lib):
     # silu: misaligned row stride
     assert L.moe_silu_mul(fake, fake, 36, 4, 32, None, fake, None) == lib.MOE_ERR_UNSUPPORTED
     # grouped GEMM: N not a multiple of 16, unknown epilogue, too many experts
-    assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 24, 64, fake, 0, None, 0, 0, None) == lib.MOE_ERR_UNSUPPORTED
-    assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 32, 64, fake, 9, None, 0, 0, None) == lib.MOE_ERR_INVALID
-    assert L.moe_grouped_gemm(fake, fake, fake, 2048, 64, 32, 64, fake, 0, None, 0, 0, None) \
+    nq = (None, None, None)    # scale_ub, z_out, z_scale (the SILU_MUL_QUANT epilogue only)
+    assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 24, 64, fake, 0, None, 0, 0, *nq, None) \
         == lib.MOE_ERR_UNSUPPORTED
-    assert L.moe_grouped_gemm_fp8_rowwise(fake, fake, fake, None, fake, 4, 64, 32, 64, fake, 0, None, 0, 0, None) \
-        == lib.MOE_ERR_INVALID
+    assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 32, 64, fake, 9, None, 0, 0, *nq, None) == lib.MOE_ERR_INVALID
+    assert L.moe_grouped_gemm(fake, fake, fake, 2048, 64, 32, 64, fake, 0, None, 0, 0, *nq, None) \
+        == lib.MOE_ERR_UNSUPPORTED
+    assert L.moe_grouped_gemm_fp8_rowwise(fake, fake, fake, None, fake, 4, 64, 32, 64, fake, 0, None, 0, 0, *nq,
+                                          None) == lib.MOE_ERR_INVALID
     # the fused combine only goes with the plain epilogue
-    assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 32, 64, fake, 1, fake, 8, 1, None) == lib.MOE_ERR_INVALID
+    assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 32, 64, fake, 1, fake, 8, 1, *nq, None) == lib.MOE_ERR_INVALID
+    # SILU_MUL_QUANT needs z_out and z_scale, a 16-byte aligned z_out and H <= 16384
+    q = lib.MOE_EPILOGUE_SILU_MUL_QUANT
+    assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 64, 64, fake, q, None, 0, 0, None, None, fake, None) \
+        == lib.MOE_ERR_INVALID
+    assert L.moe_grouped_gemm_fp8_rowwise(fake, fake, fake, fake, fake, 4, 64, 64, 64, fake, q, None, 0, 0, None,
+                                          fake, None, None) == lib.MOE_ERR_INVALID
+    assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 64, 64, fake, q, None, 0, 0, None, ctypes.c_void_p(0x1008),
+                              fake, None) == lib.MOE_ERR_UNSUPPORTED
+    assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 2 * 16400, 64, fake, q, None, 0, 0, None, fake, fake, None) \
+        == lib.MOE_ERR_UNSUPPORTED
+    assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 64, 64, fake, q, fake, 8, 1, None, fake, fake, None) \
+        == lib.MOE_ERR_INVALID
     n = ctypes.c_size_t(0)
     assert L.moe_expert_mlp_workspace_size(0, ctypes.byref(n)) == lib.MOE_ERR_INVALID
     assert L.moe_expert_mlp(fake, fake, fake, fake, 4, 64, 32, 32, fake, fake, None, 0, 0, fake, 0, 0, None) \
@@ -85,9 +99,9 @@ def test_host_side_validation_without_gpu(lib):
     assert L.moe_expert_mlp(fake, fake, fake, fake, 4, 64, 128, 96, fake, fake, None, 0, 0, fake, 1 << 20,
                             lib.MOE_WEIGHTS_PACKED, None) == lib.MOE_ERR_UNSUPPORTED
     # packed weights: N (and its halves with SiLU*mul) a multiple of 128
-    assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 96, 64, fake, lib.MOE_WEIGHTS_PACKED, None, 0, 0, None) \
-        == lib.MOE_ERR_UNSUPPORTED
-    assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 128, 64, fake, lib.MOE_WEIGHTS_PACKED | 1, None, 0, 0,
+    assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 96, 64, fake, lib.MOE_WEIGHTS_PACKED, None, 0, 0, *nq,
+                              None) == lib.MOE_ERR_UNSUPPORTED
+    assert L.moe_grouped_gemm(fake, fake, fake, 4, 64, 128, 64, fake, lib.MOE_WEIGHTS_PACKED | 1, None, 0, 0, *nq,
                               None) == lib.MOE_ERR_UNSUPPORTED                    # SiLU halves of 64 rows
     # pack size: bf16 [2, 256, 208] -> 4 row blocks x ceil(416 / 128) = 4 column blocks of 16 KB
     assert L.moe_pack_weights_size(2, 256, 208, lib.MOE_DTYPE_BF16, ctypes.byref(n)) == lib.MOE_OK

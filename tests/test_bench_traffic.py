@@ -8,8 +8,8 @@ import bench
 from moe_token_routing_index_gb300 import workloads
 
 CSRC = bench.ROOT / "moe_token_routing_index_gb300" / "csrc"
-STAGES = {"route", "gather", "gather_quant", "expert_mlp", "gemm_w13", "gemm_w13_silu", "silu_quant", "gemm_w2",
-          "scatter", "finalize", "router"}
+STAGES = {"route", "gather", "gather_quant", "expert_mlp", "gemm_w13_silu_quant", "gemm_w13_silu", "gemm_w2",
+          "scatter", "finalize", "router_route"}
 
 
 def test_traffic_entries_name_existing_sources_and_stages():

@@ -64,7 +64,8 @@ def test_all_tokens_on_one_expert(name):
         wf = lambda ids: (w13[ids].float().cpu().numpy(), w2[ids].float().cpu().numpy())
     else:
         wf = lambda ids: (bits(w13[ids]), bits(w2[ids]))
-    ref, _ = oracle.moe_forward_tokens(sample, bits(x), bits(s), k, wf, fp8=cfg.fp8, scale_ub=cfg.scale_ub)
+    ref, _ = oracle.moe_forward_tokens(sample, bits(x), bits(s), k, wf, fp8=cfg.fp8, z_bf16=cfg.fp8,
+                                       scale_ub=cfg.scale_ub)
     got, exp = f64(bits(out[torch.from_numpy(sample).cuda()])), f64(ref)
     tol = 6e-2 if cfg.fp8 else 2e-2
     a = np.abs(exp)

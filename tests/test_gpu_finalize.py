@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from moe_token_routing_index_gb300 import workloads
-from tests.helpers import bits, f64, is_sentinel, rms, sentinel_like
+from tests.helpers import assert_forward_close, bits, f64, is_sentinel, rms, sentinel_like
 
 pytestmark = pytest.mark.gpu
 
@@ -126,11 +126,6 @@ def _host_weights(cfg, w13, w2):
     return lambda ids: (bits(w13[ids]), bits(w2[ids]))
 
 
-def _bf16_step(v):
-    a = np.abs(v)
-    return np.exp2(np.floor(np.log2(np.where(a > 0, a, 1e-38))) - 7)
-
-
 @pytest.mark.parametrize("name,with_shared", [("tiny", False), ("tiny", True), ("fine_grained", True),
                                               ("padded_fp8", True), ("decode", False)])
 def test_output_weighted_layer(name, with_shared):
@@ -155,15 +150,14 @@ def test_output_weighted_layer(name, with_shared):
     base = None
     if sh is not None:
         conv = (lambda t: t.float().cpu().numpy()) if cfg.fp8 else bits
-        base = oracle.shared_expert(xs, conv(sh[0]), conv(sh[1]), fp8=cfg.fp8, scale_ub=cfg.scale_ub)
+        base = oracle.shared_expert(xs, conv(sh[0]), conv(sh[1]), fp8=cfg.fp8, z_bf16=cfg.fp8,
+                                    scale_ub=cfg.scale_ub)
     ref = oracle.moe_forward_output_weighted(xs, ss, cfg.top_k, _host_weights(cfg, w13, w2), fp8=cfg.fp8,
-                                             shared_out=base, scale_ub=cfg.scale_ub)["out"]
+                                             z_bf16=cfg.fp8, shared_out=base, scale_ub=cfg.scale_ub)["out"]
     got = f64(bits(out[torch.from_numpy(sample).cuda()]))
     exp = f64(ref)
     tol = 6e-2 if cfg.fp8 else 2e-2
-    err = np.abs(got - exp)
-    assert np.all(err <= tol * rms(exp) + _bf16_step(exp)), err.max() / rms(exp)
-    assert (err <= tol * rms(exp)).mean() >= 0.999
+    assert_forward_close(got, exp, tol, f"output-weighted forward {name} (shared {with_shared})")
     if Tv < cfg.T:
         assert is_sentinel(out[Tv:])
 
@@ -192,14 +186,12 @@ def test_output_weighted_layer_with_router(name):
     sample = np.arange(Tv) if Tv <= 64 else np.unique(np.concatenate([[0, Tv - 1], rng.integers(0, Tv, 10)]))
     xs, ss = np.ascontiguousarray(bits(x)[sample]), np.ascontiguousarray(scores[sample])
     conv = (lambda t: t.float().cpu().numpy()) if cfg.fp8 else bits
-    base = oracle.shared_expert(xs, conv(sh[0]), conv(sh[1]), fp8=cfg.fp8, scale_ub=cfg.scale_ub)
+    base = oracle.shared_expert(xs, conv(sh[0]), conv(sh[1]), fp8=cfg.fp8, z_bf16=cfg.fp8, scale_ub=cfg.scale_ub)
     ref = oracle.moe_forward_output_weighted(xs, ss, cfg.top_k, _host_weights(cfg, w13, w2), fp8=cfg.fp8,
-                                             shared_out=base, scale_ub=cfg.scale_ub)["out"]
+                                             z_bf16=cfg.fp8, shared_out=base, scale_ub=cfg.scale_ub)["out"]
     got = f64(bits(out[torch.from_numpy(sample).cuda()]))
     exp = f64(ref)
     tol = 6e-2 if cfg.fp8 else 2e-2
-    err = np.abs(got - exp)
-    assert np.all(err <= tol * rms(exp) + _bf16_step(exp)), err.max() / rms(exp)
-    assert (err <= tol * rms(exp)).mean() >= 0.999
+    assert_forward_close(got, exp, tol, f"output-weighted layer {name}")
     if Tv < cfg.T:
         assert is_sentinel(out[Tv:])

@@ -176,6 +176,128 @@ def test_grouped_gemm_bf16_workloads_sampled(name):
     _check_close(bits(o[rows]), o_ref, _abs_bound_bf16(bits(z)[rows], w2_u, sub_cnt))
 
 
+def _sample_rows_with_tail(cnt, rng, per_expert=3, tile=128):
+    """First, last, the first row of the last (partial) tile, and a few random rows of
+    every non-empty expert (sorted)."""
+    rows, off = [], 0
+    for c in cnt:
+        if c:
+            rows += [off, off + c - 1, off + (c - 1) // tile * tile] + list(rng.integers(off, off + c, per_expert))
+        off += c
+    return np.unique(np.array(rows, np.int64))
+
+
+def _fp8_bound(xq_rows, xs_rows, wq, ws, sub_cnt):
+    """2^-20 * sum_k |x_k w_k| * xs * ws for the sampled rows (per expert segment)."""
+    dx = oracle.e4m3_decode(xq_rows).astype(np.float64)
+    out = np.zeros((xq_rows.shape[0], wq.shape[1]))
+    off = 0
+    for i, c in enumerate(sub_cnt):
+        dw = oracle.e4m3_decode(wq[i]).astype(np.float64)
+        out[off:off + c] = (np.abs(dx[off:off + c]) @ np.abs(dw).T) * xs_rows[off:off + c, None] * ws[i][None, :]
+        off += c
+    return 2.0 ** -20 * out
+
+
+@pytest.mark.parametrize("variant", ["single", "pairs", "packed"])
+@pytest.mark.parametrize("name", ["prefill_fp8", "padded_fp8"])
+def test_grouped_gemm_fp8_workloads_sampled(name, variant):
+    """Full-size FP8-rowwise w13 and w2 GEMMs of the FP8 workloads, with the workload's
+    weights quantised per row on the device: every non-empty expert's first, last,
+    last-tile and random rows against the oracle (fp32 accumulation bound), for 128-row
+    tiles, CTA-pair tiles and packed weights; the SILU_MUL_QUANT epilogue on the full
+    problem equal to silu_mul of the plain output and to the oracle's row rule on its
+    bf16 z (codes and scales bit for bit)."""
+    mb = _mb()
+    cfg = workloads.CONFIGS[name]
+    r = oracle.route(bits(workloads.make_scores(cfg)), cfg.top_k, cfg.valid_tokens)
+    cnt = r["counts"][:cfg.E]
+    a = int(cnt.sum())
+    cd = torch.from_numpy(cnt.copy()).cuda()
+    w13f, w2f = workloads.make_weights(cfg, device="cuda")
+    w13q, w13s = mb.moe_quantize_rows(w13f)
+    w2q, w2s = mb.moe_quantize_rows(w2f)
+    del w13f, w2f
+    g = torch.Generator().manual_seed(17)
+    # codes across the range (clamped: PyTorch's e4m3fn cast turns values past 448 into NaN)
+    xq = (torch.randn(a, cfg.D, generator=g) * 60).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).cuda()
+    xs = (torch.rand(a, generator=g) * 0.02 + 0.001).cuda()
+    flags = mb.MOE_GEMM_CTA_PAIRS if variant == "pairs" else 0
+    a13 = mb.moe_pack_weights(w13q) if variant == "packed" else w13q
+    a2 = mb.moe_pack_weights(w2q) if variant == "packed" else w2q
+    ub = torch.tensor([cfg.scale_ub or 1200.0], dtype=torch.float32, device="cuda")
+    y = mb.moe_grouped_gemm_fp8_rowwise(xq, a13, cd, xs, w13s, epilogue=flags)
+    zb = torch.empty(a, cfg.H, dtype=torch.bfloat16, device="cuda")
+    zq, zs = mb.moe_grouped_gemm_fp8_rowwise(xq, a13, cd, xs, w13s, epilogue=mb.MOE_EPILOGUE_SILU_MUL_QUANT | flags,
+                                             out=zb, scale_ub=ub)
+    o = mb.moe_grouped_gemm_fp8_rowwise(zq, a2, cd, zs, w2s, epilogue=flags)
+    torch.cuda.synchronize()
+    assert mb.device_error() == 0
+    assert torch.equal(zb, mb.moe_silu_mul(y, cfg.H))
+    zq_ref, zs_ref = oracle.quantize_rows(oracle.bf16_to_f32(bits(zb)), float(ub.item()))
+    np.testing.assert_array_equal(bits(zq), zq_ref)
+    np.testing.assert_array_equal(zs.cpu().numpy(), zs_ref)
+    rows = _sample_rows_with_tail(cnt, np.random.default_rng(0))
+    exp_of_row = np.repeat(np.arange(cfg.E), cnt)[rows]
+    used = sorted(set(exp_of_row.tolist()))
+    sub_cnt = np.array([(exp_of_row == e).sum() for e in used], np.int32)
+    xq_h, xs_h = bits(xq)[rows], xs.cpu().numpy()[rows]
+    w13_h, w13s_h = bits(w13q[used]), w13s[used].cpu().numpy()
+    y_ref = oracle.grouped_gemm_fp8(xq_h, w13_h, sub_cnt, xs_h, w13s_h)
+    _check_close(bits(y[rows]), y_ref, _fp8_bound(xq_h, xs_h, w13_h, w13s_h, sub_cnt))
+    zq_h, zs_h = bits(zq)[rows], zs.cpu().numpy()[rows]
+    w2_h, w2s_h = bits(w2q[used]), w2s[used].cpu().numpy()
+    o_ref = oracle.grouped_gemm_fp8(zq_h, w2_h, sub_cnt, zs_h, w2s_h)
+    _check_close(bits(o[rows]), o_ref, _fp8_bound(zq_h, zs_h, w2_h, w2s_h, sub_cnt))
+
+
+SILU_QUANT_SHAPES = [s for s in SHAPES if s[2] % 32 == 0] + [
+    (2, [77, 300], 2 * 8192, 64, 400),       # z rows of 8192 elements (8 warps per row, 4 vectors each)
+    (1, [33], 2 * 16384, 32, None),          # the largest H the row pass takes
+]
+
+
+@pytest.mark.parametrize("pairs", [False, True])
+@pytest.mark.parametrize("ub", [None, 0.75])
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("E,counts,N,K,a_max", SILU_QUANT_SHAPES)
+def test_silu_mul_quant_epilogue(E, counts, N, K, a_max, fp8, ub, pairs):
+    """MOE_EPILOGUE_SILU_MUL_QUANT: y holds the SILU_MUL epilogue's bf16 z bit for bit, and
+    (z_out, z_scale) equal the quantising gather of that z with identity indices and unit
+    scores, and the oracle's row rule on it, bit for bit; rows past the counts untouched.
+    ub = 0.75 makes the bound bind on most rows."""
+    mb = _mb()
+    x, w, cnt, a = _problem(E, counts, N, K, a_max, seed=11 * N + K, std=0.2)
+    cd = torch.from_numpy(cnt).cuda()
+    H = N // 2
+    if fp8:
+        xq, xs = mb.moe_quantize_rows(x.float().cuda())
+        wq, ws = mb.moe_quantize_rows(w.float().cuda())
+        gemm = lambda **kw: mb.moe_grouped_gemm_fp8_rowwise(xq, wq, cd, xs, ws, **kw)
+    else:
+        gemm = lambda **kw: mb.moe_grouped_gemm(x.cuda(), w.cuda(), cd, **kw)
+    flags = mb.MOE_GEMM_CTA_PAIRS if pairs else 0
+    ubt = None if ub is None else torch.tensor([ub], dtype=torch.float32, device="cuda")
+    z_ref = gemm(epilogue=mb.MOE_EPILOGUE_SILU_MUL | flags)
+    rows = x.shape[0]
+    zb = sentinel_like((rows, H), torch.bfloat16)
+    zq = sentinel_like((rows, H), torch.float8_e4m3fn)
+    zs = sentinel_like((rows,), torch.float32)
+    got = gemm(epilogue=mb.MOE_EPILOGUE_SILU_MUL_QUANT | flags, out=zb, scale_ub=ubt, z_out=zq, z_scale=zs)
+    assert got[0] is zq and got[1] is zs
+    torch.cuda.synchronize()
+    assert mb.device_error() == 0
+    assert torch.equal(zb[:a], z_ref[:a])
+    ident = torch.arange(a, dtype=torch.int32, device="cuda")
+    q2, s2 = mb.moe_gather_scale_quant(zb[:a].contiguous(), ident, torch.zeros_like(ident), None, ubt)
+    assert torch.equal(zq[:a].view(torch.uint8), q2.view(torch.uint8))
+    assert torch.equal(zs[:a], s2)
+    q_ref, s_ref = oracle.quantize_rows(oracle.bf16_to_f32(bits(zb[:a])), ub)
+    np.testing.assert_array_equal(bits(zq[:a]), q_ref)
+    np.testing.assert_array_equal(zs[:a].cpu().numpy(), s_ref)
+    assert is_sentinel(zb[a:]) and is_sentinel(zq[a:]) and is_sentinel(zs[a:])
+
+
 @pytest.mark.parametrize("E,counts,D,H,a_max", [(1, [128], 64, 128, None), (3, [5, 0, 130], 256, 512, None),
                                                 (5, [300, 17, 0, 64, 250], 272, 528, 700),
                                                 (16, [8] * 12 + [0] * 4, 512, 1024, 130)])

@@ -16,23 +16,13 @@ import torch
 
 import oracle
 from moe_token_routing_index_gb300 import workloads
-from tests.helpers import bits, f64, is_sentinel, rms, sentinel_like
+from tests.helpers import assert_forward_close, bits, f64, is_sentinel, rms, sentinel_like
 
 pytestmark = pytest.mark.gpu
 
 
-def _bf16_step(v):
-    a = np.abs(v)
-    return np.exp2(np.floor(np.log2(np.where(a > 0, a, 1e-38))) - 7)
-
-
-def _assert_close(got, exp, tol):
-    err = np.abs(got - exp)
-    bound = tol * rms(exp)
-    strict_ok = (err <= bound).mean()
-    msg = f"max|err| {err.max():.3e} = {err.max() / rms(exp):.4f} rms; strict bound met on {strict_ok:.5f}"
-    assert np.all(err <= bound + _bf16_step(exp)), msg
-    assert strict_ok >= 0.999, msg
+def _assert_close(got, exp, tol, label=""):
+    assert_forward_close(got, exp, tol, label)
 
 
 def _host_weights(cfg, w13, w2):
@@ -84,10 +74,12 @@ def test_layer_tiny_full(with_router, with_shared):
     scores = bits(layer.buffers(cfg.T, "cuda").extra["scores"]) if with_router else bits(given)
     base = None
     if with_shared:
-        base = oracle.shared_expert(bits(x), *_host_shared(cfg, sh), fp8=cfg.fp8, scale_ub=cfg.scale_ub)
-    ref = oracle.moe_forward(bits(x), scores, cfg.top_k, _host_weights(cfg, w13, w2), fp8=cfg.fp8, out_init=base,
-                             scale_ub=cfg.scale_ub)
-    _assert_close(f64(bits(out)), f64(ref["out"]), _tol(cfg))
+        base = oracle.shared_expert(bits(x), *_host_shared(cfg, sh), fp8=cfg.fp8, z_bf16=cfg.fp8,
+                                    scale_ub=cfg.scale_ub)
+    ref = oracle.moe_forward(bits(x), scores, cfg.top_k, _host_weights(cfg, w13, w2), fp8=cfg.fp8, z_bf16=cfg.fp8,
+                             out_init=base, scale_ub=cfg.scale_ub)
+    _assert_close(f64(bits(out)), f64(ref["out"]), _tol(cfg),
+                  f"layer tiny (router {with_router}, shared {with_shared})")
 
 
 @pytest.mark.parametrize("name", ["decode", "prefill_fp8", "fine_grained", "padded_fp8"])
@@ -98,17 +90,18 @@ def test_layer_workloads_sampled(name):
     Tv = cfg.valid_tokens
     scores = bits(layer.buffers(cfg.T, "cuda").extra["scores"])
     rng = np.random.default_rng(2)
-    sample = np.unique(np.concatenate([[0, Tv - 1], rng.integers(0, Tv, 10)]))
+    sample = np.unique(np.concatenate([[0, Tv - 1], rng.integers(0, Tv, 30)]))
     xb = bits(x)
     base = oracle.shared_expert(np.ascontiguousarray(xb[sample]), *_host_shared(cfg, sh), fp8=cfg.fp8,
-                                scale_ub=cfg.scale_ub)
+                                z_bf16=cfg.fp8, scale_ub=cfg.scale_ub)
     ref, _ = oracle.moe_forward_tokens(sample, xb, scores, cfg.top_k, _host_weights(cfg, w13, w2), fp8=cfg.fp8,
-                                       out_init=None, scale_ub=cfg.scale_ub)
+                                       z_bf16=cfg.fp8, out_init=None, scale_ub=cfg.scale_ub)
     # the routed rows of the sample, added into the shared rows (fp32 sum, one rounding per element)
     res = oracle.moe_forward(np.ascontiguousarray(xb[sample]), np.ascontiguousarray(scores[sample]), cfg.top_k,
-                             _host_weights(cfg, w13, w2), fp8=cfg.fp8, out_init=base, scale_ub=cfg.scale_ub)
+                             _host_weights(cfg, w13, w2), fp8=cfg.fp8, z_bf16=cfg.fp8, out_init=base,
+                             scale_ub=cfg.scale_ub)
     got = f64(bits(out[torch.from_numpy(sample).cuda()]))
-    _assert_close(got, f64(res["out"]), _tol(cfg))
+    _assert_close(got, f64(res["out"]), _tol(cfg), f"layer {name} ({len(sample)} sampled tokens)")
     # the shared part alone is what the routed part was added to
     assert rms(f64(res["out"]) - f64(ref)) > 0
     if Tv < cfg.T:

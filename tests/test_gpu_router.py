@@ -104,3 +104,73 @@ def test_router_scores_deterministic_and_count_clamped():
     o3 = mb.moe_router_scores(x, w, nv)
     assert mb.device_error() & mb.MOE_DEVERR_BAD_COUNT
     assert torch.equal(o1, o3)
+
+
+ROUTE_KEYS = ("counts", "expert_offsets", "expert_indices", "token_indices", "inv_rows", "topk_weights")
+
+
+def _router_route_case(x, w, top_k, Tv):
+    """moe_router_route against moe_router_scores followed by moe_route, bit for bit, and
+    against the oracle's routing of the GPU's scores; nothing written past Tv."""
+    mb = _mb()
+    T, E = x.shape[0], w.shape[0]
+    nv = torch.tensor([Tv], dtype=torch.int32, device="cuda")
+    a_max = T * top_k
+    out = {k: sentinel_like((E + 1,) if k in ("counts", "expert_offsets") else (max(a_max, 1),),
+                            torch.float32 if k == "topk_weights" else torch.int32) for k in ROUTE_KEYS}
+    scores = sentinel_like((T, E), torch.bfloat16)
+    mb.moe_router_route(x, w, top_k, nv, scores=scores, with_weights=True, out=out)
+    ref_scores = mb.moe_router_scores(x, w, nv, out=sentinel_like((T, E), torch.bfloat16))
+    ref = mb.moe_route(ref_scores, top_k, nv, with_weights=True)
+    torch.cuda.synchronize()
+    assert mb.device_error() == 0
+    assert torch.equal(scores.view(torch.int16), ref_scores.view(torch.int16))
+    assert is_sentinel(scores[Tv:])
+    a = Tv * top_k
+    assert torch.equal(out["counts"], ref["counts"]) and torch.equal(out["expert_offsets"], ref["expert_offsets"])
+    for k in ROUTE_KEYS[2:]:
+        assert torch.equal(out[k][:a].view(torch.int32), ref[k][:a].view(torch.int32)), k
+        assert is_sentinel(out[k][a:a_max]), f"{k} written past the routed rows"
+    r_ref = oracle.route(bits(scores), top_k, Tv)
+    np.testing.assert_array_equal(out["counts"].cpu().numpy(), r_ref["counts"])
+    np.testing.assert_array_equal(out["token_indices"][:a].cpu().numpy(), r_ref["token_indices"])
+    np.testing.assert_array_equal(out["expert_indices"][:a].cpu().numpy(), r_ref["expert_indices"])
+    np.testing.assert_array_equal(out["inv_rows"][:a].cpu().numpy().reshape(Tv, top_k), r_ref["inv"])
+    np.testing.assert_array_equal(out["topk_weights"][:a].cpu().numpy().reshape(Tv, top_k),
+                                  oracle.topk_weights(bits(scores)[:Tv], r_ref))
+    return scores
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill_fp8", "fine_grained", "padded_fp8"])
+def test_router_route_workloads(name):
+    """The top-k selection in the router's epilogue, on every workload's router."""
+    cfg = workloads.CONFIGS[name]
+    x = workloads.make_tokens(cfg).cuda()
+    w = workloads.make_router(cfg).cuda()
+    scores = _router_route_case(x, w, cfg.top_k, cfg.valid_tokens)
+    _check_scores(bits(scores), bits(x), bits(w), cfg.valid_tokens)
+
+
+@pytest.mark.parametrize("T,D,E,top_k,Tv", [(1, 16, 1, 1, 1), (130, 48, 8, 8, 129), (300, 1040, 24, 3, 300),
+                                            (257, 64, 256, 6, 200), (1000, 7168, 100, 4, 999),
+                                            (5, 16384, 200, 2, 5), (4096, 256, 16, 2, 0),
+                                            (40000, 128, 64, 8, 39999), (16384, 4096, 128, 4, 11000)])
+def test_router_route_ragged_shapes(T, D, E, top_k, Tv):
+    """Ragged token counts (chunks cut by the valid count, tiles split over clusters of
+    1-8 CTAs), E up to 256 (two column groups per lane), top_k = E, no valid token."""
+    g = torch.Generator().manual_seed(T * 5 + D + E)
+    x = torch.randn(T, D, generator=g).to(torch.bfloat16).cuda()
+    w = (torch.randn(E, D, generator=g) / D ** 0.5).to(torch.bfloat16).cuda()
+    _router_route_case(x, w, top_k, Tv)
+
+
+def test_router_route_ties_go_to_the_lower_expert():
+    """A router with equal rows gives equal scores for those experts: the lower index wins."""
+    g = torch.Generator().manual_seed(3)
+    T, D, E, k = 200, 128, 32, 4
+    x = torch.randn(T, D, generator=g).to(torch.bfloat16).cuda()
+    w = (torch.randn(E, D, generator=g) / D ** 0.5).to(torch.bfloat16)
+    w[5] = w[20]
+    w[6] = w[20]
+    w[31] = w[0]
+    _router_route_case(x, w.cuda(), k, T)
