@@ -610,6 +610,8 @@ __global__ void __launch_bounds__(kThreads) silu_mul_quant_kernel(const __nv_bfl
                                                                   float* __restrict__ z_scale, unsigned int* err) {
   constexpr int kGroupThreads = 32 * G, kGroups = kThreads / kGroupThreads;
   __shared__ float s_red[kWarps];
+  pdl_launch_dependents();  // the next kernel may start its prologue
+  pdl_wait();               // the previous kernel's output is visible
   const int valid = valid_rows(valid_p, sum_counts, E, a, err);
   const int group = threadIdx.x / kGroupThreads, gt = threadIdx.x % kGroupThreads;
   const int stride = gridDim.x * kGroups;
@@ -676,6 +678,8 @@ __global__ void __launch_bounds__(kThreads) scatter_add_rows_kernel(uint4* __res
                                                                     int D8, const int32_t* __restrict__ valid_p,
                                                                     const int32_t* __restrict__ sum_counts, int E,
                                                                     unsigned int* err) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int valid = valid_rows(valid_p, sum_counts, E, a, err);
   const int lane = threadIdx.x & 31;
   const int chunks = (D8 + kChunk - 1) / kChunk;
@@ -730,6 +734,8 @@ __global__ void __launch_bounds__(kThreads) scatter_add_tokens_kernel(uint4* __r
                                                                       const int32_t* __restrict__ valid_p,
                                                                       const int32_t* __restrict__ sum_counts, int E,
                                                                       unsigned int* err) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int valid = valid_rows(valid_p, sum_counts, E, a, err);
   if (valid % k != 0 && blockIdx.x == 0 && threadIdx.x == 0) flag_error(err, MOE_DEVERR_BAD_COUNT);
   int Tv = valid / k;
@@ -816,6 +822,8 @@ __global__ void __launch_bounds__(kThreads) topk_finalize_kernel(uint4* __restri
                                                                  const int32_t* __restrict__ idx, int M, int k,
                                                                  const int32_t* __restrict__ valid_p,
                                                                  const uint4* __restrict__ shared, unsigned int* err) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int Mv = read_count(valid_p, M, err);
   const int lane = threadIdx.x & 31;
   const int chunks = (D8 + kChunk - 1) / kChunk;
@@ -899,6 +907,23 @@ cudaError_t launch_gather_scale(const GatherArgs& g, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Launch with programmatic stream serialization: the kernel may start while the
+// previous kernel of the stream finishes; it calls pdl_wait() before reading
+// anything that kernel (or any earlier one) wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), int grid, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1] = {pdl_attribute()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 // Row groups: the fewest warps per row (G) with at most 4 vectors (32 fp32) per
 // thread, 8 vectors only past 8 warps (D or H above 8192).
 inline int pick_group(int nvec) {
@@ -950,9 +975,10 @@ cudaError_t launch_silu_mul(const SiluArgs& g, cudaStream_t s) {
 #define MOE_SILU_QUANT(G, VPT)                                                                              \
   do {                                                                                                      \
     auto k = silu_mul_quant_kernel<G, VPT, SILU>;                                                           \
-    k<<<persistent_grid(k, g.a, kThreads / (32 * G)), kThreads, 0, s>>>(                                    \
-        static_cast<const __nv_bfloat16*>(g.x0), static_cast<const __nv_bfloat16*>(g.x1), g.ld, g.a, H8,      \
-        g.valid, g.sum_counts, g.E, g.scale_ub, static_cast<uint2*>(g.z), g.z_scale, g.err);                \
+    return launch_pdl(k, persistent_grid(k, g.a, kThreads / (32 * G)), s,                                    \
+                      static_cast<const __nv_bfloat16*>(g.x0), static_cast<const __nv_bfloat16*>(g.x1), g.ld, \
+                      g.a, H8, g.valid, g.sum_counts, g.E, g.scale_ub, static_cast<uint2*>(g.z), g.z_scale,   \
+                      g.err);                                                                               \
   } while (0)
 
 template <bool SILU>
@@ -961,13 +987,12 @@ cudaError_t launch_row_quant(const SiluArgs& g, cudaStream_t s) {
   const int G = pick_group(H8);
   const bool full = H8 > 32 * G * 4;
   switch (G * 2 + (full ? 1 : 0)) {
-    case 2: MOE_SILU_QUANT(1, 4); break;
-    case 4: MOE_SILU_QUANT(2, 4); break;
-    case 8: MOE_SILU_QUANT(4, 4); break;
-    case 16: MOE_SILU_QUANT(8, 4); break;
-    default: MOE_SILU_QUANT(8, 8); break;  // rows past 8192 elements
+    case 2: MOE_SILU_QUANT(1, 4);
+    case 4: MOE_SILU_QUANT(2, 4);
+    case 8: MOE_SILU_QUANT(4, 4);
+    case 16: MOE_SILU_QUANT(8, 4);
+    default: MOE_SILU_QUANT(8, 8);  // rows past 8192 elements
   }
-  return cudaGetLastError();
 }
 #undef MOE_SILU_QUANT
 
@@ -979,27 +1004,25 @@ cudaError_t launch_scatter_add(const ScatterArgs& g, cudaStream_t s) {
   const int D8 = g.D / 8;
   if (g.inv) {
     // the common top_k values get every row load of an item in flight at once
-#define MOE_SCATTER_TOKENS(K, U)                                                                                   \
-  do {                                                                                                             \
-    auto k = g.accumulate ? scatter_add_tokens_kernel<true, K, U> : scatter_add_tokens_kernel<false, K, U>;         \
-    const int grid = persistent_grid(k, (int64_t)g.T * ((D8 + 32 * U - 1) / (32 * U)), kWarps);                   \
-    k<<<grid, kThreads, 0, s>>>(static_cast<uint4*>(g.out), static_cast<const uint4*>(g.in), g.inv, g.top_k, g.a, \
-                                g.T, D8, g.valid, g.sum_counts, g.E, g.err);                                       \
+#define MOE_SCATTER_TOKENS(K, U)                                                                                 \
+  do {                                                                                                           \
+    auto k = g.accumulate ? scatter_add_tokens_kernel<true, K, U> : scatter_add_tokens_kernel<false, K, U>;       \
+    const int grid = persistent_grid(k, (int64_t)g.T * ((D8 + 32 * U - 1) / (32 * U)), kWarps);                 \
+    return launch_pdl(k, grid, s, static_cast<uint4*>(g.out), static_cast<const uint4*>(g.in), g.inv, g.top_k,    \
+                      g.a, g.T, D8, g.valid, g.sum_counts, g.E, g.err);                                          \
   } while (0)
     switch (g.top_k) {
-      case 2: MOE_SCATTER_TOKENS(2, 4); break;
-      case 4: MOE_SCATTER_TOKENS(4, 4); break;
-      case 8: MOE_SCATTER_TOKENS(8, 2); break;
-      default: MOE_SCATTER_TOKENS(0, 4); break;
+      case 2: MOE_SCATTER_TOKENS(2, 4);
+      case 4: MOE_SCATTER_TOKENS(4, 4);
+      case 8: MOE_SCATTER_TOKENS(8, 2);
+      default: MOE_SCATTER_TOKENS(0, 4);
     }
 #undef MOE_SCATTER_TOKENS
-  } else {
-    auto k = g.accumulate ? scatter_add_rows_kernel<true> : scatter_add_rows_kernel<false>;
-    const int grid = persistent_grid(k, (int64_t)g.a * ((D8 + kChunk - 1) / kChunk), kWarps);
-    k<<<grid, kThreads, 0, s>>>(static_cast<uint4*>(g.out), static_cast<const uint4*>(g.in), g.token_indices, g.a,
-                                g.T, D8, g.valid, g.sum_counts, g.E, g.err);
   }
-  return cudaGetLastError();
+  auto k = g.accumulate ? scatter_add_rows_kernel<true> : scatter_add_rows_kernel<false>;
+  const int grid = persistent_grid(k, (int64_t)g.a * ((D8 + kChunk - 1) / kChunk), kWarps);
+  return launch_pdl(k, grid, s, static_cast<uint4*>(g.out), static_cast<const uint4*>(g.in), g.token_indices, g.a,
+                    g.T, D8, g.valid, g.sum_counts, g.E, g.err);
 }
 
 cudaError_t launch_topk_finalize(const FinalizeArgs& g, cudaStream_t s) {
@@ -1008,9 +1031,8 @@ cudaError_t launch_topk_finalize(const FinalizeArgs& g, cudaStream_t s) {
   auto k = g.shared ? (f32 ? topk_finalize_kernel<true, true> : topk_finalize_kernel<true, false>)
                     : (f32 ? topk_finalize_kernel<false, true> : topk_finalize_kernel<false, false>);
   const int grid = persistent_grid(k, (int64_t)g.M * ((D8 + kChunk - 1) / kChunk), kWarps);
-  k<<<grid, kThreads, 0, s>>>(static_cast<uint4*>(g.out), static_cast<const uint4*>(g.rows), g.n_rows, D8, g.weights,
-                              g.idx, g.M, g.k, g.valid, static_cast<const uint4*>(g.shared), g.err);
-  return cudaGetLastError();
+  return launch_pdl(k, grid, s, static_cast<uint4*>(g.out), static_cast<const uint4*>(g.rows), g.n_rows, D8,
+                    g.weights, g.idx, g.M, g.k, g.valid, static_cast<const uint4*>(g.shared), g.err);
 }
 
 }  // namespace moe

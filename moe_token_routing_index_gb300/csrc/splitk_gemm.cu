@@ -26,7 +26,7 @@
 // Warp roles as in the grouped GEMM: warp 0 TMA producer (128 x 128-byte A
 // boxes, B boxes of 128 bytes of K, 128B swizzle), warp 1 MMA issuer and owner
 // of the tensor memory, warps 2-5 move the accumulator rows to shared memory
-// (one row per thread); all six warps reduce.  Waits on the pipeline are
+// (one row per thread); all twelve warps (6-11 idle until then) reduce.  Waits on the pipeline are
 // bounded (1 s); on expiry the kernel records MOE_DEVERR_TIMEOUT, drains what
 // it issued, still meets its cluster at both barriers, frees tensor memory and
 // returns.
@@ -46,7 +46,7 @@ using namespace tc;
 constexpr int kRBM = 128;          // rows per tile
 constexpr int kRBKBytes = 128;     // bytes of K per stage: 64 bf16
 constexpr int kRBK = kRBKBytes / 2;
-constexpr int kRThreads = 192;
+constexpr int kRThreads = 384;   // warps 0-5: producer, MMA, 4 to park the partial; all 12 reduce
 constexpr int kMinKb = 8;          // K blocks per split, at least
 constexpr double kFixedKbPerCta = 6.0;  // a CTA's fixed cost (prologue, epilogue, reduction) in K blocks
 constexpr int kMaxSplit = 8;       // portable cluster size
@@ -352,10 +352,11 @@ __global__ void __launch_bounds__(kRThreads, 1)
         }
       }
     }
-  } else {
+  } else if (warp < 6) {
     // -------------------------------- epilogue: park the partial tile in shared memory
     // The MMAs that read the operand ring have completed once tfull fires, so the
     // ring's first bytes take the partial: row r at smem + r * pstride floats.
+    // (Warps 6-11 only join the reduction below.)
     const int sub = warp & 3;  // the TMEM lane quarter this warp may read
     const int r = sub * 32 + lane;
     if (mbar_wait(bar_tfull, 0, s_abort)) {
