@@ -559,12 +559,19 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
     return res
 
 
-# ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, from the captures
-# summarised under profiles/, with the hash of the kernel sources they were taken
-# on: when those sources change the figure no longer applies and is reported as null.
+# ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the stage's kernels, from
+# the captures summarised under profiles/, with the hash of the kernel sources they were
+# taken on (one file, or a tuple of files for a stage of two kernels): when those sources
+# change the figure no longer applies and is reported as null.
 TRAFFIC: dict = {
-    ("decode", "expert_mlp"): (4_037_701_632 + 5_910_016, "grouped_gemm.cu", "f88d8b86b567"),
-    ("fine_grained", "gemm_w13_silu"): (2_559_575_552 + 133_741_824, "grouped_gemm.cu", "f88d8b86b567"),
+    # the w13 GEMM alone, active experts only (moe_token_routing_index_gb300.cases w13 fine_grained)
+    ("fine_grained", "gemm_w13_silu"): (1_951_564_800 + 133_523_456, "grouped_gemm.cu", "2e6f5978e1bf"),
+    ("decode", "expert_mlp"): (4_037_734_912 + 5_925_888, "grouped_gemm.cu", "2e6f5978e1bf"),
+    # the GEMM and its quantising row pass (cases w13 prefill_fp8 / padded_fp8)
+    ("prefill_fp8", "gemm_w13_silu_quant"): (1_385_779_712 + 125_699_328 + 134_235_136 + 29_882_624,
+                                             ("grouped_gemm.cu", "rowwise.cu"), "13f5f6dd63d5"),
+    ("padded_fp8", "gemm_w13_silu_quant"): (1_792_836_352 + 128_443_136 + 135_184_640 + 32_742_912,
+                                            ("grouped_gemm.cu", "rowwise.cu"), "13f5f6dd63d5"),
 }
 
 
@@ -578,11 +585,11 @@ def _code_only(text: str) -> str:
     return " ".join(text.split())
 
 
-def kernel_source_hash(name: str) -> str:
-    """sha1 (12 hex digits) of the code of a kernel source and of every local header it
-    reaches through `#include "..."`, in first-reach order (comments and whitespace
-    dropped): counters captured on one build are reported only while that code is
-    unchanged."""
+def kernel_source_hash(name) -> str:
+    """sha1 (12 hex digits) of the code of a kernel source (or of several, in order) and of
+    every local header it reaches through `#include "..."`, in first-reach order (comments
+    and whitespace dropped): counters captured on one build are reported only while that
+    code is unchanged."""
     import hashlib
     import re
 
@@ -598,7 +605,8 @@ def kernel_source_hash(name: str) -> str:
         for inc in re.findall(r'^\s*#\s*include\s+"([^"]+)"', path.read_text(), re.M):
             visit(path.parent / inc)
 
-    visit(csrc / name)
+    for n in ((name,) if isinstance(name, str) else name):
+        visit(csrc / n)
     h = hashlib.sha1()
     for f in order:
         h.update(_code_only(f.read_text()).encode())

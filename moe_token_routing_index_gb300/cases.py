@@ -1,0 +1,129 @@
+"""Single-GEMM cases at the workloads' shapes, for timing and ncu captures.
+
+    python -m moe_token_routing_index_gb300.cases w13 fine_grained [--tiles pairs|single] [--launches N]
+    python -m moe_token_routing_index_gb300.cases fp8_w13 grouped|one [--tiles single|pairs] [--launches N]
+
+w13: the workload's w13 grouped GEMM as the layer runs it (SiLU*mul epilogue for bf16
+layers, SiLU*mul + row quantisation for FP8 layers, tile-packed weights), with the
+per-expert counts of routing the workload's scores (moe_route on the device).  Only
+the active experts' weights are allocated: the GEMM never reads the others, so the
+launch moves the same bytes as inside the whole forward while holding a few GB
+instead of the workload's full weight set.  Inputs are random with the workload's
+shapes (the values do not change the traffic or the time).
+
+fp8_w13: the prefill-shaped FP8 w13 GEMM (8192 rows, K = 5120, N = 16384, plain
+epilogue), its rows split 16 x 512 over the experts ("grouped", as the prefill
+workload routes them) or all in one expert ("one").
+
+Each case runs 2 warm-up launches and then N timed ones (CUDA events), and prints
+one JSON line.  Every launch is the library's own kernel.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+
+import torch
+
+from . import binding as mb
+from . import workloads
+
+
+def _time(fn, launches: int) -> float:
+    for _ in range(2):
+        fn()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(launches):
+        fn()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / launches * 1e3
+
+
+def case_w13(name: str, tiles: str, launches: int) -> dict:
+    cfg = workloads.CONFIGS[name]
+    dev = torch.device("cuda")
+    scores = workloads.make_scores(cfg).to(dev)
+    nv = None if cfg.Tv is None else torch.tensor([cfg.Tv], dtype=torch.int32, device=dev)
+    counts = mb.moe_route(scores, cfg.top_k, nv)["counts"][: cfg.E].cpu()
+    active = counts[counts > 0].to(torch.int32)
+    E, D, H = int(active.numel()), cfg.D, cfg.H
+    a = int(active.sum())
+    g = torch.Generator(device=dev).manual_seed(0)
+    w = torch.randn(E, 2 * H, D, device=dev, generator=g) * cfg.weight_std
+    x = torch.randn(a, D, device=dev, generator=g)
+    cd = active.to(dev)
+    flags = mb.MOE_GEMM_CTA_PAIRS if tiles == "pairs" else 0
+    if cfg.fp8:
+        wq, ws = mb.moe_quantize_rows(w)
+        del w
+        w = mb.moe_pack_weights(wq)
+        xq, xs = mb.moe_quantize_rows(x)
+        zb = torch.empty(a, H, dtype=torch.bfloat16, device=dev)
+        zq = torch.empty(a, H, dtype=torch.float8_e4m3fn, device=dev)
+        zs = torch.empty(a, dtype=torch.float32, device=dev)
+        ub = torch.tensor([cfg.scale_ub or 1200.0], dtype=torch.float32, device=dev)
+        fn = lambda: mb.moe_grouped_gemm_fp8_rowwise(xq, w, cd, xs, ws, epilogue=mb.MOE_EPILOGUE_SILU_MUL_QUANT | flags,
+                                                     out=zb, scale_ub=ub, z_out=zq, z_scale=zs)
+        wb = 1
+    else:
+        w = mb.moe_pack_weights(w.to(torch.bfloat16))
+        xb = x.to(torch.bfloat16)
+        z = torch.empty(a, H, dtype=torch.bfloat16, device=dev)
+        fn = lambda: mb.moe_grouped_gemm(xb, w, cd, epilogue=mb.MOE_EPILOGUE_SILU_MUL | flags, out=z)
+        wb = 2
+    us = _time(fn, launches)
+    flops = 2.0 * a * 2 * H * D
+    alg = E * 2 * H * D * wb + a * D * wb + a * H * 2
+    if mb.device_error() != 0:
+        raise RuntimeError("device-side error")
+    return {"case": f"w13 {name}", "tiles": tiles, "experts": E, "rows": a, "max_rows": int(active.max()),
+            "us": round(us, 1), "TFLOP/s": round(flops / us / 1e6, 1), "algorithmic_bytes": alg}
+
+
+def case_fp8_w13(shape: str, tiles: str, launches: int) -> dict:
+    cfg = workloads.CONFIGS["prefill_fp8"]
+    dev = torch.device("cuda")
+    E, D, H, a = cfg.E, cfg.D, cfg.H, 8192
+    g = torch.Generator(device=dev).manual_seed(0)
+    wq, ws = mb.moe_quantize_rows(torch.randn(E, 2 * H, D, device=dev, generator=g) * cfg.weight_std)
+    w = mb.moe_pack_weights(wq)
+    del wq
+    xq, xs = mb.moe_quantize_rows(torch.randn(a, D, device=dev, generator=g))
+    if shape == "grouped":
+        counts = torch.full((E,), a // E, dtype=torch.int32, device=dev)
+    else:
+        counts = torch.zeros(E, dtype=torch.int32, device=dev)
+        counts[0] = a
+    y = torch.empty(a, 2 * H, dtype=torch.bfloat16, device=dev)
+    flags = mb.MOE_GEMM_CTA_PAIRS if tiles == "pairs" else 0
+    us = _time(lambda: mb.moe_grouped_gemm_fp8_rowwise(xq, w, counts, xs, ws, epilogue=flags, out=y), launches)
+    if mb.device_error() != 0:
+        raise RuntimeError("device-side error")
+    return {"case": f"fp8_w13 {shape}", "tiles": tiles, "us": round(us, 1),
+            "TFLOP/s": round(2.0 * a * 2 * H * D / us / 1e6, 1)}
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("case", choices=["w13", "fp8_w13"])
+    p.add_argument("which", help="w13: a workload name; fp8_w13: grouped or one")
+    p.add_argument("--tiles", choices=["single", "pairs"], default=None,
+                   help="128-row tiles or 256-row tiles on CTA pairs (default: pairs for bf16, single for FP8)")
+    p.add_argument("--launches", type=int, default=20)
+    args = p.parse_args(argv)
+    if args.case == "w13":
+        cfg = workloads.CONFIGS[args.which]
+        tiles = args.tiles or ("single" if cfg.fp8 else "pairs")
+        res = case_w13(args.which, tiles, args.launches)
+    else:
+        if args.which not in ("grouped", "one"):
+            p.error("fp8_w13 takes grouped or one")
+        res = case_fp8_w13(args.which, args.tiles or "single", args.launches)
+    print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -19,8 +19,9 @@
 //              two halves, bf16 rounding, stores with row/column masks.
 // Tiles: for each expert e, ceil(count_e / 128) row tiles x the N tiles;
 // consecutive tile ids walk the row tiles of one weight slice first, so CTAs
-// running together share that slice in L2.  Every CTA derives the tile list
-// from the device counts itself (no host synchronisation).
+// running together share that slice in L2, in bands of row tiles whose x rows
+// fit a share of L2 (band_order).  Every CTA derives the tile list from the
+// device counts itself (no host synchronisation).
 //
 // Every mbarrier wait is bounded (1 s of %globaltimer); on expiry the kernel
 // records MOE_DEVERR_TIMEOUT, all roles stop, in-flight copies and MMAs are
@@ -80,9 +81,25 @@ struct Tile {
   int expert, row0, rows, n_idx;
 };
 
+// The row-tile and N-tile index of tile `local` of an expert with mt row tiles and
+// n_tiles N tiles.  The tiles are walked in bands of `band` row tiles; inside a band
+// N-major with the row tiles innermost, so the CTAs running together share one weight
+// slice and the band's rows of x, and every other band walks N backwards, so that it
+// starts on the weight slices the band before read last, while they are in L2.
+// band >= mt: one band (N-major over all row tiles).
+__device__ __forceinline__ void band_order(int local, int mt, int n_tiles, int band, int* m_idx, int* n_idx) {
+  const int b = local / (band * n_tiles);
+  const int bm = min(band, mt - b * band);
+  const int lb = local - b * band * n_tiles;
+  int n = lb / bm;
+  if (b & 1) n = n_tiles - 1 - n;
+  *n_idx = n;
+  *m_idx = b * band + lb % bm;
+}
+
 // Decode tile id -> (expert, first routed row, valid rows, N-tile index).
-__device__ __forceinline__ Tile decode_tile(int tile, int E, int n_tiles, const int* tile_start, const int* row_off,
-                                            const int* mtiles) {
+__device__ __forceinline__ Tile decode_tile(int tile, int E, int n_tiles, int band, const int* tile_start,
+                                            const int* row_off, const int* mtiles) {
   const int mt_global = tile / n_tiles;  // which row tile, counting over experts
   int lo = 0, hi = E - 1;                // find e with tile_start[e] <= mt_global < tile_start[e + 1]
   while (lo < hi) {
@@ -91,11 +108,11 @@ __device__ __forceinline__ Tile decode_tile(int tile, int E, int n_tiles, const 
     else hi = mid - 1;
   }
   const int e = lo;
-  const int local = tile - tile_start[e] * n_tiles;  // within the expert: N-major, row tiles innermost
-  const int m_idx = local % mtiles[e];
+  int m_idx, n_idx;
+  band_order(tile - tile_start[e] * n_tiles, mtiles[e], n_tiles, band, &m_idx, &n_idx);
   Tile t;
   t.expert = e;
-  t.n_idx = local / mtiles[e];
+  t.n_idx = n_idx;
   t.row0 = row_off[e] + m_idx * kBM;
   const int rows_left = row_off[e + 1] - t.row0;
   t.rows = rows_left < kBM ? rows_left : kBM;
@@ -112,6 +129,7 @@ struct Phase {
   int n_out;          // stored columns: N, or N / 2 for SILU_MUL
   int n_tile_cols;    // stored columns per tile
   int n_tiles;        // tiles along N
+  int band;           // row tiles per band of the tile order (band_order)
   int num_kb;         // K blocks
   __nv_bfloat16* y;   // [a_max, n_out], or [T_out, n_out] when scattering
   const float* x_scale;
@@ -406,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(
   auto locate = [&](int tile, int* ph) {
     *ph = (NPHASE == 2 && tile >= tiles0) ? 1 : 0;
     const Phase& p = *ph ? p1 : p0;
-    return decode_tile(*ph ? tile - tiles0 : tile, E, p.n_tiles, tile_start, row_off, mtiles);
+    return decode_tile(*ph ? tile - tiles0 : tile, E, p.n_tiles, p.band, tile_start, row_off, mtiles);
   };
 
   if (warp == 0) {
@@ -785,11 +803,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_pair_kernel(
       else hi = mid - 1;
     }
     const int e = lo;
-    const int local = tile - tile_start[e] * p.n_tiles;
+    int m_idx, n_idx;
+    band_order(tile - tile_start[e] * p.n_tiles, mtiles[e], p.n_tiles, p.band, &m_idx, &n_idx);
     Tile t;
     t.expert = e;
-    t.n_idx = local / mtiles[e];
-    t.row0 = row_off[e] + (local % mtiles[e]) * kPairBM;
+    t.n_idx = n_idx;
+    t.row0 = row_off[e] + m_idx * kPairBM;
     const int rows_left = row_off[e + 1] - t.row0;
     t.rows = rows_left < kPairBM ? rows_left : kPairBM;
     return t;
@@ -963,8 +982,21 @@ __global__ void pack_weights_kernel(const uint8_t* __restrict__ w, int64_t rows,
   }
 }
 
+// Bytes of x rows that one band of the tile order may span: on the fine-grained w13
+// GEMM (K = 7168 bf16, 8 experts of 4096 rows) bands of 8 pair row tiles (29 MB of x)
+// moved the least DRAM traffic, 2.06 GB per launch against 2.51 GB in one band per
+// expert; 6 and 10 row tiles moved 2.23 and 2.17 GB.
+constexpr int64_t kBandBytes = 30ll << 20;
+
+int band_rows_tiles(int tile_rows, int K, bool fp8) {
+  const int64_t per_tile = (int64_t)tile_rows * K * (fp8 ? 1 : 2);
+  const int64_t b = kBandBytes / (per_tile > 0 ? per_tile : 1);
+  return (int)(b < 1 ? 1 : (b > 1024 ? 1024 : b));
+}
+
 Phase make_phase(int N, int K, int epi, bool fp8, void* y, const float* xs, const float* ws) {
   Phase p;
+  p.band = band_rows_tiles(kBM, K, fp8);
   p.N = N;
   p.K = K;
   p.epi = epi;
@@ -1086,6 +1118,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& g, cudaStream_t s) {
   CUtensorMap my = mb;
   if (!g.scatter) p.tma_store = make_map_sw128(&my, g.y, g.a_max, p.n_out, false, 32) ? 1 : 0;
   if (g.pairs) {
+    p.band = band_rows_tiles(kPairBM, g.K, g.fp8);
     if (g.fp8) return launch_pair<true>(ma, mb, my, g.counts, p, g.E, g.a_max, g.err, s);
     return launch_pair<false>(ma, mb, my, g.counts, p, g.E, g.a_max, g.err, s);
   }

@@ -100,12 +100,14 @@ class MoELayer:
         # None: one launch for both bf16 GEMMs when the batch averages at most one
         # 128-row tile per expert (weight-streaming, HBM-bound), else two launches.
         self.fused_mlp = fused_mlp
-        # None: 256-row tiles on CTA pairs when they pad the expert rows little more
-        # than 128-row tiles do (judged from the previous forward's counts; before the
-        # first, when the batch averages at least 256 rows per expert).  The output is
-        # the same bit for bit either way.  Per clock the pair tiles keep the tensor
-        # pipe busier (FP8 prefill w13 on GB300: 2.20 against 1.85 TFLOP/s per MHz),
-        # and they stay ahead under the 1.4 kW power cap.
+        # None: 256-row tiles on CTA pairs for the bf16 GEMMs when they pad the expert
+        # rows little more than 128-row tiles do (judged from the previous forward's
+        # counts; before the first, when the batch averages at least 256 rows per
+        # expert).  The output is the same bit for bit either way.  The FP8 GEMMs keep
+        # 128-row tiles: inside a whole forward on GB300 their pair tiles ran slower
+        # (prefill, 512 rows per expert: 0.953 against 0.890 ms per step, the clock
+        # lower under the power cap) or padded more rows (344 rows per expert: 1.062
+        # against 0.901 ms), although in isolation they keep the tensor pipe busier.
         self.cta_pairs = cta_pairs
         self._counts_host: torch.Tensor | None = None   # pinned copy of the last forward's counts
         self._counts_event: torch.cuda.Event | None = None
@@ -432,6 +434,8 @@ class MoELayer:
     def use_cta_pairs(self, T: int) -> bool:
         if self.cta_pairs is not None:
             return self.cta_pairs
+        if self.fp8:
+            return False
         last = self._last_counts()
         if last is not None:
             return self.prefer_pairs(last)
@@ -445,7 +449,7 @@ class MoELayer:
 
     def _note_counts(self, counts: torch.Tensor):
         """Start a copy of this forward's counts to pinned host memory (for the tile choice)."""
-        if self._capturing or self.cta_pairs is not None:
+        if self._capturing or self.fp8 or self.cta_pairs is not None:
             return
         if self._counts_host is None:
             self._counts_host = torch.empty(self.E + 1, dtype=torch.int32).pin_memory()

@@ -251,6 +251,45 @@ def test_grouped_gemm_fp8_workloads_sampled(name, variant):
     _check_close(bits(o[rows]), o_ref, _fp8_bound(zq_h, zs_h, w2_h, w2s_h, sub_cnt))
 
 
+@pytest.mark.parametrize("fp8", [False, True])
+def test_banded_tile_order_long_k(fp8):
+    """A reduction long enough that the tile order splits each expert's row tiles into
+    bands (bf16: 2 row tiles per band of 128-row tiles, 1 per band of pair tiles; FP8: 4
+    and 2), with every other band walking N backwards and a partial last band: pairs ==
+    single-CTA tiles bit for bit, and every expert's first, last, last-tile and random
+    rows within the oracle bound."""
+    mb = _mb()
+    E, counts, N, K = 3, [700, 0, 300], 512, 61440
+    g = torch.Generator().manual_seed(123)
+    a = sum(counts)
+    x = torch.randn(a, K, generator=g).to(torch.bfloat16)
+    w = (torch.randn(E, N, K, generator=g) * 0.01).to(torch.bfloat16)
+    cnt = np.array(counts, np.int32)
+    cd = torch.from_numpy(cnt).cuda()
+    rows = _sample_rows_with_tail(cnt, np.random.default_rng(3))
+    exp_of_row = np.repeat(np.arange(E), cnt)[rows]
+    used = sorted(set(exp_of_row.tolist()))
+    sub_cnt = np.array([(exp_of_row == e).sum() for e in used], np.int32)
+    if fp8:
+        xq, xs = mb.moe_quantize_rows(x.float().cuda())
+        wq, ws = mb.moe_quantize_rows(w.float().cuda())
+        y1 = mb.moe_grouped_gemm_fp8_rowwise(xq, wq, cd, xs, ws)
+        y2 = mb.moe_grouped_gemm_fp8_rowwise(xq, wq, cd, xs, ws, epilogue=mb.MOE_GEMM_CTA_PAIRS)
+        xq_h, xs_h = bits(xq)[rows], xs.cpu().numpy()[rows]
+        wq_h, ws_h = bits(wq[used]), ws[used].cpu().numpy()
+        ref = oracle.grouped_gemm_fp8(xq_h, wq_h, sub_cnt, xs_h, ws_h)
+        bound = _fp8_bound(xq_h, xs_h, wq_h, ws_h, sub_cnt)
+    else:
+        y1 = mb.moe_grouped_gemm(x.cuda(), w.cuda(), cd)
+        y2 = mb.moe_grouped_gemm(x.cuda(), w.cuda(), cd, epilogue=mb.MOE_GEMM_CTA_PAIRS)
+        ref = oracle.grouped_gemm_bf16(bits(x)[rows], bits(w[used]), sub_cnt)
+        bound = _abs_bound_bf16(bits(x)[rows], bits(w[used]), sub_cnt)
+    torch.cuda.synchronize()
+    assert mb.device_error() == 0
+    assert torch.equal(y1, y2)
+    _check_close(bits(y1[rows]), ref, bound)
+
+
 SILU_QUANT_SHAPES = [s for s in SHAPES if s[2] % 32 == 0] + [
     (2, [77, 300], 2 * 8192, 64, 400),       # z rows of 8192 elements (8 warps per row, 4 vectors each)
     (1, [33], 2 * 16384, 32, None),          # the largest H the row pass takes
