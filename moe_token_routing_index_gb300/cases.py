@@ -16,10 +16,12 @@ fp8_w13: the prefill-shaped FP8 w13 GEMM (8192 rows, K = 5120, N = 16384, plain
 epilogue), its rows split 16 x 512 over the experts ("grouped", as the prefill
 workload routes them) or all in one expert ("one").
 
-rowwise: every row kernel of the library at the workload's shapes, on the routing of
-its scores: moe_route, moe_gather_scale, moe_gather_scale_quant, moe_silu_mul,
-moe_silu_mul_quant, moe_scatter_add, moe_scatter_add_padded (the routed rows as the
-padded layout with one rank) and moe_topk_finalize.  Each launch is timed alone with
+rowwise: every bandwidth- or latency-bound kernel of the library at the workload's
+shapes, on the routing of its scores: moe_router_scores and moe_router_route (router
+weight of the whole-layer workload), moe_route, moe_gather_scale,
+moe_gather_scale_quant, moe_silu_mul, moe_silu_mul_quant, moe_scatter_add,
+moe_scatter_add_padded (the routed rows as the padded layout with one rank) and
+moe_topk_finalize.  Each launch is timed alone with
 CUDA events after a 256 MB write that evicts L2; the line gives the mean time, the
 algorithmic bytes and GB/s (and the fraction of the measured HBM copy peak when
 MEASURED_PEAKS.json sits beside the package).
@@ -158,8 +160,17 @@ def case_rowwise(name: str, launches: int) -> dict:
     ub = torch.tensor([cfg.scale_ub], dtype=torch.float32, device=dev) if cfg.scale_ub else None
     valid = r["counts"][E:]   # the routed-row count on the device, as the layer passes it
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    wr = workloads.make_router(cfg, device=dev)
+    rs = torch.empty(T, E, dtype=torch.bfloat16, device=dev)
+    rws = torch.empty(max(mb.moe_router_workspace_size(T, D, E), 1), dtype=torch.uint8, device=dev)
+    rr_ws = torch.empty(max(mb.moe_router_route_workspace_size(T, D, E, k), 1), dtype=torch.uint8, device=dev)
+    _, rr_out = mb.moe_router_route(x, wr, k, nv, scores=rs, workspace=rr_ws)   # its outputs, allocated once
+    router_bytes = Tv * D * 2 + E * D * 2 + Tv * E * 2
     # (callable, algorithmic bytes per launch; the per-kernel figures of the roofline table)
     kernels = {
+        "moe_router_scores": (lambda: mb.moe_router_scores(x, wr, nv, out=rs, workspace=rws), router_bytes),
+        "moe_router_route": (lambda: mb.moe_router_route(x, wr, k, nv, scores=rs, out=rr_out, workspace=rr_ws),
+                             router_bytes + a * 12 + 8 * (E + 1)),
         "moe_route": (lambda: mb.moe_route(scores, k, nv, with_weights=True, out=r, workspace=ws),
                       Tv * E * 2 + a * 12 + 8 * (E + 1)),
         "moe_gather_scale": (lambda: mb.moe_gather_scale(x, ti, ei, scores, valid, inv_rows=inv, top_k=k, out=xr),

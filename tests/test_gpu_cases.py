@@ -9,7 +9,7 @@ def test_rowwise_case_times_every_row_kernel():
     from moe_token_routing_index_gb300 import cases
 
     res = cases.case_rowwise("tiny", 2)
-    assert set(res["kernels"]) == {"moe_route", "moe_gather_scale", "moe_gather_scale_quant", "moe_silu_mul",
+    assert set(res["kernels"]) == {"moe_router_scores", "moe_router_route", "moe_route", "moe_gather_scale", "moe_gather_scale_quant", "moe_silu_mul",
                                    "moe_silu_mul_quant", "moe_scatter_add", "moe_scatter_add_padded",
                                    "moe_topk_finalize"}
     for d in res["kernels"].values():
