@@ -565,13 +565,13 @@ def report(args, cfg, world, ms, stage_ms, counts, clocks, e2e_ms, h2d, d2h, lay
 # change the figure no longer applies and is reported as null.
 TRAFFIC: dict = {
     # the w13 GEMM alone, active experts only (moe_token_routing_index_gb300.cases w13 fine_grained)
-    ("fine_grained", "gemm_w13_silu"): (1_951_564_800 + 133_523_456, "grouped_gemm.cu", "2e6f5978e1bf"),
-    ("decode", "expert_mlp"): (4_037_734_912 + 5_925_888, "grouped_gemm.cu", "2e6f5978e1bf"),
+    ("fine_grained", "gemm_w13_silu"): (2_077_630_720 + 134_013_184, "grouped_gemm.cu", "e0257906703a"),
+    ("decode", "expert_mlp"): (4_037_685_504 + 5_910_016, "grouped_gemm.cu", "e0257906703a"),
     # the GEMM and its quantising row pass (cases w13 prefill_fp8 / padded_fp8)
-    ("prefill_fp8", "gemm_w13_silu_quant"): (1_385_779_712 + 125_699_328 + 134_235_136 + 29_882_624,
-                                             ("grouped_gemm.cu", "rowwise.cu"), "13f5f6dd63d5"),
-    ("padded_fp8", "gemm_w13_silu_quant"): (1_792_836_352 + 128_443_136 + 135_184_640 + 32_742_912,
-                                            ("grouped_gemm.cu", "rowwise.cu"), "13f5f6dd63d5"),
+    ("prefill_fp8", "gemm_w13_silu_quant"): (1_385_728_768 + 126_059_520 + 134_234_624 + 29_979_392,
+                                             ("grouped_gemm.cu", "rowwise.cu"), "cd11016e2830"),
+    ("padded_fp8", "gemm_w13_silu_quant"): (1_792_874_496 + 128_456_448 + 135_185_152 + 32_439_296,
+                                            ("grouped_gemm.cu", "rowwise.cu"), "cd11016e2830"),
 }
 
 

@@ -93,8 +93,7 @@ __global__ void __launch_bounds__(kThreads) gather_scale_kernel(
     const uint4* __restrict__ x, int T, int D8, const int32_t* __restrict__ ti, const int32_t* __restrict__ ei,
     int a, const void* __restrict__ scores, int dtype, int64_t st, int64_t se, int E,
     const int32_t* __restrict__ valid_p, uint4* __restrict__ out, unsigned int* err) {
-  pdl_launch_dependents();  // the next kernel may start its prologue
-  pdl_wait();               // the routing written by the previous kernel is visible
+  pdl_wait();  // launched while the routing kernel runs: its output is visible from here
   const int valid = read_count(valid_p, a, err);
   const int lane = threadIdx.x & 31;
   const int chunks = (D8 + kGatherChunk - 1) / kGatherChunk;
@@ -313,8 +312,7 @@ __global__ void __launch_bounds__(kStagedMaxWarps * 32, 1) gather_staged_kernel(
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);                      // [warps][NB]
   int* s_tok = reinterpret_cast<int*>(smem + nwb * NB * 8);                // [warps][NB]: staged token or -1
   uint8_t* slots = smem + ((nwb * NB * 16 + 127) / 128) * 128;             // [warps][NB][row_bytes]
-  pdl_launch_dependents();  // the next kernel may start its prologue
-  pdl_wait();               // the routing written by the previous kernel is visible
+  pdl_wait();  // launched while the routing kernel runs: its output is visible from here
   const int valid = read_count(valid_p, a, err);
   const int nrows = inv ? k : 1;  // routed rows per item
   int items = valid;
@@ -610,8 +608,6 @@ __global__ void __launch_bounds__(kThreads) silu_mul_quant_kernel(const __nv_bfl
                                                                   float* __restrict__ z_scale, unsigned int* err) {
   constexpr int kGroupThreads = 32 * G, kGroups = kThreads / kGroupThreads;
   __shared__ float s_red[kWarps];
-  pdl_launch_dependents();  // the next kernel may start its prologue
-  pdl_wait();               // the previous kernel's output is visible
   const int valid = valid_rows(valid_p, sum_counts, E, a, err);
   const int group = threadIdx.x / kGroupThreads, gt = threadIdx.x % kGroupThreads;
   const int stride = gridDim.x * kGroups;
@@ -678,8 +674,6 @@ __global__ void __launch_bounds__(kThreads) scatter_add_rows_kernel(uint4* __res
                                                                     int D8, const int32_t* __restrict__ valid_p,
                                                                     const int32_t* __restrict__ sum_counts, int E,
                                                                     unsigned int* err) {
-  pdl_launch_dependents();
-  pdl_wait();
   const int valid = valid_rows(valid_p, sum_counts, E, a, err);
   const int lane = threadIdx.x & 31;
   const int chunks = (D8 + kChunk - 1) / kChunk;
@@ -734,8 +728,6 @@ __global__ void __launch_bounds__(kThreads) scatter_add_tokens_kernel(uint4* __r
                                                                       const int32_t* __restrict__ valid_p,
                                                                       const int32_t* __restrict__ sum_counts, int E,
                                                                       unsigned int* err) {
-  pdl_launch_dependents();
-  pdl_wait();
   const int valid = valid_rows(valid_p, sum_counts, E, a, err);
   if (valid % k != 0 && blockIdx.x == 0 && threadIdx.x == 0) flag_error(err, MOE_DEVERR_BAD_COUNT);
   int Tv = valid / k;
@@ -822,8 +814,6 @@ __global__ void __launch_bounds__(kThreads) topk_finalize_kernel(uint4* __restri
                                                                  const int32_t* __restrict__ idx, int M, int k,
                                                                  const int32_t* __restrict__ valid_p,
                                                                  const uint4* __restrict__ shared, unsigned int* err) {
-  pdl_launch_dependents();
-  pdl_wait();
   const int Mv = read_count(valid_p, M, err);
   const int lane = threadIdx.x & 31;
   const int chunks = (D8 + kChunk - 1) / kChunk;
@@ -907,20 +897,12 @@ cudaError_t launch_gather_scale(const GatherArgs& g, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-// Launch with programmatic stream serialization: the kernel may start while the
-// previous kernel of the stream finishes; it calls pdl_wait() before reading
-// anything that kernel (or any earlier one) wrote.
+// Plain launch of a row kernel (kThreads per block), after the previous kernel of
+// the stream.  Programmatic dependent launch is kept for the gathers only: on the
+// row pass, the scatters and the finalize it made the steps slower.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), int grid, cudaStream_t s, Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1] = {pdl_attribute()};
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
-  if (e != cudaSuccess) return e;
+cudaError_t launch_rows(void (*kern)(KArgs...), int grid, cudaStream_t s, Args... args) {
+  kern<<<grid, kThreads, 0, s>>>(static_cast<KArgs>(args)...);
   return cudaGetLastError();
 }
 
@@ -975,7 +957,7 @@ cudaError_t launch_silu_mul(const SiluArgs& g, cudaStream_t s) {
 #define MOE_SILU_QUANT(G, VPT)                                                                              \
   do {                                                                                                      \
     auto k = silu_mul_quant_kernel<G, VPT, SILU>;                                                           \
-    return launch_pdl(k, persistent_grid(k, g.a, kThreads / (32 * G)), s,                                    \
+    return launch_rows(k, persistent_grid(k, g.a, kThreads / (32 * G)), s,                                    \
                       static_cast<const __nv_bfloat16*>(g.x0), static_cast<const __nv_bfloat16*>(g.x1), g.ld, \
                       g.a, H8, g.valid, g.sum_counts, g.E, g.scale_ub, static_cast<uint2*>(g.z), g.z_scale,   \
                       g.err);                                                                               \
@@ -1008,7 +990,7 @@ cudaError_t launch_scatter_add(const ScatterArgs& g, cudaStream_t s) {
   do {                                                                                                           \
     auto k = g.accumulate ? scatter_add_tokens_kernel<true, K, U> : scatter_add_tokens_kernel<false, K, U>;       \
     const int grid = persistent_grid(k, (int64_t)g.T * ((D8 + 32 * U - 1) / (32 * U)), kWarps);                 \
-    return launch_pdl(k, grid, s, static_cast<uint4*>(g.out), static_cast<const uint4*>(g.in), g.inv, g.top_k,    \
+    return launch_rows(k, grid, s, static_cast<uint4*>(g.out), static_cast<const uint4*>(g.in), g.inv, g.top_k,    \
                       g.a, g.T, D8, g.valid, g.sum_counts, g.E, g.err);                                          \
   } while (0)
     switch (g.top_k) {
@@ -1021,7 +1003,7 @@ cudaError_t launch_scatter_add(const ScatterArgs& g, cudaStream_t s) {
   }
   auto k = g.accumulate ? scatter_add_rows_kernel<true> : scatter_add_rows_kernel<false>;
   const int grid = persistent_grid(k, (int64_t)g.a * ((D8 + kChunk - 1) / kChunk), kWarps);
-  return launch_pdl(k, grid, s, static_cast<uint4*>(g.out), static_cast<const uint4*>(g.in), g.token_indices, g.a,
+  return launch_rows(k, grid, s, static_cast<uint4*>(g.out), static_cast<const uint4*>(g.in), g.token_indices, g.a,
                     g.T, D8, g.valid, g.sum_counts, g.E, g.err);
 }
 
@@ -1031,7 +1013,7 @@ cudaError_t launch_topk_finalize(const FinalizeArgs& g, cudaStream_t s) {
   auto k = g.shared ? (f32 ? topk_finalize_kernel<true, true> : topk_finalize_kernel<true, false>)
                     : (f32 ? topk_finalize_kernel<false, true> : topk_finalize_kernel<false, false>);
   const int grid = persistent_grid(k, (int64_t)g.M * ((D8 + kChunk - 1) / kChunk), kWarps);
-  return launch_pdl(k, grid, s, static_cast<uint4*>(g.out), static_cast<const uint4*>(g.rows), g.n_rows, D8,
+  return launch_rows(k, grid, s, static_cast<uint4*>(g.out), static_cast<const uint4*>(g.rows), g.n_rows, D8,
                     g.weights, g.idx, g.M, g.k, g.valid, static_cast<const uint4*>(g.shared), g.err);
 }
 
