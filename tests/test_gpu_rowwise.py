@@ -276,3 +276,53 @@ def test_binding_rejects_strided_matrices():
     # rows of y may be strided (the ABI takes the row stride): a column slice is accepted
     z = mb.moe_silu_mul(torch.randn(8, 96, device="cuda").to(torch.bfloat16)[:, :64], 32)
     assert z.shape == (8, 32) and mb.device_error() == 0
+
+
+@pytest.mark.parametrize("staged", [False, True])
+@pytest.mark.parametrize("quant", [False, True])
+def test_gather_sees_inputs_of_a_slow_preceding_kernel(staged, quant):
+    """The gathers are launched with programmatic stream serialization: they may start
+    before the previous kernel ends when that kernel signals (the routing kernels do;
+    every forward's parity test covers that case), and must otherwise wait for it as any
+    launch does.  Here the inputs come from torch kernels that never signal, queued
+    behind a reduction over 1 GiB that feeds every input (token indices, expert indices,
+    scores, valid count), so the GPU is busy when the gather is enqueued.  In three
+    rounds with changing inputs, each result equals the oracle's gather of the final
+    inputs bit for bit."""
+    mb = _mb()
+    T, D, E, k = 512, 2048, 16, (4 if staged else 1)
+    a = T * k
+    g = torch.Generator(device="cuda").manual_seed(3)
+    x = torch.randn(T, D, device="cuda", generator=g).to(torch.bfloat16)
+    big = torch.ones(1 << 28, device="cuda")                     # 1 GiB of fp32 ones
+    for rnd in range(3):
+        zero = (big.sum() * 0.0).to(torch.int32)                 # 0, produced by a slow kernel
+        perm = torch.randperm(T, device="cuda", generator=g).to(torch.int32)
+        tok = (perm.repeat_interleave(k) + zero).contiguous()    # routed row -> token
+        exp = ((torch.arange(a, device="cuda", dtype=torch.int32) * 7 + rnd) % E + zero).contiguous()
+        scores = (torch.rand(T, E, device="cuda", generator=g) + zero.float()).to(torch.bfloat16)
+        valid = (torch.tensor([a - 3 * rnd], device="cuda", dtype=torch.int32) + zero).contiguous()
+        inv = None
+        if staged:   # token-major: token t's k rows are rows t*k .. t*k+k-1 of the buffer, in order
+            order = torch.argsort(perm.long())
+            inv = ((order.view(T, 1) * k + torch.arange(k, device="cuda").view(1, k)).reshape(-1)
+                   .to(torch.int32) + zero).contiguous()
+            tok = perm.repeat_interleave(k).to(torch.int32)
+            tok = (tok + zero).contiguous()
+            valid = (torch.tensor([a], device="cuda", dtype=torch.int32) + zero).contiguous()
+        kw = dict(inv_rows=inv, top_k=k) if staged else {}
+        if quant:
+            out, sc = mb.moe_gather_scale_quant(x, tok, exp, scores, None, valid, **kw)
+        else:
+            out = mb.moe_gather_scale(x, tok, exp, scores, valid, **kw)
+        torch.cuda.synchronize()
+        assert mb.device_error() == 0
+        n = int(valid.item())
+        ti, ei, sb = tok.cpu().numpy(), exp.cpu().numpy(), bits(scores.cpu())
+        if quant:   # bit-exact against the oracle: codes and scales
+            q_ref, s_ref = oracle.gather_scale_quant(bits(x.cpu()), ti, ei, sb, None, n)
+            assert np.array_equal(out[:n].view(torch.uint8).cpu().numpy(), q_ref[:n]), f"round {rnd}"
+            assert np.array_equal(sc[:n].cpu().numpy(), s_ref[:n]), f"round {rnd}"
+        else:
+            ref = oracle.gather_scale(bits(x.cpu()), ti, ei, sb, n)
+            assert np.array_equal(bits(out[:n].cpu()), ref[:n]), f"round {rnd}"
